@@ -1,0 +1,226 @@
+"""CPU oracle for paged varlen attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and reference legs may import this package.  The CUDA product path never
+imports it, and it never imports the product path.
+
+The arithmetic lives in ``pa_oracle.c`` (plain C, fp64; its header names the
+passages each function follows).  This module compiles it with gcc and
+marshals numpy arrays into it.  ``paging.py`` holds the page and byte
+arithmetic, ``brute.py`` a pure-Python fp64 restatement for tiny cases.
+
+bf16 tensors are passed as numpy ``uint16`` bit patterns (exact bf16 values);
+outputs are fp64 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "pa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def compile_oracle(src: str, out: str) -> str:
+    """gcc -O2 -fopenmp; -ffp-contract=off keeps every multiply and add a
+    separate IEEE operation, so x86 and Arm hosts give the same bits."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC", "-std=c11",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile pa_oracle.c into liboracle.so next to it when stale."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(SOURCE):
+        compile_oracle(SOURCE, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {a.dtype}")
+    return a
+
+
+def host_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _check(rc: int, what: str):
+    if rc == 1:
+        raise OracleError(f"{what}: invalid argument")
+    if rc == 2:
+        raise OracleError(f"{what}: block id or slot outside the pool")
+    if rc != 0:
+        raise OracleError(f"{what}: status {rc}")
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> exact fp64 values."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+class Oracle:
+    """One loaded copy of the oracle library (the default one, or a test's
+    deliberately mutated copy)."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_round_bf16_array.restype = None
+        lib.oracle_round_bf16_array.argtypes = [P, P, i64]
+        lib.oracle_kv_append.restype = i32
+        lib.oracle_kv_append.argtypes = [P, P, P, i64, P, P, i64, i32, i32, i32]
+        lib.oracle_attention_varlen.restype = i32
+        lib.oracle_attention_varlen.argtypes = [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, f64,
+                                                P, P, P, i32, i32]
+        lib.oracle_attention_sampled.restype = i32
+        lib.oracle_attention_sampled.argtypes = [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, f64,
+                                                 i32, P, P, P, P, P, i32, i32]
+        lib.oracle_merge_lse.restype = i32
+        lib.oracle_merge_lse.argtypes = [P, P, P, P, P, P, i64, i32, i32]
+        self.lib = lib
+        self.path = lib_path
+
+    def round_bf16(self, x) -> np.ndarray:
+        """fp64 -> bf16 bit patterns, round to nearest even."""
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+        out = np.zeros(x.shape, np.uint16)
+        self.lib.oracle_round_bf16_array(_ptr(x), _ptr(out), x.size)
+        return out
+
+    def kv_append(self, k_new, v_new, slot_mapping, k_cache, v_cache):
+        """Scatter new K/V rows into the HND pools, in place.
+
+        k_new, v_new: uint16 [N, Hkv, D]; slot_mapping int64 [N] (negative =
+        skip); k_cache, v_cache: uint16 [num_blocks, Hkv, P, D]."""
+        k_new, v_new = _c(k_new, np.uint16), _c(v_new, np.uint16)
+        slot_mapping = _c(slot_mapping, np.int64)
+        for c in (k_cache, v_cache):
+            if not (c.flags.c_contiguous and c.dtype == np.uint16):
+                raise TypeError("caches must be C-contiguous uint16")
+        N, Hkv, D = k_new.shape
+        nb, _, P, _ = k_cache.shape
+        _check(self.lib.oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache),
+                                         _ptr(v_cache), nb, P, Hkv, D), "kv_append")
+
+    def _common(self, q, k_cache, v_cache, block_tables, seq_lens, qo_indptr):
+        q = _c(q, np.uint16)
+        k_cache, v_cache = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
+        block_tables = _c(block_tables, np.int32)
+        if block_tables.ndim != 2:
+            raise TypeError("block_tables must be 2-D")
+        seq_lens, qo_indptr = _c(seq_lens, np.int32), _c(qo_indptr, np.int32)
+        return q, k_cache, v_cache, block_tables, seq_lens, qo_indptr
+
+    def attention_varlen(self, q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, sm_scale, n_threads=None):
+        """Exact paged varlen attention.
+
+        q uint16 [total_q, Hq, D]; caches uint16 [num_blocks, Hkv, P, D];
+        block_tables int32 [num_reqs, max_blocks]; seq_lens int32 [num_reqs]
+        (KV length after this step's append); qo_indptr int32 [num_reqs + 1].
+        Returns (out fp64 [total_q, Hq, D], lse fp64 [total_q, Hq])."""
+        q, k_cache, v_cache, block_tables, seq_lens, qo_indptr = self._common(
+            q, k_cache, v_cache, block_tables, seq_lens, qo_indptr)
+        total_q, Hq, D = q.shape
+        nb, Hkv, P, _ = k_cache.shape
+        R = seq_lens.shape[0]
+        nt = n_threads or host_threads()
+        max_len = max(int(seq_lens.max()) if R else 1, 1)
+        out = np.zeros((total_q, Hq, D), np.float64)
+        lse = np.zeros((total_q, Hq), np.float64)
+        scratch = np.zeros(nt * max_len, np.float64)
+        _check(self.lib.oracle_attention_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                                                block_tables.shape[1], _ptr(seq_lens), _ptr(qo_indptr), R, Hq, Hkv,
+                                                D, P, float(sm_scale), _ptr(out), _ptr(lse), _ptr(scratch), max_len,
+                                                nt), "attention_varlen")
+        return out, lse
+
+    def attention_sampled(self, q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, sm_scale, sample_tok,
+                          sample_head, n_threads=None):
+        """The same definition at a list of (query token, q head) samples.
+        Returns (out fp64 [n, D], lse fp64 [n])."""
+        q, k_cache, v_cache, block_tables, seq_lens, qo_indptr = self._common(
+            q, k_cache, v_cache, block_tables, seq_lens, qo_indptr)
+        st, sh = _c(sample_tok, np.int32), _c(sample_head, np.int32)
+        total_q, Hq, D = q.shape
+        nb, Hkv, P, _ = k_cache.shape
+        R = seq_lens.shape[0]
+        nt = n_threads or host_threads()
+        max_len = max(int(seq_lens.max()) if R else 1, 1)
+        n = st.shape[0]
+        out = np.zeros((n, D), np.float64)
+        lse = np.zeros((n,), np.float64)
+        scratch = np.zeros(nt * max_len, np.float64)
+        _check(self.lib.oracle_attention_sampled(_ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                                                 block_tables.shape[1], _ptr(seq_lens), _ptr(qo_indptr), R, Hq, Hkv,
+                                                 D, P, float(sm_scale), n, _ptr(st), _ptr(sh), _ptr(out), _ptr(lse),
+                                                 _ptr(scratch), max_len, nt), "attention_sampled")
+        return out, lse
+
+    def merge_lse(self, o_a, lse_a, o_b, lse_b):
+        """LSE merge of two partial attentions.  o_* uint16 [rows, H, D]
+        (bf16 bits), lse_* [rows, H].  Returns (o fp64, lse fp64)."""
+        o_a, o_b = _c(o_a, np.uint16), _c(o_b, np.uint16)
+        lse_a = np.ascontiguousarray(np.asarray(lse_a, np.float64))
+        lse_b = np.ascontiguousarray(np.asarray(lse_b, np.float64))
+        rows, H, D = o_a.shape
+        o = np.zeros((rows, H, D), np.float64)
+        lse = np.zeros((rows, H), np.float64)
+        _check(self.lib.oracle_merge_lse(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o), _ptr(lse), rows,
+                                         H, D), "merge_lse")
+        return o, lse
+
+
+_default = None
+_lock = threading.Lock()
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def round_bf16(x):
+    return default().round_bf16(x)
+
+
+def kv_append(*a, **kw):
+    return default().kv_append(*a, **kw)
+
+
+def attention_varlen(*a, **kw):
+    return default().attention_varlen(*a, **kw)
+
+
+def attention_sampled(*a, **kw):
+    return default().attention_sampled(*a, **kw)
+
+
+def merge_lse(*a, **kw):
+    return default().merge_lse(*a, **kw)

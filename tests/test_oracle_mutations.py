@@ -1,0 +1,53 @@
+"""The pins have teeth: each plausible mistake, planted in a copy of the
+oracle's C source on the CPU, makes at least one pin fail.
+
+Each mutant is compiled into a temporary directory and its pins are run in a
+child process, so a mutant that misbehaves cannot take the test run down.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "causal_off_by_one": ("int n_keys = pos + 1;", "int n_keys = pos > 0 ? pos : 1;"),
+    "top_left_causal": ("int pos = seq_len - qo_len + j;", "int pos = j;"),
+    "gqa_interleaved": ("int kvh = h / G;", "int kvh = h % a->Hkv;"),
+    "scale_dropped": ("s[t] = a->sm_scale * dot;", "s[t] = dot;"),
+    "softmax_sign": ("double w = exp(s[t] - m);", "double w = exp(m - s[t]);"),
+    "values_from_keys": ("o[d] += w * bf16_to_double(a->v_cache[", "o[d] += w * bf16_to_double(a->k_cache["),
+    "page_index_mod": ("int64_t block = table[t / a->p];\n    if", "int64_t block = table[(t / a->p) % 2];\n    if"),
+    "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "nhd_layout": ("return (((size_t)block * (size_t)Hkv + (size_t)kvh) * (size_t)p + (size_t)off) * (size_t)D",
+                   "return (((size_t)block * (size_t)p + (size_t)off) * (size_t)Hkv + (size_t)kvh) * (size_t)D"),
+    "append_offset": ("int off = (int)(slot % block_size);", "int off = (int)((slot + 1) % block_size);"),
+    "merge_weight_sign": ("double wa = exp(la - M), wb = exp(lb - M);", "double wa = exp(M - la), wb = exp(lb - M);"),
+    "merge_lse_dropped": ("lse_out[i] = M + log(wa + wb);", "lse_out[i] = M;"),
+    "normalise_dropped": ("for (int d = 0; d < a->D; ++d) o[d] /= l;", ""),
+    "round_truncates": ("double r = ldexp(rint(ldexp(m, 8)), e - 8);", "double r = ldexp(trunc(ldexp(m, 8)), e - 8);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutant_src = tmp_path / "mutant.c"
+    mutant_src.write_text(src.replace(old, new))
+    lib = oracle.compile_oracle(str(mutant_src), str(tmp_path / "libmutant.so"))
+    res = subprocess.run([sys.executable, "-m", "tests.oracle_pins", lib], cwd=ROOT, capture_output=True, text=True,
+                         timeout=300)
+    assert res.returncode != 0, f"no pin caught mutant {name}:\n{res.stdout}\n{res.stderr}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    lib = oracle.compile_oracle(oracle.SOURCE, str(tmp_path / "libcopy.so"))
+    res = subprocess.run([sys.executable, "-m", "tests.oracle_pins", lib], cwd=ROOT, capture_output=True, text=True,
+                         timeout=300)
+    assert res.returncode == 0, res.stdout + res.stderr
