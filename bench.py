@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Benchmark of the paged varlen attention hot path on GB300.
+
+One step = pa_kv_append of the step's new tokens + pa_attention_varlen over
+one layer of a continuous batch, both through the C ABI (libpa).  Default
+workload: the short-dialogue decode step -- 64 decode rows with contexts
+uniform in [2048, 2303], 16-token pages placed at random in a 10,922-block
+pool, 32 q heads / 8 kv heads, head_dim 128, bf16, N(0,1) data.
+
+Metric: achieved HBM GB/s of the step's algorithmic bytes (unique KV pages
++ q + out + block table + append), also reported as tokens per layer-step
+per second.  Between timed steps a 256 MiB buffer is written to flush the
+129 MB L2, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+With N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica on its own GPU (the path has no exchange step); value is
+the sum of all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_decode_varlen_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention achieved HBM GB/s (% of GB300 peak); tokens/layer-step/s"
+L2_FLUSH_BYTES = 256 << 20
+WORKLOADS = {
+    "short": "short-dialogue decode step: 64 decode rows, seq_len U[2048,2303], 16-token pages in a 10,922-block "
+             "pool, GQA 32/8 heads, head_dim 128, bf16, 1 layer, kv_append of 64 tokens",
+    "shared": "shared-prefix long-context decode: 16 rows, seq_len U[8192,8447], first 6144 tokens (384 pages) "
+              "shared, 5461-block pool, GQA 32/8, head_dim 128, bf16, 1 layer, kv_append of 16 tokens",
+    "mixed": "mixed chunked-prefill batch: one 512-token chunk at offset 1536 + 63 decode rows seq_len "
+             "U[2048,8192], 24,576-block pool, GQA 32/8, head_dim 128, bf16, 1 layer, kv_append of 575 tokens",
+    "tiny": "tiny decode: 4 decode rows seq_len {17,100,256,513}, 64-block pool, GQA 32/8, head_dim 128, bf16",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "paged_kv_decode_varlen_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        self.gpu_index = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, line in self.rows:
+            if self.t0 is None or not (self.t0 - 0.05 <= t <= (self.t1 or t) + 0.05):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
+                power.append(float(parts[4]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_median": statistics.median(power)}
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_step_time(batch, rows=None):
+    """Wall time of the oracle doing one step (append on a copy of the pool,
+    then attention) over `rows` (default all) of the batch."""
+    import oracle
+    b = batch if rows is None else subset(batch, rows)
+    k, v = b.k_cache, b.v_cache
+    t0 = time.perf_counter()
+    oracle.kv_append(b.k_new, b.v_new, b.slot_mapping, k, v)
+    oracle.attention_varlen(b.q, k, v, b.block_tables, b.seq_lens, b.qo_indptr, b.sm_scale)
+    return time.perf_counter() - t0, b
+
+
+def subset(b, rows):
+    """The sub-batch of the given requests (sharing the same pool arrays)."""
+    rows = np.asarray(rows)
+    qo = np.diff(b.qo_indptr)[rows]
+    ind = np.concatenate([[0], np.cumsum(qo)]).astype(np.int32)
+    toks = np.concatenate([np.arange(b.qo_indptr[r], b.qo_indptr[r + 1]) for r in rows]) if len(rows) else \
+        np.zeros(0, np.int64)
+    return W.Batch(q=b.q[toks], k_cache=b.k_cache, v_cache=b.v_cache, block_tables=b.block_tables[rows],
+                   seq_lens=b.seq_lens[rows], qo_indptr=ind, k_new=b.k_new[toks], v_new=b.v_new[toks],
+                   slot_mapping=b.slot_mapping[toks], sm_scale=b.sm_scale, meta=b.meta)
+
+
+def cpu_baseline(batch, min_seconds=10.0, max_seconds=30.0):
+    import oracle
+    cores = oracle.host_threads()
+    bytes_full = W.step_bytes(batch)["unique"]
+    reps, total = 0, 0.0
+    while total < min_seconds and (reps == 0 or total + total / reps <= max_seconds):
+        t, _ = oracle_step_time(batch)
+        total += t
+        reps += 1
+    value = bytes_full * reps / total / 1e9
+    return {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} full step(s) of the same workload (append + attention, all rows), "
+                      f"{total:.1f} s of CPU time, fp64 C oracle, {cores} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    batch = W.workload_batch(args.workload)
+    n_req = batch.num_reqs
+    # size each step so that warm-up + timed steps take about 90 s
+    t_row, _ = oracle_step_time(batch, rows=[0])
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows_per_step = int(max(1, min(n_req, budget // max(t_row, 1e-6))))
+    cursor = 0
+
+    def step():
+        nonlocal cursor
+        rows = [(cursor + i) % n_req for i in range(rows_per_step)]
+        cursor = (cursor + rows_per_step) % n_req
+        t, sb = oracle_step_time(batch, rows=rows)
+        return t, W.step_bytes(sb)["unique"], sb.total_q
+
+    for _ in range(args.warmup):
+        step()
+    tot_t, tot_b, tot_q = 0.0, 0, 0
+    for _ in range(args.steps):
+        t, nb, nq = step()
+        tot_t += t
+        tot_b += nb
+        tot_q += nq
+    value = tot_b / tot_t / 1e9
+    cores = oracle.host_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload], "l2": "n/a (CPU)"},
+        "tokens_per_layer_step_per_s": round(tot_q / tot_t, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {rows_per_step} of {n_req} requests (rotating), append + "
+                                   f"attention, fp64 C oracle, {cores} threads"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="short")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    from paged_kv_decode_varlen_gb300 import build as pa_build
+    pa_build.build()
+    from paged_kv_decode_varlen_gb300 import binding as B
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    batch = W.workload_batch(args.workload, seed_offset=rank)
+    sb = W.step_bytes(batch)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    host = {
+        "q": bf(batch.q).pin_memory(), "k_new": bf(batch.k_new).pin_memory(), "v_new": bf(batch.v_new).pin_memory(),
+        "slot_mapping": torch.from_numpy(batch.slot_mapping).pin_memory(),
+        "block_tables": torch.from_numpy(batch.block_tables).pin_memory(),
+        "seq_lens": torch.from_numpy(batch.seq_lens).pin_memory(),
+        "qo_indptr": torch.from_numpy(batch.qo_indptr).pin_memory(),
+    }
+    d = {k: v.to(dev) for k, v in host.items()}
+    k_cache = bf(batch.k_cache).to(dev)
+    v_cache = bf(batch.v_cache).to(dev)
+    out = torch.empty_like(d["q"])
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    R, total_q = batch.num_reqs, batch.total_q
+    ws = B.new_workspace(B.pa_attention_workspace_size(R, total_q, 32, 128, int(batch.seq_lens.max())), dev)
+    ws_app = B.new_workspace(B.PA_ERROR_WORD_BYTES, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    seq_h, ind_h = host["seq_lens"], host["qo_indptr"]
+    stream = torch.cuda.current_stream()
+
+    def step(src):
+        B.pa_kv_append(src["k_new"], src["v_new"], src["slot_mapping"], k_cache, v_cache, workspace=ws_app)
+        B.pa_attention_varlen(src["q"], k_cache, v_cache, src["block_tables"], src["seq_lens"], src["qo_indptr"],
+                              batch.sm_scale, seq_lens_host=seq_h, qo_indptr_host=ind_h, out=out, workspace=ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step(d)
+    torch.cuda.synchronize()
+    if B.pa_get_device_error(ws) or B.pa_get_device_error(ws_app):
+        raise RuntimeError("device error word set during warm-up")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    B.pa_trace_enable(True)
+    n0 = B.pa_launch_count()
+    clocks.mark(True)
+    for i in range(args.steps):
+        flush.fill_(1)
+        evs[i][0].record(stream)
+        step(d)
+        evs[i][1].record(stream)
+    barrier()
+    clocks.mark(False)
+    launches = B.pa_launch_count() - n0
+    B.pa_trace_enable(False)
+    trace = B.pa_trace_read(1 << 15)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    clk = clocks.stop()
+
+    # end to end through the C ABI with host buffers: H2D of the step's
+    # inputs from pinned memory, the step, D2H of the output
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size()
+    e2e_steps = min(args.steps, 1000)
+    eevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
+    barrier()
+    for i in range(e2e_steps):
+        flush.fill_(1)
+        eevs[i][0].record(stream)
+        for k_, t in host.items():
+            d[k_].copy_(t, non_blocking=True)
+        step(d)
+        out_host.copy_(out, non_blocking=True)
+        eevs[i][1].record(stream)
+    barrier()
+    e2e_ms = [a.elapsed_time(b) for a, b in eevs]
+    if B.pa_get_device_error(ws) or B.pa_get_device_error(ws_app):
+        raise RuntimeError("device error word set during the timed steps")
+
+    t_step = sum(step_ms) / len(step_ms)
+    t_e2e = sum(e2e_ms) / len(e2e_ms)
+    if world > 1:
+        tt = torch.tensor([t_step, t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_step, t_e2e = float(tt[0]), float(tt[1])
+    bytes_all = sb["unique"] * world
+    value = bytes_all / (t_step * 1e-3) / 1e9
+    e2e_value = bytes_all / (t_e2e * 1e-3) / 1e9
+
+    dec = [ms for k_, ms in trace if k_ == "decode"]
+    peak, peak_kind = load_peaks()
+    dec_ms = sum(dec) / len(dec) if dec else None
+    achieved = sb["decode_kernel"] / (dec_ms * 1e-3) / 1e9 if dec_ms else None
+    kernel_share = {}
+    for k_, ms in trace:
+        kernel_share[k_] = kernel_share.get(k_, 0.0) + ms
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload], "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "bytes_per_step": sb["unique"], "logical_bytes_per_step": sb["logical"],
+                   "query_tokens_per_step": sb["query_tokens"]},
+        "tokens_per_layer_step_per_s": round(sb["query_tokens"] * world / (t_step * 1e-3), 1),
+        "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode", "achieved": round(achieved, 2) if achieved else None,
+                     "peak": peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if
+                     peak_kind == "measured" else "fallback 6.8 TB/s", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4) if achieved else None,
+                     "traffic": profiled_traffic(args.workload),
+                     "algorithmic_bytes_per_launch": sb["decode_kernel"],
+                     "avg_launch_ms": round(dec_ms, 5) if dec_ms else None,
+                     "kernel_time_share": {k_: round(v / sum(kernel_share.values()), 4)
+                                           for k_, v in kernel_share.items()}},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(t_e2e, 5), "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(batch)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,203 @@
+/*
+ * pa.h -- C ABI of libpa: paged varlen attention for GB300 (sm_103a).
+ *
+ * One iteration-level (continuous) batch mixes decode rows (qo_len = 1) and
+ * chunked-prefill rows (qo_len > 1, causal, starting at an offset).  Every
+ * row reads its keys and values through a block table of fixed 16-token
+ * pages; pages holding a shared prefix are referenced by many block tables
+ * and stored once.
+ *
+ * Sources for the semantics (page titles and sections):
+ *   - "Inference optimisation" (AI-infra book ch. 8), §8.1.1: prefill stores
+ *     the keys and values of each layer; decode reads the whole context.
+ *   - same, §8.3.1 and Fig. 8-10: fixed-size blocks, per-request block table
+ *     from logical to physical block, logical order recovered through it.
+ *   - same, §8.3.2 and Fig. 8-13: shared prefix blocks referenced by several
+ *     block tables, stored once.
+ *   - same, §8.2.3 and Fig. 8-8/8-9: a chunk of c new tokens after h old ones;
+ *     new token j (0-based) attends to h + j + 1 keys.
+ *   - "vLLM, SGLang and continuous batching", section "PagedAttention":
+ *     16-token blocks, block table, attention kernel reads K/V through it.
+ *   - "Disaggregated prefill and decode": qo_len / kv_len per request
+ *     (decode sends qo_len = 1), and the HND page layout (head before token
+ *     inside a page, so one head's page is contiguous).
+ *
+ * Conventions shared by every call:
+ *   - All tensors are device memory owned by the caller.  The library never
+ *     allocates device memory; scratch space is the caller's `workspace`.
+ *   - All launches are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  A call that returns PA_OK has only enqueued
+ *     work.
+ *   - Arguments are validated on the host first; on any error nothing is
+ *     launched and the status says why (pa_last_error_message() has detail).
+ *   - bf16 means IEEE bfloat16 (torch.bfloat16).  Row-major, densely packed.
+ *   - KV pool layout (HND): k_cache and v_cache are each
+ *     [num_blocks, num_kv_heads, block_size, head_dim] bf16, so one
+ *     (block, kv head) slab is block_size * head_dim * 2 bytes, contiguous.
+ *     Base pointers must be 16-byte aligned.
+ *   - Supported shapes: head_dim = 128, block_size = 16,
+ *     num_q_heads = 4 * num_kv_heads (GQA groups of 4 consecutive query
+ *     heads per kv head: q head h reads kv head h / 4).  Others give
+ *     PA_ERR_UNSUPPORTED.
+ *   - Kernels never trap.  A block id or slot outside the pool found on the
+ *     device is skipped (its keys are masked out / its write is dropped) and
+ *     recorded in the error word at the start of the workspace; read it with
+ *     pa_get_device_error() after synchronising the stream.
+ *   - Every wait inside a kernel is bounded in time; a wait that gives up
+ *     records PA_ERR_DEVICE_TIMEOUT in the error word and the kernel returns.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,         /* null pointer, bad size, inconsistent metadata */
+  PA_ERR_UNSUPPORTED = 2,         /* shape outside what the kernels implement */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the *_workspace_size() query */
+  PA_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+  PA_ERR_DEVICE_INDEX = 5,        /* (error word) block id or slot outside the pool */
+  PA_ERR_DEVICE_TIMEOUT = 6       /* (error word) a bounded in-kernel wait gave up */
+} pa_status;
+
+#define PA_ABI_VERSION 1
+#define PA_HEAD_DIM 128
+#define PA_BLOCK_SIZE 16
+#define PA_GQA_GROUP 4
+#define PA_ERROR_WORD_BYTES 256   /* the workspace's first bytes hold the device error word */
+#define PA_MAX_SEQ_LEN (1 << 20)  /* longest supported sequence (tokens) */
+
+int32_t pa_abi_version(void);
+const char* pa_status_string(int32_t status);
+/* Detail of the last host-side error on the calling thread ("" if none). */
+const char* pa_last_error_message(void);
+
+/*
+ * pa_kv_append -- write this step's new keys and values into their slots.
+ *   For new token i with slot = slot_mapping[i] >= 0, block = slot / 16 and
+ *   offset = slot % 16, and every kv head h:
+ *     k_cache[block, h, offset, :] = k_new[i, h, :]   (v likewise)
+ *   Bytes are copied exactly.  slot < 0 means "no write" (padding).  Slots
+ *   must be distinct; with duplicates the surviving row is unspecified.
+ * k_new, v_new   [n_tokens, num_kv_heads, head_dim] bf16, 16-byte aligned.
+ * slot_mapping   [n_tokens] int64, device.
+ * k_cache, v_cache  the HND pools, modified in place.
+ * workspace      device, >= PA_ERROR_WORD_BYTES bytes; only the error word is
+ *                used.  A slot >= num_blocks * 16 is skipped and recorded as
+ *                PA_ERR_DEVICE_INDEX.
+ * n_tokens = 0 is valid and launches nothing.
+ */
+pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                       void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                       int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_attention_workspace_size -- bytes of device workspace that
+ * pa_attention_varlen needs for a batch with at most these sizes.  The
+ * workspace holds the error word and the split-KV partial results.
+ */
+size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
+                                   int32_t max_seq_len);
+
+/*
+ * pa_attention_varlen -- causal GQA softmax attention over a paged KV cache
+ * for a varlen batch.
+ *   Request r has qo_len = qo_indptr[r+1] - qo_indptr[r] query tokens, rows
+ *   qo_indptr[r] .. qo_indptr[r+1]-1 of q, and seq_len = seq_lens[r] keys
+ *   (the KV length after this step's append, so 0 <= qo_len <= seq_len).
+ *   Query j of request r sits at position p = seq_len - qo_len + j and, for
+ *   every q head h with kv head g = h / 4:
+ *     s_t  = sm_scale * <q[row, h, :], K_g[t, :]>      for t = 0 .. p
+ *     out[row, h, :] = sum_t exp(s_t - m) V_g[t, :] / sum_t exp(s_t - m)
+ *     lse[row, h]    = m + ln(sum_t exp(s_t - m)),  m = max_t s_t
+ *   where K_g[t, :] = k_cache[block_tables[r, t / 16], g, t % 16, :].
+ *   Decode rows (qo_len = 1) use the split-KV decode kernel; rows with
+ *   qo_len > 1 use the tensor-core prefill kernel; rows with qo_len = 0 are
+ *   skipped.  Arithmetic is fp32 on bf16 data; out is rounded to bf16.
+ * q              [total_q, num_q_heads, head_dim] bf16, 16-byte aligned.
+ * block_tables   [num_reqs, max_blocks_per_req] int32, device.  Entries past
+ *                ceil(seq_len / 16) are never read.
+ * seq_lens       [num_reqs] int32, device.
+ * qo_indptr      [num_reqs + 1] int32, device; qo_indptr[0] = 0, non-decreasing,
+ *                qo_indptr[num_reqs] = total_q.
+ * seq_lens_host, qo_indptr_host  host copies of the same two arrays; the
+ *                launch plan (which rows decode, how many KV splits) is made
+ *                from them on the host.  They must equal the device arrays.
+ * out            [total_q, num_q_heads, head_dim] bf16, 16-byte aligned.
+ * lse            [total_q, num_q_heads] float32 (natural log), or NULL.
+ * workspace      device, >= pa_attention_workspace_size(num_reqs, total_q,
+ *                num_q_heads, head_dim, max over r of seq_lens) bytes,
+ *                256-byte aligned.  Its error word is not cleared by this
+ *                call (see pa_clear_device_error).
+ */
+pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                              const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* seq_lens,
+                              const int32_t* qo_indptr, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
+                              int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, float sm_scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_merge_lse -- combine two partial attentions of the same queries over
+ * disjoint key sets A and B (log-sum-exp identity):
+ *   M = max(lse_a, lse_b), w_a = exp(lse_a - M), w_b = exp(lse_b - M)
+ *   o = (w_a o_a + w_b o_b) / (w_a + w_b),  lse = M + ln(w_a + w_b)
+ *   A part with lse = -inf has weight 0 (its o is ignored); if both are
+ *   -inf, o = 0 and lse = -inf.
+ * o_a, o_b, o_out  [rows, num_heads, head_dim] bf16, 16-byte aligned;
+ *                  o_out may alias o_a or o_b.
+ * lse_a, lse_b     [rows, num_heads] float32.
+ * lse_out          [rows, num_heads] float32 or NULL; must not overlap lse_a
+ *                  or lse_b.
+ * head_dim must be a multiple of 8.
+ */
+pa_status pa_merge_lse(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,
+                       float* lse_out, int64_t rows, int32_t num_heads, int32_t head_dim, pa_stream_t stream);
+
+/*
+ * Error word.  pa_get_device_error copies the word at the start of
+ * `workspace` to the host (synchronous: call it after the stream that used
+ * the workspace has been synchronised) and stores PA_OK or the first
+ * PA_ERR_DEVICE_* recorded.  pa_clear_device_error zeroes it on `stream`.
+ */
+pa_status pa_get_device_error(const void* workspace, int32_t* code_out);
+pa_status pa_clear_device_error(void* workspace, pa_stream_t stream);
+
+/*
+ * Tuning and diagnostics.
+ *   pa_set_decode_splits(n): n > 0 forces n KV splits per decode row (capped
+ *     by the workspace bound), 0 restores the automatic plan.  Process-wide.
+ *   pa_launch_count(): kernels this library has launched in this process.
+ *   pa_trace_enable(1): from now on every launch records a CUDA event before
+ *     and after itself on its stream (at most 16384 launches are kept; the
+ *     events are created by this call, on the current device);
+ *     pa_trace_read() waits for the recorded events, returns per launch the
+ *     kernel kind (pa_kernel_kind) and its duration in milliseconds, and
+ *     clears the trace.  pa_trace_enable(0) stops recording.
+ */
+typedef enum {
+  PA_KERNEL_KV_APPEND = 1,
+  PA_KERNEL_DECODE = 2,
+  PA_KERNEL_COMBINE = 3,
+  PA_KERNEL_PREFILL = 4,
+  PA_KERNEL_MERGE = 5
+} pa_kernel_kind;
+
+pa_status pa_set_decode_splits(int32_t n);
+int64_t pa_launch_count(void);
+pa_status pa_trace_enable(int32_t on);
+pa_status pa_trace_read(int32_t* kinds, float* ms, int32_t capacity, int32_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,446 @@
+// C ABI of libpa: host-side validation, launch planning and diagnostics.
+// The arithmetic is in the kernel files; this file only checks arguments,
+// decides the launch plan from the host copies of the batch metadata and
+// enqueues the kernels on the caller's stream.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "pa.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+std::atomic<int64_t> g_launches{0};
+std::atomic<int32_t> g_forced_splits{0};
+
+pa_status fail(pa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+pa_status ok() {
+  g_msg[0] = '\0';
+  return PA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------------ trace
+constexpr int kTraceCap = 16384;
+struct TraceRec {
+  int32_t kind;
+  cudaEvent_t begin, end;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;       // recorded, not yet read
+std::vector<cudaEvent_t> g_evpool;   // idle events
+
+cudaEvent_t take_event() {
+  if (!g_evpool.empty()) {
+    cudaEvent_t e = g_evpool.back();
+    g_evpool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Enqueue one kernel through `launch`, counting it and, when tracing,
+// bracketing it with events on the same stream.
+template <class F>
+pa_status run_launch(int32_t kind, const char* name, cudaStream_t stream, F&& launch) {
+  cudaEvent_t b = nullptr, e = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (g_trace_on && (int)g_trace.size() < kTraceCap) {
+      b = take_event();
+      e = take_event();
+    }
+  }
+  if (b && e) cudaEventRecord(b, stream);
+  const cudaError_t err = launch();
+  if (b && e) {
+    cudaEventRecord(e, stream);
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace.push_back({kind, b, e});
+  }
+  if (err != cudaSuccess) return fail(PA_ERR_CUDA, "%s: %s", name, cudaGetErrorString(err));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return PA_OK;
+}
+
+// --------------------------------------------------------------- planning
+constexpr int kMinPagesPerSplit = 8;
+constexpr int kDecodeCtasPerSm = 3;
+constexpr int kTargetWaves = 4;
+
+int pages_of(int64_t len) { return (int)((len + pa::kPage - 1) / pa::kPage); }
+
+// Most KV splits a decode row of up to max_seq_len keys may use; the
+// workspace is sized for it.
+int split_cap(int32_t max_seq_len) {
+  const int pages = std::max(1, pages_of(max_seq_len));
+  return std::max(1, std::min(pa::kMaxSplits, (pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit));
+}
+
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+// KV splits per decode row: enough CTAs for ~kTargetWaves waves of
+// kDecodeCtasPerSm CTAs per SM, at least kMinPagesPerSplit pages per split,
+// at most kDecodeMaxPagesPerCta pages per CTA, within the workspace cap.
+int plan_splits(int n_decode, int num_kv_heads, int32_t max_decode_len, int cap) {
+  const int pages = std::max(1, pages_of(max_decode_len));
+  const int min_splits = (pages + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta;
+  int s;
+  const int forced = g_forced_splits.load();
+  if (forced > 0) {
+    s = forced;
+  } else {
+    const int64_t work = (int64_t)std::max(1, n_decode) * num_kv_heads;
+    const int64_t target = (int64_t)sm_count() * kDecodeCtasPerSm * kTargetWaves;
+    s = (int)std::min<int64_t>(pa::kMaxSplits, (target + work - 1) / work);
+    s = std::min(s, (pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit);
+  }
+  s = std::max(s, min_splits);
+  return std::max(1, std::min(s, cap));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WorkspaceLayout {
+  size_t part_o, part_lse, total;
+};
+
+WorkspaceLayout layout(int splits, int32_t total_q, int32_t num_q_heads, int32_t head_dim) {
+  WorkspaceLayout w;
+  w.part_o = PA_ERROR_WORD_BYTES;
+  if (splits <= 1) {
+    w.part_lse = w.part_o;
+    w.total = PA_ERROR_WORD_BYTES;
+    return w;
+  }
+  const size_t rows = (size_t)splits * (size_t)std::max(total_q, 0) * (size_t)std::max(num_q_heads, 0);
+  w.part_lse = w.part_o + align256(rows * (size_t)head_dim * 4);
+  w.total = w.part_lse + align256(rows * 4);
+  return w;
+}
+
+pa_status check_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+    return fail(PA_ERR_INVALID_ARG, "head counts, head_dim and block_size must be positive");
+  if (head_dim != PA_HEAD_DIM) return fail(PA_ERR_UNSUPPORTED, "head_dim %d (only %d)", head_dim, PA_HEAD_DIM);
+  if (block_size != PA_BLOCK_SIZE)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (only %d)", block_size, PA_BLOCK_SIZE);
+  if (num_q_heads != PA_GQA_GROUP * num_kv_heads)
+    return fail(PA_ERR_UNSUPPORTED, "num_q_heads %d != %d x num_kv_heads %d", num_q_heads, PA_GQA_GROUP,
+                num_kv_heads);
+  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads %d > 65535", num_kv_heads);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
+
+const char* pa_status_string(int32_t s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "PA_ERR_WORKSPACE_TOO_SMALL";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE_INDEX: return "PA_ERR_DEVICE_INDEX";
+    case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+const char* pa_last_error_message(void) { return g_msg; }
+
+pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                       void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                       int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (n_tokens < 0) return fail(PA_ERR_INVALID_ARG, "n_tokens %lld < 0", (long long)n_tokens);
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
+  pa_status s = check_shape(PA_GQA_GROUP * num_kv_heads, num_kv_heads, head_dim, block_size);
+  if (s != PA_OK) return s;
+  if (!k_cache || !v_cache || !workspace) return fail(PA_ERR_INVALID_ARG, "null cache or workspace pointer");
+  if (n_tokens > 0 && (!k_new || !v_new || !slot_mapping)) return fail(PA_ERR_INVALID_ARG, "null input pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8) || !aligned(workspace, 4))
+    return fail(PA_ERR_INVALID_ARG, "tensors must be 16-byte aligned (slot_mapping 8, workspace 4)");
+  if (workspace_bytes < PA_ERROR_WORD_BYTES)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %d bytes", workspace_bytes, PA_ERROR_WORD_BYTES);
+  if (n_tokens == 0) return ok();
+  pa::AppendParams p;
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.slot_mapping = slot_mapping;
+  p.n_tokens = n_tokens;
+  p.k_cache = static_cast<uint16_t*>(k_cache);
+  p.v_cache = static_cast<uint16_t*>(v_cache);
+  p.num_blocks = num_blocks;
+  p.num_kv_heads = num_kv_heads;
+  p.err = static_cast<int*>(workspace);
+  s = run_launch(PA_KERNEL_KV_APPEND, "kv_append", stream, [&] { return pa::launch_kv_append(p, stream); });
+  return s == PA_OK ? ok() : s;
+}
+
+size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
+                                   int32_t max_seq_len) {
+  (void)num_reqs;
+  if (total_q < 0 || num_q_heads < 0 || head_dim < 0) return 0;
+  return layout(split_cap(std::max(max_seq_len, 1)), total_q, num_q_heads, head_dim).total;
+}
+
+pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                              const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* seq_lens,
+                              const int32_t* qo_indptr, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
+                              int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, float sm_scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_status s = check_shape(num_q_heads, num_kv_heads, head_dim, block_size);
+  if (s != PA_OK) return s;
+  if (num_reqs < 0 || num_reqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_reqs %d outside [0, 65535]", num_reqs);
+  if (total_q < 0) return fail(PA_ERR_INVALID_ARG, "total_q %d < 0", total_q);
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
+  if (!(fabsf(sm_scale) < INFINITY)) return fail(PA_ERR_INVALID_ARG, "sm_scale must be finite");
+  if (!seq_lens_host || !qo_indptr_host) return fail(PA_ERR_INVALID_ARG, "host metadata pointers are required");
+  if (!k_cache || !v_cache || !workspace || !seq_lens || !qo_indptr || (num_reqs > 0 && !block_tables) ||
+      (total_q > 0 && (!q || !out)))
+    return fail(PA_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || !aligned(lse, 4) || !aligned(block_tables, 4))
+    return fail(PA_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned, workspace 256-byte aligned");
+  if (qo_indptr_host[0] != 0) return fail(PA_ERR_INVALID_ARG, "qo_indptr[0] = %d, must be 0", qo_indptr_host[0]);
+  if (qo_indptr_host[num_reqs] != total_q)
+    return fail(PA_ERR_INVALID_ARG, "qo_indptr[num_reqs] = %d != total_q = %d", qo_indptr_host[num_reqs], total_q);
+
+  // classify rows and collect the plan inputs
+  int n_decode = 0;
+  int32_t max_len = 1, max_decode_len = 1;
+  std::vector<std::pair<int32_t, int32_t>> tiles;  // (kv extent of the tile, item index) for ordering
+  static thread_local pa::PrefillItems items;
+  std::vector<int32_t> item_req, item_q0;
+  for (int r = 0; r < num_reqs; ++r) {
+    const int32_t qo_len = qo_indptr_host[r + 1] - qo_indptr_host[r];
+    const int32_t L = seq_lens_host[r];
+    if (qo_len < 0) return fail(PA_ERR_INVALID_ARG, "qo_indptr decreases at request %d", r);
+    if (L < 0 || L > PA_MAX_SEQ_LEN)
+      return fail(L < 0 ? PA_ERR_INVALID_ARG : PA_ERR_UNSUPPORTED, "seq_lens[%d] = %d outside [0, %d]", r, L,
+                  PA_MAX_SEQ_LEN);
+    if (qo_len > L) return fail(PA_ERR_INVALID_ARG, "request %d: qo_len %d > seq_len %d", r, qo_len, L);
+    if (pages_of(L) > max_blocks_per_req)
+      return fail(PA_ERR_INVALID_ARG, "request %d: %d pages > max_blocks_per_req %d", r, pages_of(L),
+                  max_blocks_per_req);
+    max_len = std::max(max_len, L);
+    if (qo_len == 1) {
+      ++n_decode;
+      max_decode_len = std::max(max_decode_len, L);
+    } else if (qo_len > 1) {
+      for (int32_t j0 = 0; j0 < qo_len; j0 += pa::kPrefillQTile) {
+        tiles.push_back({L - qo_len + std::min(qo_len, j0 + pa::kPrefillQTile), (int32_t)item_req.size()});
+        item_req.push_back(r);
+        item_q0.push_back(j0);
+      }
+    }
+  }
+  const int cap = split_cap(max_len);
+  const int splits = n_decode > 0 ? plan_splits(n_decode, num_kv_heads, max_decode_len, cap) : 1;
+  const WorkspaceLayout wl = layout(splits, total_q, num_q_heads, head_dim);
+  const size_t need = layout(cap, total_q, num_q_heads, head_dim).total;
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+  if (total_q == 0) return ok();
+
+  char* ws = static_cast<char*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  const float scale_log2 = sm_scale * pa::kLog2e;
+
+  if (!tiles.empty()) {
+    // longest key extent first, so the big tiles do not form the tail
+    std::stable_sort(tiles.begin(), tiles.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+    pa::PrefillParams pp;
+    pp.q = static_cast<const uint16_t*>(q);
+    pp.k_cache = static_cast<const uint16_t*>(k_cache);
+    pp.v_cache = static_cast<const uint16_t*>(v_cache);
+    pp.num_blocks = num_blocks;
+    pp.block_tables = block_tables;
+    pp.max_blocks_per_req = max_blocks_per_req;
+    pp.seq_lens = seq_lens;
+    pp.qo_indptr = qo_indptr;
+    pp.num_q_heads = num_q_heads;
+    pp.num_kv_heads = num_kv_heads;
+    pp.scale_log2 = scale_log2;
+    pp.out = static_cast<uint16_t*>(out);
+    pp.lse = lse;
+    pp.err = err;
+    for (size_t base = 0; base < tiles.size(); base += pa::kMaxPrefillItems) {
+      const size_t n = std::min(tiles.size() - base, (size_t)pa::kMaxPrefillItems);
+      items.count = (int32_t)n;
+      for (size_t i = 0; i < n; ++i) {
+        const int32_t idx = tiles[base + i].second;
+        items.req[i] = item_req[idx];
+        items.q_start[i] = item_q0[idx];
+      }
+      s = run_launch(PA_KERNEL_PREFILL, "prefill", stream, [&] { return pa::launch_prefill(pp, items, stream); });
+      if (s != PA_OK) return s;
+    }
+  }
+
+  if (n_decode > 0) {
+    pa::DecodeParams dp;
+    dp.q = static_cast<const uint16_t*>(q);
+    dp.k_cache = static_cast<const uint16_t*>(k_cache);
+    dp.v_cache = static_cast<const uint16_t*>(v_cache);
+    dp.num_blocks = num_blocks;
+    dp.block_tables = block_tables;
+    dp.max_blocks_per_req = max_blocks_per_req;
+    dp.seq_lens = seq_lens;
+    dp.qo_indptr = qo_indptr;
+    dp.num_reqs = num_reqs;
+    dp.num_q_heads = num_q_heads;
+    dp.num_kv_heads = num_kv_heads;
+    dp.num_splits = splits;
+    dp.scale_log2 = scale_log2;
+    dp.out = static_cast<uint16_t*>(out);
+    dp.lse = lse;
+    dp.part_o = reinterpret_cast<float*>(ws + wl.part_o);
+    dp.part_lse = reinterpret_cast<float*>(ws + wl.part_lse);
+    dp.total_q = total_q;
+    dp.err = err;
+    s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, stream); });
+    if (s != PA_OK) return s;
+    if (splits > 1) {
+      s = run_launch(PA_KERNEL_COMBINE, "combine", stream, [&] { return pa::launch_combine(dp, stream); });
+      if (s != PA_OK) return s;
+    }
+  }
+  return ok();
+}
+
+pa_status pa_merge_lse(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,
+                       float* lse_out, int64_t rows, int32_t num_heads, int32_t head_dim, pa_stream_t stream) {
+  if (rows < 0 || num_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0)
+    return fail(PA_ERR_INVALID_ARG, "rows >= 0, num_heads > 0 and head_dim a positive multiple of 8 required");
+  if (rows == 0) return ok();
+  if (!o_a || !lse_a || !o_b || !lse_b || !o_out) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(o_a, 16) || !aligned(o_b, 16) || !aligned(o_out, 16))
+    return fail(PA_ERR_INVALID_ARG, "o tensors must be 16-byte aligned");
+  if (lse_out) {
+    const size_t n = (size_t)rows * num_heads * sizeof(float);
+    auto overlap = [n](const void* a, const void* b) {
+      const char* x = static_cast<const char*>(a);
+      const char* y = static_cast<const char*>(b);
+      return x < y + n && y < x + n;
+    };
+    if (overlap(lse_out, lse_a) || overlap(lse_out, lse_b))
+      return fail(PA_ERR_INVALID_ARG, "lse_out must not overlap lse_a or lse_b");
+  }
+  pa::MergeParams p;
+  p.o_a = static_cast<const uint16_t*>(o_a);
+  p.lse_a = lse_a;
+  p.o_b = static_cast<const uint16_t*>(o_b);
+  p.lse_b = lse_b;
+  p.o_out = static_cast<uint16_t*>(o_out);
+  p.lse_out = lse_out;
+  p.rows = rows;
+  p.num_heads = num_heads;
+  p.head_dim = head_dim;
+  pa_status s = run_launch(PA_KERNEL_MERGE, "merge_lse", stream, [&] { return pa::launch_merge(p, stream); });
+  return s == PA_OK ? ok() : s;
+}
+
+pa_status pa_get_device_error(const void* workspace, int32_t* code_out) {
+  if (!workspace || !code_out) return fail(PA_ERR_INVALID_ARG, "null pointer");
+  int32_t v = 0;
+  const cudaError_t e = cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "reading the error word: %s", cudaGetErrorString(e));
+  *code_out = v;
+  return ok();
+}
+
+pa_status pa_clear_device_error(void* workspace, pa_stream_t stream) {
+  if (!workspace) return fail(PA_ERR_INVALID_ARG, "null workspace");
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "clearing the error word: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+pa_status pa_set_decode_splits(int32_t n) {
+  if (n < 0 || n > pa::kMaxSplits) return fail(PA_ERR_INVALID_ARG, "splits %d outside [0, %d]", n, pa::kMaxSplits);
+  g_forced_splits.store(n);
+  return ok();
+}
+
+int64_t pa_launch_count(void) { return g_launches.load(); }
+
+pa_status pa_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = on != 0;
+  // create the events up front so that recording costs no event creation
+  while (g_trace_on && (int)(g_evpool.size() + 2 * g_trace.size()) < 2 * kTraceCap) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return fail(PA_ERR_CUDA, "creating trace events");
+    g_evpool.push_back(e);
+  }
+  return ok();
+}
+
+pa_status pa_trace_read(int32_t* kinds, float* ms, int32_t capacity, int32_t* count) {
+  if (!count || capacity < 0 || (capacity > 0 && (!kinds || !ms))) return fail(PA_ERR_INVALID_ARG, "bad arguments");
+  std::vector<TraceRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    recs.swap(g_trace);
+  }
+  int32_t n = 0;
+  pa_status st = PA_OK;
+  for (const TraceRec& r : recs) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.end);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.begin, r.end);
+    if (e != cudaSuccess && st == PA_OK) st = fail(PA_ERR_CUDA, "trace event: %s", cudaGetErrorString(e));
+    if (n < capacity) {
+      kinds[n] = r.kind;
+      ms[n] = t;
+    }
+    ++n;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    for (const TraceRec& r : recs) {
+      g_evpool.push_back(r.begin);
+      g_evpool.push_back(r.end);
+    }
+  }
+  *count = std::min(n, capacity);
+  return st == PA_OK ? ok() : st;
+}
+
+}  // extern "C"

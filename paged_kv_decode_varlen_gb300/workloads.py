@@ -39,13 +39,23 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
 
 
+def _to_bf16_bits_fast(x: np.ndarray) -> np.ndarray:
+    """Same rounding as f32_to_bf16_bits (nearest even), via torch when it is
+    importable (several times faster on large arrays)."""
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        return f32_to_bf16_bits(x)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
 def normal_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
     """i.i.d. N(0,1) rounded to bf16, generated in chunks to bound memory."""
     n = int(np.prod(shape))
     out = np.empty(n, np.uint16)
     for s in range(0, n, chunk):
         e = min(n, s + chunk)
-        out[s:e] = f32_to_bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+        out[s:e] = _to_bf16_bits_fast(rng.standard_normal(e - s, dtype=np.float32))
     return out.reshape(shape)
 
 
@@ -118,6 +128,7 @@ def make_batch(seq_lens, qo_lens, *, num_blocks: int, seed: int, num_q_heads: in
         # cached tokens (positions before this step's new ones), page by page;
         # shared pages are written once, by the first request.
         written = set()
+        full, partial = [], []
         for r in range(R):
             old = int(seq_lens[r] - qo_lens[r])
             for i in range(-(-old // P)):
@@ -126,8 +137,15 @@ def make_batch(seq_lens, qo_lens, *, num_blocks: int, seed: int, num_q_heads: in
                     continue
                 written.add(blk)
                 n_tok = min(P, old - i * P)
-                k_cache[blk, :, :n_tok, :] = normal_bf16(rng, (Hkv, n_tok, D))
-                v_cache[blk, :, :n_tok, :] = normal_bf16(rng, (Hkv, n_tok, D))
+                (full if n_tok == P else partial).append((blk, n_tok))
+        ids = np.array([blk for blk, _ in full], np.int64)
+        for s in range(0, len(ids), 4096):   # whole pages, in bounded batches
+            part = ids[s:s + 4096]
+            k_cache[part] = normal_bf16(rng, (len(part), Hkv, P, D))
+            v_cache[part] = normal_bf16(rng, (len(part), Hkv, P, D))
+        for blk, n_tok in partial:
+            k_cache[blk, :, :n_tok, :] = normal_bf16(rng, (Hkv, n_tok, D))
+            v_cache[blk, :, :n_tok, :] = normal_bf16(rng, (Hkv, n_tok, D))
 
     qo_indptr = np.zeros(R + 1, np.int32)
     qo_indptr[1:] = np.cumsum(qo_lens)
@@ -197,3 +215,50 @@ def sweep_point(batch: int, context: int, *, seed: int = SEED0 + 5) -> dict:
     need = shared // 16 + batch * (pages - shared // 16)
     return dict(seq_lens=[context] * batch, qo_lens=[1] * batch, num_blocks=int(need * 1.1) + 1,
                 shared_prefix_tokens=shared, seed=seed)
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting of one step (per layer), for throughput figures.
+#   KV: 2 (K, V) x kv heads x head_dim x 2 B = 4096 B per token per layer
+#   (for 8 kv heads, 128 dims).  Unique bytes count each physical page once
+#   (whole pages of shared prefixes, exact tokens of private tails); logical
+#   bytes count every request's keys.  q and out: total_q x Hq x D x 2 B each.
+#   Block table: 4 B per page read.  Append: k_new + v_new read and written
+#   (4 x Hkv x D x 2 B... i.e. 2 x 4096 B per token) plus the 8-byte slot.
+# Split-KV partial results are implementation overhead and are not counted.
+# ---------------------------------------------------------------------------
+def step_bytes(b: Batch) -> dict:
+    total_q, Hq, D = b.q.shape
+    _, Hkv, P, _ = b.k_cache.shape
+    per_tok = 2 * Hkv * D * 2
+    qo = np.diff(b.qo_indptr)
+    active = qo > 0
+    seq = b.seq_lens.astype(np.int64)
+    logical_kv = int((seq[active] * per_tok).sum())
+    # unique: tokens held by distinct physical pages that active rows read
+    seen = {}
+    for r in np.nonzero(active)[0]:
+        L = int(seq[r])
+        for i in range(-(-L // P)):
+            blk = int(b.block_tables[r, i])
+            seen[blk] = max(seen.get(blk, 0), min(P, L - i * P))
+    unique_kv = sum(seen.values()) * per_tok
+    decode = active & (qo == 1)
+    qo_bytes = 2 * total_q * Hq * D * 2
+    table_bytes = int(sum(4 * (-(-int(L) // P)) for L in seq[active]))
+    meta_bytes = 8 * len(seq) + 4
+    append_bytes = int((b.slot_mapping >= 0).sum()) * (2 * per_tok + 8)
+    dec_seen = {}
+    for r in np.nonzero(decode)[0]:
+        L = int(seq[r])
+        for i in range(-(-L // P)):
+            blk = int(b.block_tables[r, i])
+            dec_seen[blk] = max(dec_seen.get(blk, 0), min(P, L - i * P))
+    decode_kv_unique = sum(dec_seen.values()) * per_tok
+    n_dec = int(decode.sum())
+    decode_kernel = decode_kv_unique + n_dec * Hq * D * 2 + int(
+        sum(4 * (-(-int(L) // P)) for L in seq[decode]))
+    return dict(unique=unique_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
+                logical=logical_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
+                unique_kv=unique_kv, logical_kv=logical_kv, decode_kernel=decode_kernel,
+                query_tokens=int(total_q))

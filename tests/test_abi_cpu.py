@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports what include/pa.h declares, and its
+host-side validation rejects bad arguments before launching anything.
+Runs without a GPU: no call here reaches a kernel."""
+import ctypes
+import subprocess
+
+import pytest
+
+from paged_kv_decode_varlen_gb300 import binding as b
+
+lib = b._lib
+FAKE = ctypes.c_void_p(1 << 20)  # non-null, aligned; never dereferenced on these paths
+
+
+def test_header_symbols_exported():
+    names = b.header_functions()
+    assert len(names) >= 13
+    out = subprocess.run(["nm", "-D", "--defined-only", b.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared in pa.h but not exported: {missing}"
+    for n in names:
+        assert getattr(lib, n) is not None
+
+
+def test_abi_version_and_status_strings():
+    assert b.pa_abi_version() == 1
+    assert b.status_string(0) == "PA_OK"
+    assert b.status_string(5) == "PA_ERR_DEVICE_INDEX"
+    assert b.status_string(99) == "PA_ERR_UNKNOWN"
+
+
+def test_workspace_size_query():
+    small = b.pa_attention_workspace_size(4, 4, 32, 128, 513)
+    big = b.pa_attention_workspace_size(64, 64, 32, 128, 2303)
+    assert small >= b.PA_ERROR_WORD_BYTES and big > small and big % 256 == 0
+    # a single short row needs no partials
+    assert b.pa_attention_workspace_size(1, 1, 32, 128, 16) == b.PA_ERROR_WORD_BYTES
+
+
+def _attn(**kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, nb=64, bt=FAKE, mb=40, sl=FAKE, qi=FAKE, slh=None, qih=None, R=2, tq=2, Hq=32,
+                Hkv=8, D=128, P=16, scale=0.088, out=FAKE, lse=None, ws=FAKE, wsb=1 << 30, stream=None)
+    args.update(kw)
+    slh = (ctypes.c_int32 * 2)(*kw.get("seq", (17, 100)))
+    qih = (ctypes.c_int32 * 3)(*kw.get("ind", (0, 1, 2)))
+    return lib.pa_attention_varlen(args["q"], args["k"], args["v"], args["nb"], args["bt"], args["mb"], args["sl"],
+                                   args["qi"], slh, qih, args["R"], args["tq"], args["Hq"], args["Hkv"], args["D"],
+                                   args["P"], args["scale"], args["out"], args["lse"], args["ws"], args["wsb"],
+                                   args["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), b.PA_ERR_UNSUPPORTED),
+    (dict(P=32), b.PA_ERR_UNSUPPORTED),
+    (dict(Hq=16), b.PA_ERR_UNSUPPORTED),
+    (dict(Hkv=0), b.PA_ERR_INVALID_ARG),
+    (dict(q=None), b.PA_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((1 << 20) + 2)), b.PA_ERR_INVALID_ARG),
+    (dict(ws=ctypes.c_void_p((1 << 20) + 16)), b.PA_ERR_INVALID_ARG),
+    (dict(ind=(0, 1, 3)), b.PA_ERR_INVALID_ARG),          # qo_indptr[R] != total_q
+    (dict(ind=(1, 1, 2)), b.PA_ERR_INVALID_ARG),          # qo_indptr[0] != 0
+    (dict(ind=(0, 2, 1), tq=1), b.PA_ERR_INVALID_ARG),    # decreasing
+    (dict(seq=(0, 100)), b.PA_ERR_INVALID_ARG),           # qo_len 1 > seq_len 0
+    (dict(seq=(17, 1000)), b.PA_ERR_INVALID_ARG),         # 63 pages > max_blocks_per_req 40
+    (dict(seq=(17, (1 << 20) + 1)), b.PA_ERR_UNSUPPORTED),
+    (dict(wsb=1024, seq=(17, 600)), b.PA_ERR_WORKSPACE_TOO_SMALL),
+    (dict(nb=0), b.PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), b.PA_ERR_INVALID_ARG),
+])
+def test_attention_validation(kw, status):
+    assert _attn(**kw) == status
+    assert lib.pa_last_error_message().decode() != ""
+
+
+def test_append_validation():
+    ws = FAKE
+    assert lib.pa_kv_append(FAKE, FAKE, FAKE, -1, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_kv_append(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 16, 8, 64, ws, 256, None) == b.PA_ERR_UNSUPPORTED
+    assert lib.pa_kv_append(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 8, 8, 128, ws, 256, None) == b.PA_ERR_UNSUPPORTED
+    assert lib.pa_kv_append(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 16, 8, 128, ws, 64, None) == \
+        b.PA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.pa_kv_append(None, FAKE, FAKE, 4, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_kv_append(ctypes.c_void_p((1 << 20) + 8), FAKE, FAKE, 4, FAKE, FAKE, 64, 16, 8, 128, ws, 256,
+                            None) == b.PA_ERR_INVALID_ARG
+    # zero tokens: valid, launches nothing
+    n0 = lib.pa_launch_count()
+    assert lib.pa_kv_append(None, None, None, 0, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == b.PA_OK
+    assert lib.pa_launch_count() == n0
+
+
+def test_merge_validation():
+    assert lib.pa_merge_lse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 32, 100, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_merge_lse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, 32, 128, None) == b.PA_ERR_INVALID_ARG
+    # lse_out overlapping lse_a is refused
+    assert lib.pa_merge_lse(FAKE, ctypes.c_void_p(1 << 24), FAKE, ctypes.c_void_p(1 << 25), FAKE,
+                            ctypes.c_void_p((1 << 24) + 8), 4, 32, 128, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_merge_lse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 32, 128, None) == b.PA_OK
+
+
+def test_split_override_bounds():
+    assert lib.pa_set_decode_splits(65) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_decode_splits(-1) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_decode_splits(0) == b.PA_OK
