@@ -9,8 +9,9 @@ pool, 32 q heads / 8 kv heads, head_dim 128, bf16, N(0,1) data.
 
 Metric: achieved HBM GB/s of the step's algorithmic bytes (unique KV pages
 + q + out + block table + append), also reported as tokens per layer-step
-per second.  Between timed steps a 256 MiB buffer is written to flush the
-129 MB L2, outside the timed events.
+per second.  Between timed steps a 256 MiB buffer is read to flush the
+129 MB L2 (a read leaves no dirty lines to write back), outside the timed
+events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -236,6 +237,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="short")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-splits", type=int, default=0, help="force KV splits per decode row (0 = automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -251,6 +253,7 @@ def main():
     pa_build.build()
     from paged_kv_decode_varlen_gb300 import binding as B
 
+    B.pa_set_decode_splits(args.decode_splits)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     if world > 1:
@@ -277,7 +280,11 @@ def main():
     R, total_q = batch.num_reqs, batch.total_q
     ws = B.new_workspace(B.pa_attention_workspace_size(R, total_q, 32, 128, int(batch.seq_lens.max())), dev)
     ws_app = B.new_workspace(B.PA_ERROR_WORD_BYTES, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        torch.sum(flush, dim=0, out=flush_sink)
     seq_h, ind_h = host["seq_lens"], host["qo_indptr"]
     stream = torch.cuda.current_stream()
 
@@ -292,13 +299,17 @@ def main():
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2()
         step(d)
     torch.cuda.synchronize()
     if B.pa_get_device_error(ws) or B.pa_get_device_error(ws_app):
         raise RuntimeError("device error word set during warm-up")
 
-    clocks = ClockSampler(local_rank)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except AttributeError:
+        gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[local_rank]
+    clocks = ClockSampler(gpu_id)
     clocks.start()
     time.sleep(0.3)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -307,7 +318,7 @@ def main():
     n0 = B.pa_launch_count()
     clocks.mark(True)
     for i in range(args.steps):
-        flush.fill_(1)
+        flush_l2()
         evs[i][0].record(stream)
         step(d)
         evs[i][1].record(stream)
@@ -327,7 +338,7 @@ def main():
     eevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     barrier()
     for i in range(e2e_steps):
-        flush.fill_(1)
+        flush_l2()
         eevs[i][0].record(stream)
         for k_, t in host.items():
             d[k_].copy_(t, non_blocking=True)
@@ -367,7 +378,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": f"replicas x{world}",
-                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "l2": "flushed between timed steps (256 MiB read outside the events)",
                    "bytes_per_step": sb["unique"], "logical_bytes_per_step": sb["logical"],
                    "query_tokens_per_step": sb["query_tokens"]},
         "tokens_per_layer_step_per_s": round(sb["query_tokens"] * world / (t_step * 1e-3), 1),

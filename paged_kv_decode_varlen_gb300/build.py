@@ -39,7 +39,20 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
+def extra_flags() -> list:
+    """Extra nvcc flags (tuning -D defines) from PA_NVCC_FLAGS; they are part
+    of the build stamp, so changing them forces a rebuild."""
+    return os.environ.get("PA_NVCC_FLAGS", "").split()
+
+
+def _stamp() -> str:
+    return " ".join(extra_flags())
+
+
 def up_to_date() -> bool:
+    stamp = LIB + ".flags"
+    if not os.path.exists(stamp) or open(stamp).read() != _stamp():
+        return False
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
@@ -52,7 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
-                     "--expt-relaxed-constexpr", "-Xptxas", "-v"]
+                     "--expt-relaxed-constexpr", "-Xptxas", "-v"] + extra_flags()
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
@@ -73,6 +86,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(LIB + ".flags", "w") as f:
+        f.write(_stamp())
     if verbose:
         print(open(os.path.join(BUILD_DIR, "ptxas.txt")).read())
     return LIB

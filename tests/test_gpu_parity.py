@@ -260,6 +260,7 @@ def test_merge_of_split_attention_equals_full():
     pa_merge_lse, equals attention over all L keys."""
     b = W.make_batch([1000] * 4, [1] * 4, num_blocks=300, seed=47)
     d = DevBatch(b)
+    B.pa_kv_append(d.k_new, d.v_new, d.slot_mapping, d.k_cache, d.v_cache)
     full, full_lse = B.pa_attention_varlen(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.qo_indptr,
                                            b.sm_scale, return_lse=True)
     a = 384
