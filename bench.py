@@ -237,7 +237,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="short")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--decode-splits", type=int, default=0, help="force KV splits per decode row (0 = automatic)")
+    ap.add_argument("--decode-ctas", type=int, default=0, help="force the persistent decode grid size (0 = automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -253,7 +253,7 @@ def main():
     pa_build.build()
     from paged_kv_decode_varlen_gb300 import binding as B
 
-    B.pa_set_decode_splits(args.decode_splits)
+    B.pa_set_decode_ctas(args.decode_ctas)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     if world > 1:

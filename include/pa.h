@@ -37,8 +37,8 @@
  *     Base pointers must be 16-byte aligned.
  *   - Supported shapes: head_dim = 128, block_size = 16,
  *     num_q_heads = 4 * num_kv_heads (GQA groups of 4 consecutive query
- *     heads per kv head: q head h reads kv head h / 4).  Others give
- *     PA_ERR_UNSUPPORTED.
+ *     heads per kv head: q head h reads kv head h / 4), num_kv_heads <= 256.
+ *     Others give PA_ERR_UNSUPPORTED.
  *   - Kernels never trap.  A block id or slot outside the pool found on the
  *     device is skipped (its keys are masked out / its write is dropped) and
  *     recorded in the error word at the start of the workspace; read it with
@@ -119,9 +119,15 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t nu
  *     out[row, h, :] = sum_t exp(s_t - m) V_g[t, :] / sum_t exp(s_t - m)
  *     lse[row, h]    = m + ln(sum_t exp(s_t - m)),  m = max_t s_t
  *   where K_g[t, :] = k_cache[block_tables[r, t / 16], g, t % 16, :].
- *   Decode rows (qo_len = 1) use the split-KV decode kernel; rows with
- *   qo_len > 1 use the tensor-core prefill kernel; rows with qo_len = 0 are
- *   skipped.  Arithmetic is fp32 on bf16 data; out is rounded to bf16.
+ *   Decode rows (qo_len = 1) use the persistent split-KV decode kernel: the
+ *   (row, kv head) key ranges are laid end to end and cut into one equal
+ *   segment per CTA, and ranges cut between CTAs are merged by log-sum-exp
+ *   inside the same kernel.  Rows with qo_len > 1 use the tensor-core
+ *   prefill kernel; rows with qo_len = 0 are skipped.  Arithmetic is fp32 on
+ *   bf16 data; out is rounded to bf16.  The launch plan is made on the host
+ *   from seq_lens_host / qo_indptr_host and travels in the kernel
+ *   parameters, so a CUDA graph captured around this call replays the plan
+ *   of the lengths it was captured with.
  * q              [total_q, num_q_heads, head_dim] bf16, 16-byte aligned.
  * block_tables   [num_reqs, max_blocks_per_req] int32, device.  Entries past
  *                ceil(seq_len / 16) are never read.
@@ -135,8 +141,14 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t nu
  * lse            [total_q, num_q_heads] float32 (natural log), or NULL.
  * workspace      device, >= pa_attention_workspace_size(num_reqs, total_q,
  *                num_q_heads, head_dim, max over r of seq_lens) bytes,
- *                256-byte aligned.  Its error word is not cleared by this
- *                call (see pa_clear_device_error).
+ *                256-byte aligned, ZERO-FILLED before its first use.  It
+ *                holds the error word, per-(request, kv head) counters of
+ *                finished key ranges and the partial results of key ranges
+ *                cut between CTAs; every call leaves the counters at zero,
+ *                so a workspace is reused without clearing.  Calls sharing a workspace must not run
+ *                concurrently.  After a PA_ERR_DEVICE_* error, zero it again.
+ *                The error word is not cleared by this call (see
+ *                pa_clear_device_error).
  */
 pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
                               const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* seq_lens,
@@ -173,8 +185,9 @@ pa_status pa_clear_device_error(void* workspace, pa_stream_t stream);
 
 /*
  * Tuning and diagnostics.
- *   pa_set_decode_splits(n): n > 0 forces n KV splits per decode row (capped
- *     by the workspace bound), 0 restores the automatic plan.  Process-wide.
+ *   pa_set_decode_ctas(n): n > 0 asks for a persistent decode grid of n CTAs
+ *     (capped by the plan limits and the workspace bound), 0 restores the
+ *     automatic plan (3 CTAs per SM).  Process-wide.
  *   pa_launch_count(): kernels this library has launched in this process.
  *   pa_trace_enable(1): from now on every launch records a CUDA event before
  *     and after itself on its stream (at most 16384 launches are kept; the
@@ -186,12 +199,12 @@ pa_status pa_clear_device_error(void* workspace, pa_stream_t stream);
 typedef enum {
   PA_KERNEL_KV_APPEND = 1,
   PA_KERNEL_DECODE = 2,
-  PA_KERNEL_COMBINE = 3,
+  PA_KERNEL_COMBINE = 3, /* reserved: the split merge is fused into PA_KERNEL_DECODE */
   PA_KERNEL_PREFILL = 4,
   PA_KERNEL_MERGE = 5
 } pa_kernel_kind;
 
-pa_status pa_set_decode_splits(int32_t n);
+pa_status pa_set_decode_ctas(int32_t n);
 int64_t pa_launch_count(void);
 pa_status pa_trace_enable(int32_t on);
 pa_status pa_trace_read(int32_t* kinds, float* ms, int32_t capacity, int32_t* count);

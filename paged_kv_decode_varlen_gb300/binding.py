@@ -54,7 +54,7 @@ _SIGS = {
     "pa_merge_lse": (_i32, [_P, _P, _P, _P, _P, _P, _i64, _i32, _i32, _P]),
     "pa_get_device_error": (_i32, [_P, ctypes.POINTER(_i32)]),
     "pa_clear_device_error": (_i32, [_P, _P]),
-    "pa_set_decode_splits": (_i32, [_i32]),
+    "pa_set_decode_ctas": (_i32, [_i32]),
     "pa_launch_count": (_i64, []),
     "pa_trace_enable": (_i32, [_i32]),
     "pa_trace_read": (_i32, [ctypes.POINTER(_i32), ctypes.POINTER(_f32), _i32, ctypes.POINTER(_i32)]),
@@ -210,8 +210,8 @@ def pa_clear_device_error(workspace, stream=None):
     _check(_lib.pa_clear_device_error(_ptr(workspace), _stream(stream)))
 
 
-def pa_set_decode_splits(n: int):
-    _check(_lib.pa_set_decode_splits(int(n)))
+def pa_set_decode_ctas(n: int):
+    _check(_lib.pa_set_decode_ctas(int(n)))
 
 
 def pa_launch_count() -> int:

@@ -113,6 +113,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses (and
+// those made visible to it) before its later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // mbarrier arrive without a transaction count (consumer release).
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");

@@ -1,37 +1,46 @@
-// Split-KV flash-decode over a paged KV cache (decode rows, qo_len = 1), and
-// the log-sum-exp combine of the splits.
+// Persistent flash-decode over a paged KV cache (decode rows, qo_len = 1).
 //
 // What is computed: for a decode row, every q head attends to all seq_len
 // keys of its kv head, read through the block table ("Inference
 // optimisation", AI-infra book ch. 8, §8.3.1 / Fig. 8-10; "vLLM, SGLang and
 // continuous batching", section "PagedAttention").  The softmax is computed
-// online in fp32 (log2 domain), and partial results over disjoint key
-// ranges are merged by the log-sum-exp identity.
+// online in fp32 (log2 domain); partial results over disjoint key ranges
+// are merged by the log-sum-exp identity.
 //
 // Design for GB300 (HBM-bound; 2 FMA per byte of K/V for the 4-head group):
-//   * grid = (split, kv head, request); one CTA streams the pages of one
-//     (request, kv head) key range.  Each page's K slab and V slab (4 KiB
-//     each, contiguous in the HND pool) are fetched by the TMA engine with
-//     two 1-D bulk copies into an 8-deep shared-memory ring guarded by
-//     mbarriers, so 64 KiB per CTA (3 CTAs per SM) are in flight.
-//   * The 4 q heads of the GQA group share every K/V element read: each
-//     K/V byte is read from HBM once per kv head.
+//   * Work stream.  For each kv head the decode rows' pages are laid end to
+//     end as one stream, cut into equal contiguous segments; CTA b takes kv
+//     head b % Hkv and segment b / Hkv, with one CTA per resident slot (3 per
+//     SM).  A CTA streams its segment through one TMA ring without
+//     restarting at row boundaries, so there is no tail of short CTAs and no
+//     per-CTA start-up latency beyond the first page.  The Hkv CTAs of a
+//     segment read the Hkv head slabs of the same blocks (one contiguous
+//     32 KiB block for 8 kv heads) at the same time.
+//   * Each page's K slab and V slab (4 KiB each, contiguous in the HND pool)
+//     are fetched by two 1-D bulk copies into an 8-deep shared-memory ring
+//     guarded by mbarriers.  The 4 q heads of the GQA group share every K/V
+//     element read.
 //   * 128 threads = 16 token slots x 8 dim chunks.  Thread (t, c) owns dims
-//     [8c, 8c+8) and [64+8c, 64+8c+8) of token t of each page, so every
-//     shared-memory read is a conflict-free 16-byte load and a score needs
-//     only a 3-step shuffle reduction over 8 lanes.
-//   * Each token slot keeps its own running max / sum / accumulator (an
-//     online softmax per slot); the 16 slots are merged once at the end.
-//   * Products and sums use packed fp32x2 FMA (two lanes per instruction).
-//     The 8-lane score reduction is transposed (each shuffle step halves the
-//     values a lane keeps), so each lane ends with one head's score, takes
-//     one exp2, and broadcasts its weight.  The running max is only re-based
-//     when it grows by more than 2^8, so the rescale branch is rarely taken.
-//   * No CTA-wide barrier in the page loop: each warp releases a stage on an
-//     "empty" mbarrier and thread 0 refills it one page later.  (An L2
-//     prefetch of the pages beyond the ring is available at compile time,
-//     PA_DECODE_L2_AHEAD; measured on GB300 it lowers throughput, so it is
-//     off.)
+//     [8c, 8c+8) and [64+8c, 64+8c+8) of token t of a page (conflict-free
+//     16-byte shared loads).  Two pages per loop iteration.  Scores use
+//     packed fp32x2 FMA on head pairs: q is held as (head 0, head 1) and
+//     (head 2, head 3) pairs per dim and each k element is used in both
+//     lanes, so the products come out as (h0, h1), (h2, h3) score pairs with
+//     no final lane sum.  A transposed 8-lane reduction then leaves each
+//     lane one complete (token, head) score, one exp2 per lane, weights
+//     broadcast back by shuffles.  The running max is re-based only when it
+//     grows by more than 2^8.
+//   * No CTA-wide barrier and no producer thread: each warp counts itself
+//     out of a stage (a shared-memory atomic) when it has read it, and the
+//     last of the 4 warps issues that stage's next page at once, so the
+//     ring stays 8 pages deep and the TMA issue work is spread over warps.
+//   * Item end: the 16 token slots are merged (a transposed shuffle
+//     reduction inside each warp, then across the 4 warps through an 8 KiB
+//     per-CTA scratch in the workspace, which stays in L2; shared memory is
+//     all ring).  An item that lies inside one segment is written out at once;
+//     an item cut by segment boundaries leaves one partial per CTA in the
+//     workspace, and the last of those CTAs to finish (a counter it resets)
+//     merges them into out / lse.
 #include <math.h>
 
 #include "common.cuh"
@@ -42,26 +51,33 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 8;      // pages in the shared-memory ring
-#ifndef PA_DECODE_L2_AHEAD
-#define PA_DECODE_L2_AHEAD 0
-#endif
-constexpr int kL2Ahead = PA_DECODE_L2_AHEAD;  // pages prefetched into L2 beyond the ring (0 = none)
+constexpr int kStages = 8;  // pages in the shared-memory ring (a power of two)
 // Rescale the running sums only when the running max grows by more than
 // 2^kRescaleSlack; until then exp2(s - m) stays below 2^kRescaleSlack.
 constexpr float kRescaleSlack = 8.f;
 
+struct Item {        // one request's pages within this CTA's segment
+  int32_t q_start;  // first page of the item in this segment
+  int32_t n;        // pages of the item in this segment
+  int32_t p0;       // row page index of the item's first page in this segment
+  int32_t r;        // request
+  int32_t L;        // seq_len of the request
+  int32_t pad;
+};
+
 struct __align__(128) DecodeSmem {
-  uint8_t k[kStages][kSlabBytes];  // reused as the slot-merge buffer (32 KiB) after the loop
+  uint8_t k[kStages][kSlabBytes];
   uint8_t v[kStages][kSlabBytes];
   uint64_t full[kStages];   // TMA landed
-  uint64_t empty[kStages];  // all warps done reading
+  int readers[kStages];     // warps done reading the stage's current page
   int32_t ids[kDecodeMaxPagesPerCta];
-  float red_m[kPage][kGroup];
-  float red_l[kPage][kGroup];
+  Item items[kDecodeMaxItemsPerCta];
+  int n_items;
+  int n_cov;                 // pages covered by the items (exactly these are issued)
+  int stage_page[kStages];   // last page issued into each stage (-1: none)
   int abort_flag;
+  int is_last;
 };
-static_assert(kStages * kSlabBytes >= kPage * kGroup * kHeadDim * 4, "merge buffer must fit in the K ring");
 
 // 8 packed bf16 pairs (two 16-byte loads) -> 8 float2
 __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float2* f) {
@@ -69,328 +85,481 @@ __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float2*
   f[4] = bf16x2_to_f2(b.x); f[5] = bf16x2_to_f2(b.y); f[6] = bf16x2_to_f2(b.z); f[7] = bf16x2_to_f2(b.w);
 }
 
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const DecodeParams p) {
+// 8 packed bf16 pairs -> 16 scalars (element order kept)
+__device__ __forceinline__ void unpack16s(const uint4& a, const uint4& b, float* f) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf16lo(w[i]);
+    f[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+// Partial scores of one token over this thread's 16 dims as head pairs
+// (h0, h1) and (h2, h3): qp[h][i] = (q[2h][dim i], q[2h+1][dim i]).
+__device__ __forceinline__ void qk16(const float2 (&qp)[2][16], const uint4& ka, const uint4& kb, float2& s01,
+                                     float2& s23) {
+  float kf[16];
+  unpack16s(ka, kb, kf);
+  float2 a0 = __fmul2_rn(qp[0][0], make_float2(kf[0], kf[0]));
+  float2 a1 = __fmul2_rn(qp[0][1], make_float2(kf[1], kf[1]));
+  float2 c0 = __fmul2_rn(qp[1][0], make_float2(kf[0], kf[0]));
+  float2 c1 = __fmul2_rn(qp[1][1], make_float2(kf[1], kf[1]));
+#pragma unroll
+  for (int i = 2; i < 16; i += 2) {
+    a0 = __ffma2_rn(qp[0][i], make_float2(kf[i], kf[i]), a0);
+    a1 = __ffma2_rn(qp[0][i + 1], make_float2(kf[i + 1], kf[i + 1]), a1);
+    c0 = __ffma2_rn(qp[1][i], make_float2(kf[i], kf[i]), c0);
+    c1 = __ffma2_rn(qp[1][i + 1], make_float2(kf[i + 1], kf[i + 1]), c1);
+  }
+  s01 = __fadd2_rn(a0, a1);
+  s23 = __fadd2_rn(c0, c1);
+}
+
+__device__ __forceinline__ void pv16(float2 (&acc)[kGroup][8], const float (&pg)[kGroup], const uint4& va,
+                                     const uint4& vb) {
+  float2 v2[8];
+  unpack16(va, vb, v2);
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    const float2 p2 = make_float2(pg[g], pg[g]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[g][j] = __ffma2_rn(p2, v2[j], acc[g][j]);
+  }
+}
+
+__device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
+  return make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
+}
+
+__device__ __forceinline__ void bar_all() { __syncthreads(); }
+
+__global__ void __launch_bounds__(kThreads, 3)
+    decode_kernel(const DecodeParams p, const __grid_constant__ DecodePlan plan) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
-  const int split = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
+  const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tok = p.qo_indptr[r];
-  if (p.qo_indptr[r + 1] - tok != 1) return;  // not a decode row
-  const int L = p.seq_lens[r];
-  const int n_pages = (L + kPage - 1) / kPage;
-  const int per = (n_pages + p.num_splits - 1) / p.num_splits;
-  const int pg0 = min(n_pages, split * per);
-  const int npg = min(n_pages, pg0 + per) - pg0;
+  const int Hkv = p.num_kv_heads;
+  const int kvh = b % Hkv, sidx = b / Hkv;
+  const int S0 = sidx * plan.seg;
+  const int npg = min(plan.total, S0 + plan.seg) - S0;
+  if (npg <= 0) return;
+  const int n_items_all = plan.n_rows;
 
-  const int ts = tid >> 3;  // token slot within a page
-  const int c = tid & 7;    // dim chunk: dims [8c, 8c+8) and [64+8c, 64+8c+8)
-  // After the transposed reduction below, lane c of a token slot holds the
-  // score of head hd = 2 * bit2(c) + bit1(c); lane base + cg[g] holds head g.
-  const int hd = ((c >> 2) & 1) * 2 + ((c >> 1) & 1);
-  const int slot_base = lane & ~7;
-
-  // Block ids of this split; an id outside the pool is recorded and its
-  // page is masked (and fetched from block 0 so the copy stays in bounds).
-  const int32_t* table = p.block_tables + (size_t)r * p.max_blocks_per_req;
-  for (int i = tid; i < npg; i += kThreads) {
-    int32_t b = table[pg0 + i];
-    if (b < 0 || b >= p.num_blocks) {
-      record_error(p.err, PA_ERR_DEVICE_INDEX);
-      b = -1;
+  // ---- item table of this segment (warp 0), 32 items per round
+  if (warp == 0) {
+    int base_q = 0, n_it = 0;
+    for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
+      const int item = plan.first_row[sidx] + k0 + lane;
+      const bool exists = item < n_items_all;
+      int r = 0, L = 0, size = 0;
+      const int p0 = (k0 + lane == 0) ? plan.first_page[sidx] : 0;
+      if (exists) {
+        r = plan.rows[item];
+        L = p.seq_lens[r];
+        size = max((L + kPage - 1) / kPage - p0, 0);
+      }
+      int incl = size;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int start = base_q + incl - size;
+      const bool in_seg = size > 0 && start < npg;
+      if (in_seg && k0 + lane < kDecodeMaxItemsPerCta) {
+        Item& it = sm.items[k0 + lane];
+        it.q_start = start;
+        it.n = min(size, npg - start);
+        it.p0 = p0;
+        it.r = r;
+        it.L = L;
+      }
+      // the table is the leading run of covered items (a gap can only come
+      // from metadata that differ from the plan)
+      const unsigned covered = __ballot_sync(0xffffffffu, in_seg);
+      const int prefix = (~covered == 0u) ? 32 : (__ffs((int)~covered) - 1);
+      n_it = k0 + prefix;
+      base_q += __shfl_sync(0xffffffffu, incl, 31);
+      if (prefix < 32 || base_q >= npg) break;
     }
-    sm.ids[i] = b;
+    if (lane == 0) {
+      if (base_q < npg) record_error(p.err, PA_ERR_DEVICE_INDEX);  // metadata differ from the plan
+      sm.n_items = min(n_it, kDecodeMaxItemsPerCta);
+    }
   }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kWarps);
+      sm.readers[s] = 0;
+      sm.stage_page[s] = -1;
     }
     sm.abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  const int n_items = sm.n_items;
+  if (n_items == 0) return;  // nothing covered (recorded above); no copy was issued
+
+  // ---- block ids of the segment's pages; an id outside the pool (or a page
+  // past the table) is recorded and masked, and fetched from block 0
+  int ok = 1;
+  for (int q = tid; q < npg; q += kThreads) {
+    int lo = 0, hi = n_items - 1;
+    while (lo < hi) {  // last item with q_start <= q
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.items[mid].q_start <= q) lo = mid; else hi = mid - 1;
+    }
+    int32_t blk = -1;
+    const Item& it = sm.items[lo];
+    const int page = it.p0 + (q - it.q_start);
+    if (q < it.q_start + it.n && page < p.max_blocks_per_req)
+      blk = p.block_tables[(size_t)it.r * p.max_blocks_per_req + page];
+    if (blk < 0 || blk >= p.num_blocks) {
+      record_error(p.err, PA_ERR_DEVICE_INDEX);
+      blk = -1;
+      ok = 0;
+    }
+    sm.ids[q] = blk;
+  }
+  if (tid == 0) {
+    // pages the items cover: exactly these are issued, and every one of
+    // them is consumed, so no copy is in flight when the CTA exits
+    sm.n_cov = sm.items[n_items - 1].q_start + sm.items[n_items - 1].n;
+  }
+  const bool ids_ok = __syncthreads_and(ok) != 0;
+  const int n_cov = sm.n_cov;
 
   const size_t slab_elems = (size_t)kPage * kHeadDim;
-  auto slab_off = [&](int i) {
-    return ((size_t)max(sm.ids[i], 0) * p.num_kv_heads + kvh) * slab_elems;
-  };
-  auto issue = [&](int i) {  // page i of this split -> stage i % kStages; page i + kL2Ahead -> L2
-    const int s = i % kStages;
-    const size_t off = slab_off(i);
+  // segment page i -> stage i % kStages (K and V slabs of kv head kvh)
+  auto issue = [&](int i) {
+    const int s = i & (kStages - 1);
+    const size_t off = ((size_t)max(sm.ids[i], 0) * Hkv + kvh) * slab_elems;
     mbar_arrive_expect_tx(&sm.full[s], 2 * kSlabBytes);
     bulk_g2s(sm.k[s], p.k_cache + off, kSlabBytes, &sm.full[s]);
     bulk_g2s(sm.v[s], p.v_cache + off, kSlabBytes, &sm.full[s]);
-    if (kL2Ahead > 0 && i + kL2Ahead < npg) {
-      const size_t poff = slab_off(i + kL2Ahead);
-      bulk_prefetch_l2(p.k_cache + poff, kSlabBytes);
-      bulk_prefetch_l2(p.v_cache + poff, kSlabBytes);
+    sm.stage_page[s] = i;  // one issuer per stage at a time
+  };
+  if (tid == 0) {
+    const int n0 = min(n_cov, kStages);
+    for (int i = 0; i < n0; ++i) issue(i);
+  }
+  // a warp is done with page i: the last of the 4 warps refills its stage
+  // with page i + kStages
+  auto release = [&](int i) {
+    const int s = i & (kStages - 1);
+    if (atomicAdd(&sm.readers[s], 1) == kWarps - 1) {
+      atomicExch(&sm.readers[s], 0);
+      if (i + kStages < n_cov) {
+        fence_proxy_async_smem();
+        issue(i + kStages);
+      }
     }
   };
-  const bool producer = (tid == 0);
-  int issued = 0;
-  if (producer) {
-    issued = min(npg, kStages);
-    for (int i = 0; i < issued; ++i) issue(i);
-  }
 
-  // q of the 4 heads of this group, scaled into the log2 domain, as float2
-  // pairs matching the K layout this thread reads.
-  float2 q2[kGroup][8];
-  {
-    const uint16_t* qrow = p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
-    const float2 sc = make_float2(p.scale_log2, p.scale_log2);
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-      const uint4 a = *reinterpret_cast<const uint4*>(qrow + g * kHeadDim + 8 * c);
-      const uint4 b = *reinterpret_cast<const uint4*>(qrow + g * kHeadDim + 64 + 8 * c);
-      unpack16(a, b, q2[g]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) q2[g][j] = __fmul2_rn(q2[g][j], sc);
-    }
-  }
-
-  float2 acc[kGroup][8];
-#pragma unroll
-  for (int g = 0; g < kGroup; ++g)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[g][j] = make_float2(0.f, 0.f);
-  // running max and sum of head hd for this token slot (kept by the lanes
-  // that own hd after the reduction)
-  float m_own = -INFINITY, l_own = 0.f;
-
+  const int ts = tid >> 3;  // token slot within a page
+  const int c = tid & 7;    // dim chunk: dims [8c, 8c+8) and [64+8c, 64+8c+8)
+  // After the transposed reduction lane c holds token u = bit0(c) of the
+  // iteration and head hd = 2 bit2(c) + bit1(c).
+  const int hd = ((c >> 2) & 1) * 2 + ((c >> 1) & 1);
+  const int slot_base = lane & ~7;
   bool aborted = false;
-  for (int i = 0; i < npg; ++i) {
-    if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) {
-      aborted = true;
-      break;
-    }
-    const int s = i % kStages;
-    if (!mbar_wait_bounded(&sm.full[s], (uint32_t)(i / kStages) & 1u)) {
-      record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
-      *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
-      aborted = true;
-      break;
-    }
-    const uint8_t* krow = sm.k[s] + ts * (kHeadDim * 2);
-    const uint4 ka = *reinterpret_cast<const uint4*>(krow + 16 * c);
-    const uint4 kb = *reinterpret_cast<const uint4*>(krow + 128 + 16 * c);
-    const bool valid = ((pg0 + i) * kPage + ts < L) && (sm.ids[i] >= 0);
+  int qg = 0;  // segment page counter at the current item's start
 
-    // partial scores over this thread's 16 dims: (h0, h1) and (h2, h3)
-    float2 sp0, sp1;
+  for (int k = 0; k < n_items && !aborted; ++k) {
+    const Item& it = sm.items[k];
+    const int tok = p.qo_indptr[it.r];
+    const int qend = qg + it.n;
+    const int pages_r = (it.L + kPage - 1) / kPage;
+    const int tail_tokens = it.L - (pages_r - 1) * kPage;
+    // segment page at which this token slot is past the row's end (the
+    // row's last page, when this slot is beyond its tokens), else none
+    const int q_inv = (ts < tail_tokens) ? -1 : qg + (pages_r - 1 - it.p0);
+
+    // q of the 4 heads of this group, scaled into the log2 domain, as head
+    // pairs (h0, h1), (h2, h3) per dim of this thread
+    float2 qp[2][16];
     {
-      float2 k2[8];
-      unpack16(ka, kb, k2);
-      float2 a0 = __fmul2_rn(q2[0][0], k2[0]), a1 = __fmul2_rn(q2[0][1], k2[1]);
-      float2 b0 = __fmul2_rn(q2[1][0], k2[0]), b1 = __fmul2_rn(q2[1][1], k2[1]);
-      float2 c0 = __fmul2_rn(q2[2][0], k2[0]), c1 = __fmul2_rn(q2[2][1], k2[1]);
-      float2 d0 = __fmul2_rn(q2[3][0], k2[0]), d1 = __fmul2_rn(q2[3][1], k2[1]);
+      const uint16_t* qrow = p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
 #pragma unroll
-      for (int j = 2; j < 8; j += 2) {
-        a0 = __ffma2_rn(q2[0][j], k2[j], a0);
-        a1 = __ffma2_rn(q2[0][j + 1], k2[j + 1], a1);
-        b0 = __ffma2_rn(q2[1][j], k2[j], b0);
-        b1 = __ffma2_rn(q2[1][j + 1], k2[j + 1], b1);
-        c0 = __ffma2_rn(q2[2][j], k2[j], c0);
-        c1 = __ffma2_rn(q2[2][j + 1], k2[j + 1], c1);
-        d0 = __ffma2_rn(q2[3][j], k2[j], d0);
-        d1 = __ffma2_rn(q2[3][j + 1], k2[j + 1], d1);
-      }
-      a0 = __fadd2_rn(a0, a1);
-      b0 = __fadd2_rn(b0, b1);
-      c0 = __fadd2_rn(c0, c1);
-      d0 = __fadd2_rn(d0, d1);
-      sp0 = make_float2(a0.x + a0.y, b0.x + b0.y);
-      sp1 = make_float2(c0.x + c0.y, d0.x + d0.y);
-    }
-    // transposed reduction over the 8 lanes of the slot: each step halves
-    // the values a lane keeps, so lane c ends with the full score of head hd
-    float sc;
-    {
-      const bool b2 = (c >> 2) & 1;
-      const float2 send = b2 ? sp0 : sp1;
-      float2 keep = b2 ? sp1 : sp0;
-      keep = __fadd2_rn(keep, make_float2(__shfl_xor_sync(0xffffffffu, send.x, 4),
-                                          __shfl_xor_sync(0xffffffffu, send.y, 4)));
-      const bool b1 = (c >> 1) & 1;
-      const float snd = b1 ? keep.x : keep.y;
-      sc = (b1 ? keep.y : keep.x) + __shfl_xor_sync(0xffffffffu, snd, 2);
-      sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-    }
-
-    // online softmax of head hd; the rescale (rare) is warp-uniform
-    const float sv = valid ? sc : -INFINITY;
-    const bool grow = sv > m_own + kRescaleSlack;
-    if (__any_sync(0xffffffffu, grow)) {
-      const float corr = grow ? fast_exp2(m_own - sv) : 1.f;  // m_own = -inf -> 0
-      if (grow) m_own = sv;
-      l_own *= corr;
+      for (int hp = 0; hp < 2; ++hp) {
+        float f0[16], f1[16];
+        unpack16s(*reinterpret_cast<const uint4*>(qrow + (2 * hp) * kHeadDim + 8 * c),
+                  *reinterpret_cast<const uint4*>(qrow + (2 * hp) * kHeadDim + 64 + 8 * c), f0);
+        unpack16s(*reinterpret_cast<const uint4*>(qrow + (2 * hp + 1) * kHeadDim + 8 * c),
+                  *reinterpret_cast<const uint4*>(qrow + (2 * hp + 1) * kHeadDim + 64 + 8 * c), f1);
 #pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        const float cg = __shfl_sync(0xffffffffu, corr, slot_base + (g >> 1) * 4 + (g & 1) * 2);
-        const float2 c2 = make_float2(cg, cg);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[g][j] = __fmul2_rn(acc[g][j], c2);
+        for (int i = 0; i < 16; ++i) qp[hp][i] = make_float2(f0[i] * p.scale_log2, f1[i] * p.scale_log2);
       }
     }
-    const float pown = valid ? fast_exp2(sv - m_own) : 0.f;
-    l_own += pown;
+    float2 acc[kGroup][8];
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[g][j] = make_float2(0.f, 0.f);
+    // running max of head hd (the same in lanes c and c ^ 1) and the sum of
+    // this lane's own weights
+    float m_own = -INFINITY, l_own = 0.f;
 
-    // values: acc[g] += p_g * V, p_g broadcast from the lane owning head g
-    // (all lanes shuffle; only valid tokens touch V)
-    float pg[kGroup];
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) pg[g] = __shfl_sync(0xffffffffu, pown, slot_base + (g >> 1) * 4 + (g & 1) * 2);
-    if (valid) {
-      const uint8_t* vrow = sm.v[s] + ts * (kHeadDim * 2);
-      const uint4 va = *reinterpret_cast<const uint4*>(vrow + 16 * c);
-      const uint4 vb = *reinterpret_cast<const uint4*>(vrow + 128 + 16 * c);
-      float2 v2[8];
-      unpack16(va, vb, v2);
-#pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        const float2 p2 = make_float2(pg[g], pg[g]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[g][j] = __ffma2_rn(p2, v2[j], acc[g][j]);
+    for (int qa = qg; qa < qend; qa += 2) {
+      const int qb = qa + 1;
+      const bool has1 = qb < qend;
+      const int sa = qa & (kStages - 1), sb = qb & (kStages - 1);
+      const uint32_t pa = (uint32_t)(qa / kStages) & 1u, pb = (uint32_t)(qb / kStages) & 1u;
+      if (!mbar_wait_bounded(&sm.full[sa], pa) || (has1 && !mbar_wait_bounded(&sm.full[sb], pb))) {
+        record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+        aborted = true;
+        break;
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[s]);  // this warp is done with stage s
-
-    // producer: refill the stage consumed one page ago once every warp has
-    // released it
-    if (producer && i >= 1) {
-      const int j = i - 1;
-      if (j + kStages < npg) {
-        if (!mbar_wait_bounded(&sm.empty[j % kStages], (uint32_t)(j / kStages) & 1u)) {
-          record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
-          *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
-          aborted = true;
-          break;
+      bool valid0 = qa != q_inv;
+      bool valid1 = has1 && (qb != q_inv);
+      if (!ids_ok) {
+        valid0 = valid0 && sm.ids[qa] >= 0;
+        valid1 = valid1 && sm.ids[min(qb, npg - 1)] >= 0;
+      }
+      // a missing second page reads whatever stage sb holds; its scores are
+      // masked below and its V is not read
+      float2 sA01, sA23, sB01, sB23;
+      {
+        const uint8_t* kr0 = sm.k[sa] + ts * (kHeadDim * 2);
+        const uint8_t* kr1 = sm.k[sb] + ts * (kHeadDim * 2);
+        const uint4 ka0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
+        const uint4 kb0 = *reinterpret_cast<const uint4*>(kr0 + 128 + 16 * c);
+        const uint4 ka1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
+        const uint4 kb1 = *reinterpret_cast<const uint4*>(kr1 + 128 + 16 * c);
+        qk16(qp, ka0, kb0, sA01, sA23);
+        qk16(qp, ka1, kb1, sB01, sB23);
+      }
+      // transposed reduction: 8 values per lane -> 1 complete (token, head)
+      float sc;
+      {
+        const bool b2 = (c >> 2) & 1, b1 = (c >> 1) & 1, b0 = c & 1;
+        float2 kA = b2 ? sA23 : sA01, kB = b2 ? sB23 : sB01;
+        const float2 oA = shfl_xor2(b2 ? sA01 : sA23, 4), oB = shfl_xor2(b2 ? sB01 : sB23, 4);
+        kA = __fadd2_rn(kA, oA);
+        kB = __fadd2_rn(kB, oB);
+        float2 kk = b1 ? make_float2(kA.y, kB.y) : make_float2(kA.x, kB.x);
+        const float2 send = b1 ? make_float2(kA.x, kB.x) : make_float2(kA.y, kB.y);
+        kk = __fadd2_rn(kk, shfl_xor2(send, 2));
+        sc = (b0 ? kk.y : kk.x) + __shfl_xor_sync(0xffffffffu, b0 ? kk.x : kk.y, 1);
+      }
+      const bool my_valid = (c & 1) ? valid1 : valid0;
+      const float sv = my_valid ? sc : -INFINITY;
+      const float mx = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, 1));  // both tokens of head hd
+      const bool grow = mx > m_own + kRescaleSlack;
+      if (__any_sync(0xffffffffu, grow)) {  // running max grew a lot: rescale (rare)
+        const float corr = grow ? fast_exp2(m_own - mx) : 1.f;  // m_own = -inf -> 0
+        if (grow) m_own = mx;
+        l_own *= corr;
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+          const float cg = __shfl_sync(0xffffffffu, corr, slot_base + (g >> 1) * 4 + (g & 1) * 2);
+          const float2 c2 = make_float2(cg, cg);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[g][j] = __fmul2_rn(acc[g][j], c2);
         }
-        issue(j + kStages);
-        issued = j + kStages + 1;
+      }
+      const float pown = my_valid ? fast_exp2(sv - m_own) : 0.f;
+      l_own += pown;
+      float pA[kGroup], pB[kGroup];
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const int src = slot_base + (g >> 1) * 4 + (g & 1) * 2;
+        pA[g] = __shfl_sync(0xffffffffu, pown, src);
+        pB[g] = __shfl_sync(0xffffffffu, pown, src + 1);
+      }
+      if (valid0) {
+        const uint8_t* vr = sm.v[sa] + ts * (kHeadDim * 2);
+        pv16(acc, pA, *reinterpret_cast<const uint4*>(vr + 16 * c),
+             *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
+      }
+      if (valid1) {
+        const uint8_t* vr = sm.v[sb] + ts * (kHeadDim * 2);
+        pv16(acc, pB, *reinterpret_cast<const uint4*>(vr + 16 * c),
+             *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
+      }
+      __syncwarp();
+      if (lane == 0) {  // this warp is done with the iteration's pages
+        release(qa);
+        if (has1) release(qb);
+      }
+      if (((qa - qg) & 15) == 0 && *reinterpret_cast<volatile int*>(&sm.abort_flag)) {
+        aborted = true;
+        break;
       }
     }
+    qg = qend;
+
+    // ---- item end: merge the 16 token slots (all threads take part)
+    bar_all();
+    if (aborted || *reinterpret_cast<volatile int*>(&sm.abort_flag)) {
+      aborted = true;
+      break;
+    }
+    float* scr = p.scratch + (size_t)b * kScratchFloats;  // this CTA's merge scratch (L2)
+    float* scr_m = scr + kWarps * kGroup * kHeadDim;
+    float* scr_l = scr_m + kWarps * kGroup;
+    {
+      const float l_pair = l_own + __shfl_xor_sync(0xffffffffu, l_own, 1);
+      float mh[kGroup], lh[kGroup], Mw[kGroup], Lw[kGroup];
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const int src = slot_base + (g >> 1) * 4 + (g & 1) * 2;
+        mh[g] = __shfl_sync(0xffffffffu, m_own, src);
+        lh[g] = __shfl_sync(0xffffffffu, l_pair, src);
+        float M = fmaxf(mh[g], __shfl_xor_sync(0xffffffffu, mh[g], 8));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+        Mw[g] = M;
+        const float f = (mh[g] == -INFINITY) ? 0.f : fast_exp2(mh[g] - M);
+        const float2 f2 = make_float2(f, f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[g][j] = __fmul2_rn(acc[g][j], f2);
+        float lsum = lh[g] * f;
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
+        Lw[g] = lsum;
+      }
+      // sum over the warp's 4 token slots, transposed: the slot with bits
+      // (s1, s0) ends with head 2 s1 + s0
+      const bool s1 = (lane >> 4) & 1, s0 = (lane >> 3) & 1;
+      float2 h0[8], h1[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // xor 16: keep heads {2 s1, 2 s1 + 1}
+        const float2 keep0 = s1 ? acc[2][j] : acc[0][j], send0 = s1 ? acc[0][j] : acc[2][j];
+        const float2 keep1 = s1 ? acc[3][j] : acc[1][j], send1 = s1 ? acc[1][j] : acc[3][j];
+        h0[j] = __fadd2_rn(keep0, shfl_xor2(send0, 16));
+        h1[j] = __fadd2_rn(keep1, shfl_xor2(send1, 16));
+      }
+      const int h = (s1 ? 2 : 0) + (s0 ? 1 : 0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // xor 8: keep head 2 s1 + s0
+        const float2 keep = s0 ? h1[j] : h0[j], send = s0 ? h0[j] : h1[j];
+        h0[j] = __fadd2_rn(keep, shfl_xor2(send, 8));
+      }
+      float* dst = scr + (warp * kGroup + h) * kHeadDim;
+      *reinterpret_cast<float4*>(dst + 8 * c) = make_float4(h0[0].x, h0[0].y, h0[1].x, h0[1].y);
+      *reinterpret_cast<float4*>(dst + 8 * c + 4) = make_float4(h0[2].x, h0[2].y, h0[3].x, h0[3].y);
+      *reinterpret_cast<float4*>(dst + 64 + 8 * c) = make_float4(h0[4].x, h0[4].y, h0[5].x, h0[5].y);
+      *reinterpret_cast<float4*>(dst + 64 + 8 * c + 4) = make_float4(h0[6].x, h0[6].y, h0[7].x, h0[7].y);
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+          scr_m[warp * kGroup + g] = Mw[g];
+          scr_l[warp * kGroup + g] = Lw[g];
+        }
+      }
+    }
+    bar_all();  // makes the scratch writes of all warps visible to the block (plain loads below)
+    // warp g merges head g across the 4 warps; lane owns dims [4 lane, +4)
+    const int g = warp;
+    const int d0 = lane * 4;
+    float mwv[kWarps];
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      mwv[w] = scr_m[w * kGroup + g];
+      M = fmaxf(M, mwv[w]);
+    }
+    float Ls = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = (mwv[w] == -INFINITY) ? 0.f : fast_exp2(mwv[w] - M);
+        const float4 x = *reinterpret_cast<const float4*>(scr + (w * kGroup + g) * kHeadDim + d0);
+        Ls += scr_l[w * kGroup + g] * f;
+        o.x = fmaf(f, x.x, o.x);
+        o.y = fmaf(f, x.y, o.y);
+        o.z = fmaf(f, x.z, o.z);
+        o.w = fmaf(f, x.w, o.w);
+      }
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    o.x *= inv;
+    o.y *= inv;
+    o.z *= inv;
+    o.w *= inv;
+    const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
+    const int head = kvh * kGroup + g;
+    const size_t orow = (size_t)tok * p.num_q_heads + head;
+    const bool complete = (it.p0 == 0) && (it.n == pages_r);
+    if (complete) {
+      uint2 packed;
+      packed.x = pack_bf16x2(o.x, o.y);
+      packed.y = pack_bf16x2(o.z, o.w);
+      *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + d0) = packed;
+      if (p.lse && lane == 0) p.lse[orow] = lse2 * kLn2;
+      bar_all();  // the merge scratch is free again
+      continue;
+    }
+    // the item is cut by segment boundaries: publish this CTA's partial
+    const int A = S0 + it.q_start - it.p0;  // stream position of the row's page 0
+    const int b0 = A / plan.seg, b1 = (A + pages_r - 1) / plan.seg;  // segments holding the row
+    const int jslot = (k == 0) ? 0 : 1;
+    const size_t slot = ((size_t)b * 2 + jslot) * kGroup + g;
+    *reinterpret_cast<float4*>(p.piece_o + slot * kHeadDim + d0) = o;
+    if (lane == 0) p.piece_lse[slot] = lse2;
+    __threadfence();
+    bar_all();
+    if (tid == 0) {
+      int* cnt = p.counters + (size_t)it.r * Hkv + kvh;
+      const int done = atomicAdd(cnt, 1);
+      sm.is_last = (done == b1 - b0);
+      if (sm.is_last) *cnt = 0;  // every piece has arrived: ready for the next call
+    }
+    bar_all();
+    if (sm.is_last) {
+      __threadfence();
+      float Mx = -INFINITY;
+      for (int bb = b0; bb <= b1; ++bb) {
+        const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+        Mx = fmaxf(Mx, __ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g));
+      }
+      float wsum = 0.f;
+      float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (Mx != -INFINITY) {
+        for (int bb = b0; bb <= b1; ++bb) {
+          const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+          const size_t sl = ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
+          const float ls = __ldcg(p.piece_lse + sl);
+          if (ls == -INFINITY) continue;
+          const float w = fast_exp2(ls - Mx);
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(p.piece_o + sl * kHeadDim + d0));
+          wsum += w;
+          a4.x = fmaf(w, x.x, a4.x);
+          a4.y = fmaf(w, x.y, a4.y);
+          a4.z = fmaf(w, x.z, a4.z);
+          a4.w = fmaf(w, x.w, a4.w);
+        }
+      }
+      const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+      uint2 packed;
+      packed.x = pack_bf16x2(a4.x * winv, a4.y * winv);
+      packed.y = pack_bf16x2(a4.z * winv, a4.w * winv);
+      *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + d0) = packed;
+      if (p.lse && lane == 0) p.lse[orow] = wsum > 0.f ? (Mx + log2f(wsum)) * kLn2 : -INFINITY;
+    }
+    bar_all();  // the merge scratch and is_last are free again
   }
 
-  __syncthreads();  // every thread has left the loop
-  if (aborted || *reinterpret_cast<volatile int*>(&sm.abort_flag)) {
-    // A wait gave up: let the copies already issued land (bounded), then leave.
-    if (producer) {
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        if (!mbar_wait_bounded(&sm.full[j % kStages], (uint32_t)(j / kStages) & 1u)) break;
-    }
-    return;
-  }
-
-  // Merge the 16 token slots: global max per head, then rescaled sums.
-  if ((c & 1) == 0) {
-    sm.red_m[ts][hd] = m_own;
-    sm.red_l[ts][hd] = l_own;
-  }
-  __syncthreads();
-  float* red = reinterpret_cast<float*>(&sm.k[0][0]);  // [16 slots][4 heads][128 dims]
-#pragma unroll
-  for (int g = 0; g < kGroup; ++g) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kPage; ++j) mx = fmaxf(mx, sm.red_m[j][g]);
-    const float mslot = sm.red_m[ts][g];
-    const float f = (mslot == -INFINITY) ? 0.f : fast_exp2(mslot - mx);
-    float* dst = red + (ts * kGroup + g) * kHeadDim;
-#pragma unroll
-    for (int j = 0; j < 4; j += 2) {
-      *reinterpret_cast<float4*>(dst + 8 * c + 2 * j) =
-          make_float4(acc[g][j].x * f, acc[g][j].y * f, acc[g][j + 1].x * f, acc[g][j + 1].y * f);
-      *reinterpret_cast<float4*>(dst + 64 + 8 * c + 2 * j) =
-          make_float4(acc[g][4 + j].x * f, acc[g][4 + j].y * f, acc[g][5 + j].x * f, acc[g][5 + j].y * f);
+  __syncthreads();  // every thread has left the item loop
+  if (*reinterpret_cast<volatile int*>(&sm.abort_flag) && tid == 0) {
+    // A wait gave up: let the last copy issued into each stage land
+    // (bounded), then leave.
+    for (int s = 0; s < kStages; ++s) {
+      const int j = *reinterpret_cast<volatile int*>(&sm.stage_page[s]);
+      if (j >= 0 && !mbar_wait_bounded(&sm.full[s], (uint32_t)(j / kStages) & 1u)) break;
     }
   }
-  __syncthreads();
-  // warp g finishes head g: lane owns dims [4 lane, 4 lane + 4)
-  const int g = warp;
-  float Mg = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kPage; ++j) Mg = fmaxf(Mg, sm.red_m[j][g]);
-  float Lg = 0.f;
-  if (Mg != -INFINITY) {
-#pragma unroll
-    for (int j = 0; j < kPage; ++j) {
-      const float mj = sm.red_m[j][g];
-      if (mj != -INFINITY) Lg += sm.red_l[j][g] * fast_exp2(mj - Mg);
-    }
-  }
-  const int d0 = lane * 4;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int j = 0; j < kPage; ++j) {
-    const float4 x = *reinterpret_cast<const float4*>(red + (j * kGroup + g) * kHeadDim + d0);
-    o.x += x.x;
-    o.y += x.y;
-    o.z += x.z;
-    o.w += x.w;
-  }
-  const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
-  o.x *= inv;
-  o.y *= inv;
-  o.z *= inv;
-  o.w *= inv;
-  const int head = kvh * kGroup + g;
-  const float lse2 = Lg > 0.f ? Mg + log2f(Lg) : -INFINITY;
-  if (p.num_splits == 1) {
-    uint2 packed;
-    packed.x = pack_bf16x2(o.x, o.y);
-    packed.y = pack_bf16x2(o.z, o.w);
-    *reinterpret_cast<uint2*>(p.out + ((size_t)tok * p.num_q_heads + head) * kHeadDim + d0) = packed;
-    if (p.lse && lane == 0) p.lse[(size_t)tok * p.num_q_heads + head] = lse2 * kLn2;
-  } else {
-    const size_t row = ((size_t)split * p.total_q + tok) * p.num_q_heads + head;
-    *reinterpret_cast<float4*>(p.part_o + row * kHeadDim + d0) = o;
-    if (lane == 0) p.part_lse[row] = lse2;
-  }
-}
-
-// One CTA per (kv head, request); warp w merges q head 4*kvh + w, each lane
-// four dims.  Weights are 2^(lse_s - max); empty splits (lse = -inf) weigh 0.
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
-  const int kvh = blockIdx.x, r = blockIdx.y;
-  const int tok = p.qo_indptr[r];
-  if (p.qo_indptr[r + 1] - tok != 1) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = kvh * kGroup + warp;
-  const size_t split_stride = (size_t)p.total_q * p.num_q_heads;
-  const size_t row0 = (size_t)tok * p.num_q_heads + head;
-  float M = -INFINITY;
-  for (int s = 0; s < p.num_splits; ++s) M = fmaxf(M, p.part_lse[s * split_stride + row0]);
-  float wsum = 0.f;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int s = 0; s < p.num_splits; ++s) {
-      const float ls = p.part_lse[s * split_stride + row0];
-      if (ls == -INFINITY) continue;
-      const float w = exp2f(ls - M);
-      const float4 x = *reinterpret_cast<const float4*>(p.part_o + (s * split_stride + row0) * kHeadDim + lane * 4);
-      wsum += w;
-      o.x = fmaf(w, x.x, o.x);
-      o.y = fmaf(w, x.y, o.y);
-      o.z = fmaf(w, x.z, o.z);
-      o.w = fmaf(w, x.w, o.w);
-    }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint2 packed;
-  packed.x = pack_bf16x2(o.x * inv, o.y * inv);
-  packed.y = pack_bf16x2(o.z * inv, o.w * inv);
-  *reinterpret_cast<uint2*>(p.out + row0 * kHeadDim + lane * 4) = packed;
-  if (p.lse && lane == 0) p.lse[row0] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 bool g_decode_attr_set[64] = {};
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -399,14 +568,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     g_decode_attr_set[dev] = true;
   }
-  dim3 grid(p.num_splits, p.num_kv_heads, p.num_reqs);
-  decode_kernel<<<grid, kThreads, sizeof(DecodeSmem), stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
-  dim3 grid(p.num_kv_heads, p.num_reqs);
-  combine_kernel<<<grid, 128, 0, stream>>>(p);
+  decode_kernel<<<grid, kThreads, sizeof(DecodeSmem), stream>>>(p, plan);
   return cudaGetLastError();
 }
 

@@ -18,6 +18,23 @@ struct AppendParams {
   int* err;
 };
 
+// Persistent decode launch plan (host-made, passed by value).  For each kv
+// head the decode rows' pages are laid end to end as one stream (row d of
+// the launch, then row d + 1, ...); every stream is cut into n_seg equal
+// segments of seg pages.  CTA b takes kv head b % Hkv and segment b / Hkv,
+// so the Hkv CTAs of a segment read the same blocks at the same time.
+constexpr int kPlanMaxRows = 1024;   // decode rows per launch
+constexpr int kPlanMaxCtas = 1024;   // CTAs per launch
+constexpr int kDecodeMaxItemsPerCta = 64;
+struct DecodePlan {
+  int32_t n_rows;                     // decode rows of this launch
+  int32_t seg;                        // pages per segment
+  int32_t total;                      // pages of one kv head's stream
+  int32_t rows[kPlanMaxRows];         // request index of decode row d
+  int32_t first_row[kPlanMaxCtas];    // row (index d) holding a segment's first page
+  int32_t first_page[kPlanMaxCtas];   // that page's index within its row
+};
+
 struct DecodeParams {
   const uint16_t* q;
   const uint16_t* k_cache;
@@ -27,18 +44,19 @@ struct DecodeParams {
   int32_t max_blocks_per_req;
   const int32_t* seq_lens;
   const int32_t* qo_indptr;
-  int32_t num_reqs;
   int32_t num_q_heads;
   int32_t num_kv_heads;
-  int32_t num_splits;
   float scale_log2;      // sm_scale * log2(e)
   uint16_t* out;         // bf16 [total_q, Hq, D]
   float* lse;            // [total_q, Hq] natural log, or null
-  float* part_o;         // fp32 [num_splits, total_q, Hq, D] (used when num_splits > 1)
-  float* part_lse;       // fp32 [num_splits, total_q, Hq], log2 domain
-  int32_t total_q;
+  float* piece_o;        // fp32 [2 * grid, 4, D]: a CTA's partial of its first / last item
+  float* piece_lse;      // fp32 [2 * grid, 4], log2 domain
+  int* counters;         // [num_reqs, Hkv] CTAs finished per item; zero between calls
+  float* scratch;        // [grid, kScratchFloats]: per-CTA merge scratch
   int* err;
 };
+// per-CTA merge scratch: 4 warps x 4 heads x D sums, then 4 x 4 max and sum
+constexpr int kScratchFloats = 4 * 4 * 128 + 2 * 4 * 4;
 
 // Prefill work items: (request, first query of the tile) pairs, passed by
 // value in the kernel's parameter block.
@@ -80,15 +98,13 @@ struct MergeParams {
 
 // Each launcher enqueues one kernel on `stream` and returns its launch error.
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
-cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
 // Query tile of the prefill kernel (query tokens per CTA).
 constexpr int kPrefillQTile = 16;
-// Decode kernel: pages of block ids a CTA may hold (bounds pages per split).
+// Decode kernel: pages a CTA may hold block ids for (bounds the segment).
 constexpr int kDecodeMaxPagesPerCta = 1024;
-constexpr int kMaxSplits = 64;
 
 }  // namespace pa

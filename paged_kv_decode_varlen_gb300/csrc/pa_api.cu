@@ -20,7 +20,7 @@ namespace {
 
 thread_local char g_msg[512] = "";
 std::atomic<int64_t> g_launches{0};
-std::atomic<int32_t> g_forced_splits{0};
+std::atomic<int32_t> g_forced_ctas{0};
 
 pa_status fail(pa_status s, const char* fmt, ...) {
   va_list ap;
@@ -84,18 +84,11 @@ pa_status run_launch(int32_t kind, const char* name, cudaStream_t stream, F&& la
 }
 
 // --------------------------------------------------------------- planning
-constexpr int kMinPagesPerSplit = 8;
-constexpr int kDecodeCtasPerSm = 3;
-constexpr int kTargetWaves = 4;
+constexpr int kDecodeCtasPerSm = 3;  // resident decode CTAs per SM (shared memory bound)
+constexpr int kSlotCap = 480;        // grid bound used for workspace sizing (>= SMs x 3)
+constexpr int kMinSegPages = 8;      // fewest pages per CTA worth a CTA
 
 int pages_of(int64_t len) { return (int)((len + pa::kPage - 1) / pa::kPage); }
-
-// Most KV splits a decode row of up to max_seq_len keys may use; the
-// workspace is sized for it.
-int split_cap(int32_t max_seq_len) {
-  const int pages = std::max(1, pages_of(max_seq_len));
-  return std::max(1, std::min(pa::kMaxSplits, (pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit));
-}
 
 int sm_count() {
   static int cached[64] = {};
@@ -108,44 +101,89 @@ int sm_count() {
   return n;
 }
 
-// KV splits per decode row: enough CTAs for ~kTargetWaves waves of
-// kDecodeCtasPerSm CTAs per SM, at least kMinPagesPerSplit pages per split,
-// at most kDecodeMaxPagesPerCta pages per CTA, within the workspace cap.
-int plan_splits(int n_decode, int num_kv_heads, int32_t max_decode_len, int cap) {
-  const int pages = std::max(1, pages_of(max_decode_len));
-  const int min_splits = (pages + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta;
-  int s;
-  const int forced = g_forced_splits.load();
-  if (forced > 0) {
-    s = forced;
-  } else {
-    const int64_t work = (int64_t)std::max(1, n_decode) * num_kv_heads;
-    const int64_t target = (int64_t)sm_count() * kDecodeCtasPerSm * kTargetWaves;
-    s = (int)std::min<int64_t>(pa::kMaxSplits, (target + work - 1) / work);
-    s = std::min(s, (pages + kMinPagesPerSplit - 1) / kMinPagesPerSplit);
-  }
-  s = std::max(s, min_splits);
-  return std::max(1, std::min(s, cap));
+// Largest persistent decode grid a call with these sizes may use (the
+// workspace holds two partial slots per CTA).
+int grid_cap(int32_t num_reqs, int32_t num_kv_heads, int32_t max_seq_len) {
+  const int64_t rows = std::min<int64_t>(std::max(num_reqs, 0), pa::kPlanMaxRows);
+  const int64_t items = rows * std::max(num_kv_heads, 1);
+  const int64_t pages = items * std::max(1, pages_of(max_seq_len));
+  int64_t g = std::max<int64_t>(kSlotCap, (pages + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta);
+  g = std::max<int64_t>(g, (items + 31) / 32);
+  return (int)std::min<int64_t>(g, pa::kPlanMaxCtas);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace: [error word | item counters (num_reqs x Hkv int32) |
+// partial o (2 x grid_cap x 4 heads x D fp32) | partial lse (fp32) |
+// per-CTA merge scratch (grid_cap x kScratchFloats fp32)].
 struct WorkspaceLayout {
-  size_t part_o, part_lse, total;
+  size_t counters, piece_o, piece_lse, scratch, total;
 };
 
-WorkspaceLayout layout(int splits, int32_t total_q, int32_t num_q_heads, int32_t head_dim) {
+WorkspaceLayout layout(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim, int32_t max_seq_len) {
   WorkspaceLayout w;
-  w.part_o = PA_ERROR_WORD_BYTES;
-  if (splits <= 1) {
-    w.part_lse = w.part_o;
-    w.total = PA_ERROR_WORD_BYTES;
-    return w;
-  }
-  const size_t rows = (size_t)splits * (size_t)std::max(total_q, 0) * (size_t)std::max(num_q_heads, 0);
-  w.part_lse = w.part_o + align256(rows * (size_t)head_dim * 4);
-  w.total = w.part_lse + align256(rows * 4);
+  const int32_t hkv = std::max(std::max(num_q_heads, 0) / PA_GQA_GROUP, 1);
+  const size_t slots = (size_t)2 * grid_cap(num_reqs, hkv, max_seq_len) * PA_GQA_GROUP;
+  w.counters = PA_ERROR_WORD_BYTES;
+  w.piece_o = w.counters + align256((size_t)std::max(num_reqs, 0) * (size_t)hkv * 4);
+  w.piece_lse = w.piece_o + align256(slots * (size_t)std::max(head_dim, 0) * 4);
+  w.scratch = w.piece_lse + align256(slots * 4);
+  w.total = w.scratch + align256((size_t)grid_cap(num_reqs, hkv, max_seq_len) * pa::kScratchFloats * 4);
   return w;
+}
+
+// Plan one persistent decode launch over decode rows rows[0..n): fills
+// plan, returns the grid size (0 when there is nothing to do, -1 when no
+// valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
+int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, int num_kv_heads, int gcap,
+                pa::DecodePlan& plan) {
+  std::vector<int32_t> pages(n);
+  int64_t total = 0;  // pages of one kv head's stream
+  for (int d = 0; d < n; ++d) {
+    pages[d] = pages_of(seq_lens_host[rows[d]]);
+    total += pages[d];
+  }
+  if (total == 0) return 0;
+  const int seg_cap = std::min(gcap / num_kv_heads, pa::kPlanMaxCtas);  // segments per stream
+  if (seg_cap < 1) return -1;
+  const int forced = g_forced_ctas.load();
+  int64_t nseg = forced > 0 ? (forced + num_kv_heads - 1) / num_kv_heads
+                            : std::min<int64_t>((int64_t)sm_count() * kDecodeCtasPerSm / num_kv_heads,
+                                                (total * num_kv_heads + kMinSegPages - 1) / kMinSegPages /
+                                                    num_kv_heads);
+  nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, seg_cap));
+  int64_t seg = (total + nseg - 1) / nseg;
+  seg = std::max<int64_t>(seg, (total + seg_cap - 1) / seg_cap);
+  seg = std::min<int64_t>(seg, pa::kDecodeMaxPagesPerCta);  // more segments if one would be too long
+  for (;;) {
+    const int ns = (int)((total + seg - 1) / seg);
+    if (ns > seg_cap) return -1;
+    // walk the row stream once: first row / page of every segment and the
+    // most rows any segment touches
+    int64_t d = 0, d_start = 0, max_items = 0;
+    for (int sidx = 0; sidx < ns; ++sidx) {
+      const int64_t S = (int64_t)sidx * seg, E = std::min(total, S + seg);
+      while (d_start + pages[d] <= S) d_start += pages[d++];
+      plan.first_row[sidx] = (int32_t)d;
+      plan.first_page[sidx] = (int32_t)(S - d_start);
+      int64_t d2 = d, st2 = d_start, cnt = 0;
+      while (d2 < n && st2 < E) {
+        ++cnt;
+        st2 += pages[d2++];
+      }
+      max_items = std::max(max_items, cnt);
+    }
+    if (max_items <= pa::kDecodeMaxItemsPerCta) {
+      plan.n_rows = n;
+      plan.seg = (int32_t)seg;
+      plan.total = (int32_t)total;
+      for (int r = 0; r < n; ++r) plan.rows[r] = rows[r];
+      return ns * num_kv_heads;
+    }
+    if (seg == 1) return -1;
+    seg = (seg + 1) / 2;  // shorter segments touch fewer rows
+  }
 }
 
 pa_status check_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
@@ -157,7 +195,7 @@ pa_status check_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_di
   if (num_q_heads != PA_GQA_GROUP * num_kv_heads)
     return fail(PA_ERR_UNSUPPORTED, "num_q_heads %d != %d x num_kv_heads %d", num_q_heads, PA_GQA_GROUP,
                 num_kv_heads);
-  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads %d > 65535", num_kv_heads);
+  if (num_kv_heads > 256) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads %d > 256", num_kv_heads);
   return PA_OK;
 }
 
@@ -213,9 +251,8 @@ pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot
 
 size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
                                    int32_t max_seq_len) {
-  (void)num_reqs;
-  if (total_q < 0 || num_q_heads < 0 || head_dim < 0) return 0;
-  return layout(split_cap(std::max(max_seq_len, 1)), total_q, num_q_heads, head_dim).total;
+  if (num_reqs < 0 || total_q < 0 || num_q_heads < 0 || head_dim < 0) return 0;
+  return layout(num_reqs, num_q_heads, head_dim, std::max(max_seq_len, 1)).total;
 }
 
 pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
@@ -242,8 +279,8 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
     return fail(PA_ERR_INVALID_ARG, "qo_indptr[num_reqs] = %d != total_q = %d", qo_indptr_host[num_reqs], total_q);
 
   // classify rows and collect the plan inputs
-  int n_decode = 0;
-  int32_t max_len = 1, max_decode_len = 1;
+  std::vector<int32_t> decode_rows;
+  int32_t max_len = 1;
   std::vector<std::pair<int32_t, int32_t>> tiles;  // (kv extent of the tile, item index) for ordering
   static thread_local pa::PrefillItems items;
   std::vector<int32_t> item_req, item_q0;
@@ -260,8 +297,7 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
                   max_blocks_per_req);
     max_len = std::max(max_len, L);
     if (qo_len == 1) {
-      ++n_decode;
-      max_decode_len = std::max(max_decode_len, L);
+      decode_rows.push_back(r);
     } else if (qo_len > 1) {
       for (int32_t j0 = 0; j0 < qo_len; j0 += pa::kPrefillQTile) {
         tiles.push_back({L - qo_len + std::min(qo_len, j0 + pa::kPrefillQTile), (int32_t)item_req.size()});
@@ -270,12 +306,9 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
       }
     }
   }
-  const int cap = split_cap(max_len);
-  const int splits = n_decode > 0 ? plan_splits(n_decode, num_kv_heads, max_decode_len, cap) : 1;
-  const WorkspaceLayout wl = layout(splits, total_q, num_q_heads, head_dim);
-  const size_t need = layout(cap, total_q, num_q_heads, head_dim).total;
-  if (workspace_bytes < need)
-    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+  const WorkspaceLayout wl = layout(num_reqs, num_q_heads, head_dim, max_len);
+  if (workspace_bytes < wl.total)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, wl.total);
   if (total_q == 0) return ok();
 
   char* ws = static_cast<char*>(workspace);
@@ -313,7 +346,7 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
     }
   }
 
-  if (n_decode > 0) {
+  if (!decode_rows.empty()) {
     pa::DecodeParams dp;
     dp.q = static_cast<const uint16_t*>(q);
     dp.k_cache = static_cast<const uint16_t*>(k_cache);
@@ -323,21 +356,26 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
     dp.max_blocks_per_req = max_blocks_per_req;
     dp.seq_lens = seq_lens;
     dp.qo_indptr = qo_indptr;
-    dp.num_reqs = num_reqs;
     dp.num_q_heads = num_q_heads;
     dp.num_kv_heads = num_kv_heads;
-    dp.num_splits = splits;
     dp.scale_log2 = scale_log2;
     dp.out = static_cast<uint16_t*>(out);
     dp.lse = lse;
-    dp.part_o = reinterpret_cast<float*>(ws + wl.part_o);
-    dp.part_lse = reinterpret_cast<float*>(ws + wl.part_lse);
-    dp.total_q = total_q;
+    dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
+    dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
+    dp.counters = reinterpret_cast<int*>(ws + wl.counters);
+    dp.scratch = reinterpret_cast<float*>(ws + wl.scratch);
     dp.err = err;
-    s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, stream); });
-    if (s != PA_OK) return s;
-    if (splits > 1) {
-      s = run_launch(PA_KERNEL_COMBINE, "combine", stream, [&] { return pa::launch_combine(dp, stream); });
+    static thread_local pa::DecodePlan plan;
+    const int gcap = grid_cap(num_reqs, num_kv_heads, max_len);
+    // one launch per kPlanMaxRows decode rows (the plan travels as kernel
+    // parameters); launches on one stream run in order and reuse the slots
+    for (size_t d0 = 0; d0 < decode_rows.size(); d0 += pa::kPlanMaxRows) {
+      const int n = (int)std::min(decode_rows.size() - d0, (size_t)pa::kPlanMaxRows);
+      const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, num_kv_heads, gcap, plan);
+      if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
+      if (grid == 0) continue;
+      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, stream); });
       if (s != PA_OK) return s;
     }
   }
@@ -392,9 +430,10 @@ pa_status pa_clear_device_error(void* workspace, pa_stream_t stream) {
   return ok();
 }
 
-pa_status pa_set_decode_splits(int32_t n) {
-  if (n < 0 || n > pa::kMaxSplits) return fail(PA_ERR_INVALID_ARG, "splits %d outside [0, %d]", n, pa::kMaxSplits);
-  g_forced_splits.store(n);
+pa_status pa_set_decode_ctas(int32_t n) {
+  if (n < 0 || n > pa::kPlanMaxCtas)
+    return fail(PA_ERR_INVALID_ARG, "decode grid %d outside [0, %d]", n, pa::kPlanMaxCtas);
+  g_forced_ctas.store(n);
   return ok();
 }
 

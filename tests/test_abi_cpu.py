@@ -33,9 +33,16 @@ def test_abi_version_and_status_strings():
 def test_workspace_size_query():
     small = b.pa_attention_workspace_size(4, 4, 32, 128, 513)
     big = b.pa_attention_workspace_size(64, 64, 32, 128, 2303)
-    assert small >= b.PA_ERROR_WORD_BYTES and big > small and big % 256 == 0
-    # a single short row needs no partials
-    assert b.pa_attention_workspace_size(1, 1, 32, 128, 16) == b.PA_ERROR_WORD_BYTES
+    assert small >= b.PA_ERROR_WORD_BYTES and big >= small and big % 256 == 0 and small % 256 == 0
+    # error word + counters (num_reqs x 8 int32) + two partial slots of 4 heads x 129 fp32 per CTA
+    # for a 480-CTA bound
+    # plus an 8320-byte merge scratch per CTA, for a 480-CTA bound
+    slots = 2 * 480 * 4
+    scratch = 480 * 8320
+    assert b.pa_attention_workspace_size(1, 1, 32, 128, 16) == 256 + 256 + slots * 512 + 15360 + scratch
+    assert b.pa_attention_workspace_size(100, 100, 32, 128, 16) == 256 + 3328 + slots * 512 + 15360 + scratch
+    # very long rows raise the grid bound (1024 pages per CTA at most)
+    assert b.pa_attention_workspace_size(1024, 1024, 32, 128, 1 << 20) > big
 
 
 def _attn(**kw):
@@ -98,7 +105,7 @@ def test_merge_validation():
     assert lib.pa_merge_lse(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 32, 128, None) == b.PA_OK
 
 
-def test_split_override_bounds():
-    assert lib.pa_set_decode_splits(65) == b.PA_ERR_INVALID_ARG
-    assert lib.pa_set_decode_splits(-1) == b.PA_ERR_INVALID_ARG
-    assert lib.pa_set_decode_splits(0) == b.PA_OK
+def test_grid_override_bounds():
+    assert lib.pa_set_decode_ctas(1025) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_decode_ctas(-1) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_decode_ctas(0) == b.PA_OK

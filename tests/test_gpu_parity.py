@@ -22,7 +22,7 @@ if torch.cuda.is_available():
 def _reset_splits():
     yield
     if torch.cuda.is_available():
-        B.pa_set_decode_splits(0)
+        B.pa_set_decode_ctas(0)
 
 
 def run_step(d: DevBatch, return_lse=True):
@@ -95,16 +95,34 @@ def test_sweep_point_parity(batch, context):
     compare(out, ref, lse, ref_lse, what=f"sweep b={batch} L={context}")
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 16, 64])
-def test_forced_splits(splits):
-    """Every split count (including more splits than pages) gives the same
-    attention within tolerance."""
-    b = W.make_batch([2100, 37, 16, 1, 700, 129], [1] * 6, num_blocks=400, seed=20 + splits)
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7, 64, 456, 1024])
+def test_forced_decode_grid(ctas):
+    """Every persistent grid size -- one CTA for all key ranges, ranges cut
+    across many CTAs, more CTAs than pages -- gives the same attention."""
+    b = W.make_batch([2100, 37, 16, 1, 700, 129], [1] * 6, num_blocks=400, seed=20 + ctas)
     d = DevBatch(b)
-    B.pa_set_decode_splits(splits)
+    B.pa_set_decode_ctas(ctas)
     out, lse = run_step(d)
     ref, ref_lse, _, _ = oracle_step(b)
-    compare(out, ref, lse, ref_lse, what=f"splits={splits}")
+    compare(out, ref, lse, ref_lse, what=f"ctas={ctas}")
+
+
+def test_workspace_reused_across_grid_sizes():
+    """The item counters in the workspace return to zero after every call,
+    so one workspace serves consecutive calls with different grid sizes."""
+    b = W.make_batch([1500, 700, 33, 2000], [1] * 4, num_blocks=300, seed=29)
+    d = DevBatch(b)
+    B.pa_kv_append(d.k_new, d.v_new, d.slot_mapping, d.k_cache, d.v_cache)
+    ref, ref_lse, _, _ = oracle_step(b)
+    ws = B.new_workspace(B.pa_attention_workspace_size(4, 4, 32, 128, 2000), "cuda")
+    for splits in (7, 3, 64, 1, 5, 5, 300):
+        B.pa_set_decode_ctas(splits)
+        out, lse = B.pa_attention_varlen(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.qo_indptr,
+                                         b.sm_scale, workspace=ws, return_lse=True)
+        torch.cuda.synchronize()
+        compare(out, ref, lse, ref_lse, what=f"reuse splits={splits}")
+    counters = ws[256:256 + 4 * 8 * 4].view(torch.int32)
+    assert int(counters.abs().sum()) == 0
 
 
 # ----------------------------------------------------------------- edge cases
