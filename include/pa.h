@@ -158,6 +158,39 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
                               void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_attention_varlen_noalloc -- pa_attention_varlen for callers that cannot
+ * allocate device memory.  The pages describe no counterpart of this call;
+ * it exists for callers that cannot obtain a workspace: code running where
+ * cudaMalloc is not allowed or not wanted (inside stream capture, in a
+ * real-time loop, under a host framework that owns all device memory), or a
+ * plugin that is handed only its input and output pointers.
+ *   Same computation, arguments and results as pa_attention_varlen, except
+ *   that there is no workspace argument: the scratch is a fixed array of
+ *   PA_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, present on every
+ *   GPU that loads the library until the process exits.  A batch whose
+ *   pa_attention_workspace_size() exceeds it is rejected with
+ *   PA_ERR_UNSUPPORTED (and a message in pa_last_error_message()).
+ *   No device memory is allocated or freed by this call.
+ * device_error   nullable device int32; if given, receives the call's device
+ *                error word (PA_OK or PA_ERR_DEVICE_*) on `stream`.
+ * Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before capturing `stream` into a graph.
+ * Sharing: every call on a device uses the same array and leaves its contents
+ *   there; each call clears its error word and counters on `stream` first.
+ *   Calls that overlap on the GPU race on the array, so issue them in order
+ *   (e.g. on one stream).
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+pa_status pa_attention_varlen_noalloc(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                                      const int32_t* block_tables, int32_t max_blocks_per_req,
+                                      const int32_t* seq_lens, const int32_t* qo_indptr,
+                                      const int32_t* seq_lens_host, const int32_t* qo_indptr_host, int32_t num_reqs,
+                                      int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, float sm_scale, void* out, float* lse,
+                                      int32_t* device_error, pa_stream_t stream);
+
+/*
  * pa_merge_lse -- combine two partial attentions of the same queries over
  * disjoint key sets A and B (log-sum-exp identity):
  *   M = max(lse_a, lse_b), w_a = exp(lse_a - M), w_b = exp(lse_b - M)

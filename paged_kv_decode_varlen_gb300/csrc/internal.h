@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pa.h"
+
 namespace pa {
 
 struct AppendParams {
@@ -95,6 +97,9 @@ struct MergeParams {
   int32_t num_heads;
   int32_t head_dim;
 };
+
+// Sets the calling thread's pa_last_error_message() text and returns s.
+pa_status set_error(pa_status s, const char* fmt, ...);
 
 // Each launcher enqueues one kernel on `stream` and returns its launch error.
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);

@@ -201,6 +201,14 @@ pa_status check_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_di
 
 }  // namespace
 
+pa_status pa::set_error(pa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
 extern "C" {
 
 int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
