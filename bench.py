@@ -228,6 +228,115 @@ def run_reference(args, rank, world):
     return 0
 
 
+# ------------------------------------------------------------- 36-layer sweep
+def device_batch(spec, device, layers):
+    """One sweep point on the device: block tables, lengths and one K/V pool
+    per layer, filled with seeded N(0,1) bf16 from a CUDA generator (the
+    largest points hold ~40 GB, too much to generate on the host)."""
+    import torch
+    b = W.make_batch(spec["seq_lens"], spec["qo_lens"], num_blocks=spec["num_blocks"], seed=spec["seed"],
+                     shared_prefix_tokens=spec["shared_prefix_tokens"], fill_pool=False)
+    g = torch.Generator(device=device)
+    g.manual_seed(spec["seed"])
+    nb = spec["num_blocks"]
+    pools = []
+    for _ in range(layers):
+        kc = torch.randn((nb, 8, 16, 128), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+        vc = torch.randn((nb, 8, 16, 128), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+        pools.append((kc, vc))
+    return b, pools
+
+
+def attention(B, prefix_pages, q, k_cache, v_cache, tables, seq, ind, scale, seq_h, ind_h, out, ws):
+    """The step's attention call: the shared-prefix entry point when the
+    batch's requests share leading pages, else pa_attention_varlen."""
+    if prefix_pages:
+        B.pa_attention_varlen_shared_prefix(q, k_cache, v_cache, tables, seq, ind, scale, prefix_pages,
+                                            seq_lens_host=seq_h, qo_indptr_host=ind_h, out=out, workspace=ws)
+    else:
+        B.pa_attention_varlen(q, k_cache, v_cache, tables, seq, ind, scale, seq_lens_host=seq_h,
+                              qo_indptr_host=ind_h, out=out, workspace=ws)
+
+
+def call_name(prefix_pages):
+    return (f"pa_attention_varlen_shared_prefix ({prefix_pages} shared pages)" if prefix_pages
+            else "pa_attention_varlen")
+
+
+def run_sweep(args):
+    """Per-layer step time of append + attention for 36 layers captured in one
+    CUDA graph, at each decode batch size and context of the sweep."""
+    import torch
+    from paged_kv_decode_varlen_gb300 import build as pa_build
+    pa_build.build()
+    from paged_kv_decode_varlen_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    layers = args.layers
+    peak, _ = load_peaks()
+    for context in [int(c) for c in args.contexts.split(",")]:
+        for batch in [int(x) for x in args.batches.split(",")]:
+            spec = W.sweep_point(batch, context)
+            b, pools = device_batch(spec, dev, layers)
+            ppages = 0 if args.no_cascade else spec["shared_prefix_tokens"] // 16
+            sb = W.step_bytes(b, ppages)
+
+            def bf(a):
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+            q, k_new, v_new = bf(b.q), bf(b.k_new), bf(b.v_new)
+            tables = torch.from_numpy(b.block_tables).to(dev)
+            seq = torch.from_numpy(b.seq_lens).to(dev)
+            ind = torch.from_numpy(b.qo_indptr).to(dev)
+            slots = torch.from_numpy(b.slot_mapping).to(dev)
+            out = torch.empty_like(q)
+            ws = B.new_workspace(B.pa_shared_prefix_workspace_size(b.num_reqs, b.total_q, 32, 128,
+                                                                   int(b.seq_lens.max()), ppages), dev)
+            ws_app = B.new_workspace(B.PA_ERROR_WORD_BYTES, dev)
+
+            def step():
+                for kc, vc in pools:
+                    B.pa_kv_append(k_new, v_new, slots, kc, vc, workspace=ws_app)
+                    attention(B, ppages, q, kc, vc, tables, seq, ind, b.sm_scale, b.seq_lens, b.qo_indptr, out, ws)
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                for _ in range(2):
+                    step()
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            if B.pa_get_device_error(ws) or B.pa_get_device_error(ws_app):
+                raise RuntimeError("device error word set in the sweep")
+            ms_step = e0.elapsed_time(e1) / args.steps
+            per_layer = ms_step / layers
+            line = {"mode": "sweep", "context": context, "batch": batch, "layers": layers,
+                    "ms_per_step": round(ms_step, 4), "us_per_layer": round(per_layer * 1e3, 3),
+                    "unique_gbs": round(sb["unique"] / (per_layer * 1e-3) / 1e9, 1),
+                    "logical_gbs": round(sb["logical"] / (per_layer * 1e-3) / 1e9, 1),
+                    "frac_of_measured_hbm": round(sb["unique"] / (per_layer * 1e-3) / 1e9 / peak, 4),
+                    "tokens_per_layer_step_per_s": round(batch / (per_layer * 1e-3), 1),
+                    "bytes_per_layer": sb["unique"], "pool_blocks": spec["num_blocks"],
+                    "attention_call": call_name(ppages),
+                    "l2": "not flushed (36 layers x distinct pools stream %.1f GB per step)" %
+                          (sb["unique"] * layers / 1e9),
+                    "graph": "36 x (kv_append + attention) in one CUDA graph"}
+            print(json.dumps(line), flush=True)
+            del pools, graph
+            torch.cuda.empty_cache()
+    return 0
+
+
 # ------------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -238,6 +347,14 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="short")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-ctas", type=int, default=0, help="force the persistent decode grid size (0 = automatic)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="36-layer decode sweep (b in 1..128 at 2048 and 8192-with-shared-prefix), one JSON line "
+                         "per point, 36 x (append + attention) captured in a CUDA graph")
+    ap.add_argument("--layers", type=int, default=36)
+    ap.add_argument("--contexts", default="2048,8192", help="sweep contexts")
+    ap.add_argument("--batches", default="1,8,32,64,128", help="sweep decode batch sizes")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="run shared-prefix batches through pa_attention_varlen instead of the shared-prefix call")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -246,6 +363,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
     import torch.distributed as dist
@@ -260,7 +379,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     batch = W.workload_batch(args.workload, seed_offset=rank)
-    sb = W.step_bytes(batch)
+    ppages = 0 if args.no_cascade else batch.meta["shared_prefix_tokens"] // 16
+    sb = W.step_bytes(batch, ppages)
 
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
@@ -278,7 +398,8 @@ def main():
     out = torch.empty_like(d["q"])
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     R, total_q = batch.num_reqs, batch.total_q
-    ws = B.new_workspace(B.pa_attention_workspace_size(R, total_q, 32, 128, int(batch.seq_lens.max())), dev)
+    ws = B.new_workspace(B.pa_shared_prefix_workspace_size(R, total_q, 32, 128, int(batch.seq_lens.max()), ppages),
+                         dev)
     ws_app = B.new_workspace(B.PA_ERROR_WORD_BYTES, dev)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -290,8 +411,8 @@ def main():
 
     def step(src):
         B.pa_kv_append(src["k_new"], src["v_new"], src["slot_mapping"], k_cache, v_cache, workspace=ws_app)
-        B.pa_attention_varlen(src["q"], k_cache, v_cache, src["block_tables"], src["seq_lens"], src["qo_indptr"],
-                              batch.sm_scale, seq_lens_host=seq_h, qo_indptr_host=ind_h, out=out, workspace=ws)
+        attention(B, ppages, src["q"], k_cache, v_cache, src["block_tables"], src["seq_lens"], src["qo_indptr"],
+                  batch.sm_scale, seq_h, ind_h, out, ws)
 
     def barrier():
         if world > 1:
@@ -364,6 +485,8 @@ def main():
     peak, peak_kind = load_peaks()
     dec_ms = sum(dec) / len(dec) if dec else None
     achieved = sb["decode_kernel"] / (dec_ms * 1e-3) / 1e9 if dec_ms else None
+    pre = [ms for k_, ms in trace if k_ == "prefix"]
+    pre_ms = sum(pre) / len(pre) if pre else None
     kernel_share = {}
     for k_, ms in trace:
         kernel_share[k_] = kernel_share.get(k_, 0.0) + ms
@@ -379,6 +502,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (256 MiB read outside the events)",
+                   "attention_call": call_name(ppages),
                    "bytes_per_step": sb["unique"], "logical_bytes_per_step": sb["logical"],
                    "query_tokens_per_step": sb["query_tokens"]},
         "tokens_per_layer_step_per_s": round(sb["query_tokens"] * world / (t_step * 1e-3), 1),
@@ -392,6 +516,10 @@ def main():
                      "avg_launch_ms": round(dec_ms, 5) if dec_ms else None,
                      "kernel_time_share": {k_: round(v / sum(kernel_share.values()), 4)
                                            for k_, v in kernel_share.items()}},
+        **({"prefix_pass": {"algorithmic_bytes_per_launch": sb["prefix_kernel"],
+                            "avg_launch_ms": round(pre_ms, 5),
+                            "achieved_gbs": round(sb["prefix_kernel"] / (pre_ms * 1e-3) / 1e9, 2)}}
+           if pre_ms else {}),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(t_e2e, 5), "steps": e2e_steps},
         "gpu_launches": launches,

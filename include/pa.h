@@ -158,6 +158,54 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
                               void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_shared_prefix_workspace_size -- bytes of device workspace that
+ * pa_attention_varlen_shared_prefix needs for a batch with at most these
+ * sizes: the pa_attention_workspace_size() layout followed by the prefix
+ * partial ([total_q, num_q_heads, head_dim + 1] fp32) and the key-chunk
+ * partials it is merged from.  shared_prefix_pages = 0 gives
+ * pa_attention_workspace_size().  Returns 0 for negative arguments.
+ */
+size_t pa_shared_prefix_workspace_size(int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
+                                       int32_t max_seq_len, int32_t shared_prefix_pages);
+
+/*
+ * pa_attention_varlen_shared_prefix -- pa_attention_varlen for a batch whose
+ * requests all begin with the same shared_prefix_pages pages (the shared
+ * prefix blocks of "Inference optimisation" ch. 8, §8.3.2 and Fig. 8-13,
+ * referenced by every block table and stored once).
+ *   Same computation, arguments and results as pa_attention_varlen (up to
+ *   fp32 rounding order), with the work split by key range:
+ *     1. one tensor-core pass attends every query token of the batch to the
+ *        prefix keys [0, 16 * shared_prefix_pages), reading each prefix page
+ *        once per kv head for all rows together (no mask is needed: every
+ *        query comes after the prefix); key chunks of it run on separate CTAs
+ *        and are merged by log-sum-exp;
+ *     2. the decode and prefill kernels attend each row to its own keys
+ *        after the prefix and fold the prefix partial into their result by
+ *        log-sum-exp before rounding to bf16.
+ *   With fewer than two requests that have queries, or shared_prefix_pages
+ *   = 0, the call runs exactly as pa_attention_varlen.
+ * shared_prefix_pages  0 <= P <= max_blocks_per_req.  The caller asserts
+ *                that entries 0 .. P-1 of every block-table row hold the same
+ *                block ids (the pass reads them from the first request that
+ *                has queries; rows that differ get that request's prefix).
+ *                Every request with qo_len > 0 must have
+ *                seq_len - qo_len >= 16 * P (the prefix is cached before this
+ *                step's queries), else PA_ERR_INVALID_ARG.
+ * workspace      >= pa_shared_prefix_workspace_size(num_reqs, total_q,
+ *                num_q_heads, head_dim, max seq_len, P) bytes, 256-byte
+ *                aligned, zero-filled before its first use, as for
+ *                pa_attention_varlen (its counters are left at zero too).
+ * Errors: as pa_attention_varlen.
+ */
+pa_status pa_attention_varlen_shared_prefix(
+    const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks, const int32_t* block_tables,
+    int32_t max_blocks_per_req, const int32_t* seq_lens, const int32_t* qo_indptr, const int32_t* seq_lens_host,
+    const int32_t* qo_indptr_host, int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int32_t shared_prefix_pages, float sm_scale, void* out, float* lse,
+    void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_attention_varlen_noalloc -- pa_attention_varlen for callers that cannot
  * allocate device memory.  The pages describe no counterpart of this call;
  * it exists for callers that cannot obtain a workspace: code running where
@@ -234,7 +282,9 @@ typedef enum {
   PA_KERNEL_DECODE = 2,
   PA_KERNEL_COMBINE = 3, /* reserved: the split merge is fused into PA_KERNEL_DECODE */
   PA_KERNEL_PREFILL = 4,
-  PA_KERNEL_MERGE = 5
+  PA_KERNEL_MERGE = 5,
+  PA_KERNEL_PREFIX = 6,      /* shared-prefix pass of pa_attention_varlen_shared_prefix */
+  PA_KERNEL_PREFIX_MERGE = 7 /* merge of that pass's key-chunk partials */
 } pa_kernel_kind;
 
 pa_status pa_set_decode_ctas(int32_t n);

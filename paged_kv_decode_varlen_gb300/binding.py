@@ -27,7 +27,7 @@ PA_ERR_CUDA = 4
 PA_ERR_DEVICE_INDEX = 5
 PA_ERR_DEVICE_TIMEOUT = 6
 PA_ERROR_WORD_BYTES = 256
-KERNEL_KINDS = {1: "kv_append", 2: "decode", 3: "combine", 4: "prefill", 5: "merge"}
+KERNEL_KINDS = {1: "kv_append", 2: "decode", 3: "combine", 4: "prefill", 5: "merge", 6: "prefix", 7: "prefix_merge"}
 
 
 class PAError(RuntimeError):
@@ -51,6 +51,9 @@ _SIGS = {
     "pa_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pa_attention_varlen": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _f32, _P, _P, _P, _sz, _P]),
+    "pa_shared_prefix_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_attention_varlen_shared_prefix": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32,
+                                                 _i32, _i32, _i32, _f32, _P, _P, _P, _sz, _P]),
     "pa_attention_varlen_noalloc": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32,
                                            _i32, _f32, _P, _P, _P, _P]),
     "pa_merge_lse": (_i32, [_P, _P, _P, _P, _P, _P, _i64, _i32, _i32, _P]),
@@ -180,6 +183,53 @@ def pa_attention_varlen(q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, 
                                     ctypes.c_void_p(slh.data_ptr()), ctypes.c_void_p(qih.data_ptr()), R, total_q, Hq,
                                     Hkv, D, P, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                     workspace.numel(), _stream(stream)))
+    return (out, lse) if (return_lse or lse is not None) else out
+
+
+def pa_shared_prefix_workspace_size(num_reqs, total_q, num_q_heads, head_dim, max_seq_len,
+                                    shared_prefix_pages) -> int:
+    return int(_lib.pa_shared_prefix_workspace_size(num_reqs, total_q, num_q_heads, head_dim, max_seq_len,
+                                                    shared_prefix_pages))
+
+
+def pa_attention_varlen_shared_prefix(q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, sm_scale,
+                                      shared_prefix_pages, *, seq_lens_host=None, qo_indptr_host=None, out=None,
+                                      lse=None, workspace=None, stream=None, return_lse=False):
+    """pa_attention_varlen for a batch whose block tables all begin with the
+    same shared_prefix_pages blocks (see include/pa.h): the prefix is
+    attended once for every query and merged into each row by log-sum-exp."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(qo_indptr, torch.int32, "qo_indptr")
+    total_q, Hq, D = q.shape
+    nb, Hkv, P, D2 = k_cache.shape
+    R = seq_lens.shape[0]
+    if v_cache.shape != k_cache.shape or D2 != D or qo_indptr.shape != (R + 1,) or block_tables.dim() != 2 \
+            or block_tables.shape[0] != R:
+        raise ValueError("inconsistent shapes")
+    slh = _host_i32(seq_lens if seq_lens_host is None else seq_lens_host)
+    qih = _host_i32(qo_indptr if qo_indptr_host is None else qo_indptr_host)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    if workspace is None:
+        max_len = int(slh.max()) if R else 1
+        workspace = new_workspace(pa_shared_prefix_workspace_size(R, total_q, Hq, D, max_len, shared_prefix_pages),
+                                  q.device)
+    _check(_lib.pa_attention_varlen_shared_prefix(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        _ptr(qo_indptr), ctypes.c_void_p(slh.data_ptr()), ctypes.c_void_p(qih.data_ptr()), R, total_q, Hq, Hkv, D,
+        P, int(shared_prefix_pages), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
     return (out, lse) if (return_lse or lse is not None) else out
 
 

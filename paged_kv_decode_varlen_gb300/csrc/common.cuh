@@ -127,4 +127,20 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // bf16 pair -> float2 (element 0 in .x)
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 
+// Log-sum-exp merge of two normalised partials over disjoint key sets with
+// log2-domain lse a and b: the merged partial is wa * o_a + wb * o_b and the
+// merged lse is returned (both empty: weights 0, lse -inf).
+__device__ __forceinline__ float merge2_weights(float a, float b, float& wa, float& wb) {
+  const float M = fmaxf(a, b);
+  if (M == -INFINITY) {
+    wa = wb = 0.f;
+    return -INFINITY;
+  }
+  const float ea = exp2f(a - M), eb = exp2f(b - M);  // an empty side gives exp2(-inf) = 0
+  const float inv = 1.f / (ea + eb);
+  wa = ea * inv;
+  wb = eb * inv;
+  return M + log2f(ea + eb);
+}
+
 }  // namespace pa

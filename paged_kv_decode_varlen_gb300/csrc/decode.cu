@@ -134,6 +134,20 @@ __device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
 
 __device__ __forceinline__ void bar_all() { __syncthreads(); }
 
+// Folds the shared-prefix partial of this output row (4 dims at po, log2
+// lse plse2) into the normalised partial o with log2 lse lse2; returns the
+// merged lse.
+__device__ __forceinline__ float fold_prefix(float4& o, float lse2, const float* po, float plse2) {
+  float wo, wp;
+  const float l = merge2_weights(lse2, plse2, wo, wp);
+  const float4 y = *reinterpret_cast<const float4*>(po);
+  o.x = fmaf(wp, y.x, o.x * wo);
+  o.y = fmaf(wp, y.y, o.y * wo);
+  o.z = fmaf(wp, y.z, o.z * wo);
+  o.w = fmaf(wp, y.w, o.w * wo);
+  return l;
+}
+
 __global__ void __launch_bounds__(kThreads, 3)
     decode_kernel(const DecodeParams p, const __grid_constant__ DecodePlan plan) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -158,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (exists) {
         r = plan.rows[item];
         L = p.seq_lens[r];
-        size = max((L + kPage - 1) / kPage - p0, 0);
+        size = max((L + kPage - 1) / kPage - p.page_offset - p0, 0);
       }
       int incl = size;
 #pragma unroll
@@ -213,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     int32_t blk = -1;
     const Item& it = sm.items[lo];
-    const int page = it.p0 + (q - it.q_start);
+    const int page = p.page_offset + it.p0 + (q - it.q_start);
     if (q < it.q_start + it.n && page < p.max_blocks_per_req)
       blk = p.block_tables[(size_t)it.r * p.max_blocks_per_req + page];
     if (blk < 0 || blk >= p.num_blocks) {
@@ -262,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int c = tid & 7;    // dim chunk: dims [8c, 8c+8) and [64+8c, 64+8c+8)
   // After the transposed reduction lane c holds token u = bit0(c) of the
   // iteration and head hd = 2 bit2(c) + bit1(c).
-  const int hd = ((c >> 2) & 1) * 2 + ((c >> 1) & 1);
   const int slot_base = lane & ~7;
   bool aborted = false;
   int qg = 0;  // segment page counter at the current item's start
@@ -271,8 +284,9 @@ __global__ void __launch_bounds__(kThreads, 3)
     const Item& it = sm.items[k];
     const int tok = p.qo_indptr[it.r];
     const int qend = qg + it.n;
-    const int pages_r = (it.L + kPage - 1) / kPage;
-    const int tail_tokens = it.L - (pages_r - 1) * kPage;
+    const int pages_abs = (it.L + kPage - 1) / kPage;
+    const int pages_r = pages_abs - p.page_offset;  // pages of the row in the stream
+    const int tail_tokens = it.L - (pages_abs - 1) * kPage;
     // segment page at which this token slot is past the row's end (the
     // row's last page, when this slot is beyond its tokens), else none
     const int q_inv = (ts < tail_tokens) ? -1 : qg + (pages_r - 1 - it.p0);
@@ -481,11 +495,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     o.y *= inv;
     o.z *= inv;
     o.w *= inv;
-    const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
+    float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
     const int head = kvh * kGroup + g;
     const size_t orow = (size_t)tok * p.num_q_heads + head;
     const bool complete = (it.p0 == 0) && (it.n == pages_r);
     if (complete) {
+      if (p.prefix_o) lse2 = fold_prefix(o, lse2, p.prefix_o + orow * kHeadDim + d0, p.prefix_lse[orow]);
       uint2 packed;
       packed.x = pack_bf16x2(o.x, o.y);
       packed.y = pack_bf16x2(o.z, o.w);
@@ -535,11 +550,17 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
       }
       const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+      a4.x *= winv;
+      a4.y *= winv;
+      a4.z *= winv;
+      a4.w *= winv;
+      float l2 = wsum > 0.f ? Mx + log2f(wsum) : -INFINITY;
+      if (p.prefix_o) l2 = fold_prefix(a4, l2, p.prefix_o + orow * kHeadDim + d0, p.prefix_lse[orow]);
       uint2 packed;
-      packed.x = pack_bf16x2(a4.x * winv, a4.y * winv);
-      packed.y = pack_bf16x2(a4.z * winv, a4.w * winv);
+      packed.x = pack_bf16x2(a4.x, a4.y);
+      packed.y = pack_bf16x2(a4.z, a4.w);
       *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + d0) = packed;
-      if (p.lse && lane == 0) p.lse[orow] = wsum > 0.f ? (Mx + log2f(wsum)) * kLn2 : -INFINITY;
+      if (p.lse && lane == 0) p.lse[orow] = l2 * kLn2;
     }
     bar_all();  // the merge scratch and is_last are free again
   }

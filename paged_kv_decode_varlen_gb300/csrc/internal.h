@@ -49,6 +49,9 @@ struct DecodeParams {
   int32_t num_q_heads;
   int32_t num_kv_heads;
   float scale_log2;      // sm_scale * log2(e)
+  int32_t page_offset;   // leading pages of every row left out (a shared prefix attended elsewhere)
+  const float* prefix_o;    // fp32 [total_q, Hq, D] normalised partial over those pages, or null
+  const float* prefix_lse;  // fp32 [total_q, Hq] its log2-domain lse (with prefix_o)
   uint16_t* out;         // bf16 [total_q, Hq, D]
   float* lse;            // [total_q, Hq] natural log, or null
   float* piece_o;        // fp32 [2 * grid, 4, D]: a CTA's partial of its first / last item
@@ -81,8 +84,37 @@ struct PrefillParams {
   int32_t num_q_heads;
   int32_t num_kv_heads;
   float scale_log2;
+  int32_t kv_key_offset;    // keys [0, kv_key_offset) left out (a shared prefix, whole pages)
+  const float* prefix_o;    // as in DecodeParams, or null
+  const float* prefix_lse;
   uint16_t* out;
   float* lse;
+  int* err;
+};
+
+// Shared-prefix pass: all total_q query tokens against the prefix keys
+// [0, prefix_keys) of block-table row table_row, cut into key chunks of
+// chunk_keys (a multiple of 64).  Chunk partials go to chunk_o / chunk_lse
+// ([n_chunks][total_q][Hq] rows), merged into prefix_o / prefix_lse by the
+// merge kernel.  With one chunk the CTAs write prefix_o / prefix_lse directly.
+struct PrefixParams {
+  const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  int64_t num_blocks;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_req;
+  int32_t table_row;
+  int32_t total_q;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t prefix_keys;
+  int32_t chunk_keys;
+  float scale_log2;
+  float* chunk_o;
+  float* chunk_lse;
+  float* prefix_o;
+  float* prefix_lse;
   int* err;
 };
 
@@ -105,6 +137,8 @@ pa_status set_error(pa_status s, const char* fmt, ...);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, cudaStream_t stream);
+cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, cudaStream_t stream);
+cudaError_t launch_prefix_merge(const PrefixParams& p, int n_chunks, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
 // Query tile of the prefill kernel (query tokens per CTA).

@@ -107,7 +107,9 @@ int grid_cap(int32_t num_reqs, int32_t num_kv_heads, int32_t max_seq_len) {
   const int64_t rows = std::min<int64_t>(std::max(num_reqs, 0), pa::kPlanMaxRows);
   const int64_t items = rows * std::max(num_kv_heads, 1);
   const int64_t pages = items * std::max(1, pages_of(max_seq_len));
-  int64_t g = std::max<int64_t>(kSlotCap, (pages + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta);
+  // CTAs needed by the longest segments, rounded up to whole waves of kSlotCap
+  int64_t g = (pages + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta;
+  g = std::max<int64_t>(1, (g + kSlotCap - 1) / kSlotCap) * kSlotCap;
   g = std::max<int64_t>(g, (items + 31) / 32);
   return (int)std::min<int64_t>(g, pa::kPlanMaxCtas);
 }
@@ -133,15 +135,48 @@ WorkspaceLayout layout(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim, 
   return w;
 }
 
+// Shared-prefix pass: the chunk count for a call and the workspace region
+// after the base layout: [prefix o (total_q x Hq x D fp32) | prefix lse |
+// chunk o (chunks x total_q x Hq x D) | chunk lse].  Chunks are sized so that chunks x Hkv x query tiles fills
+// about two CTAs per SM; kPrefixCtaCap bounds that for workspace sizing.
+constexpr int kPrefixCtaCap = 512;
+constexpr int kPrefixKeyTile = 64;  // keys per tensor-core tile
+
+int64_t prefix_qtiles(int32_t total_q) { return ((int64_t)std::max(total_q, 0) + pa::kPrefillQTile - 1) / pa::kPrefillQTile; }
+
+int prefix_chunk_cap(int32_t total_q, int32_t hkv, int32_t prefix_pages) {
+  const int64_t groups = std::max<int64_t>(1, prefix_qtiles(total_q) * std::max(hkv, 1));
+  const int64_t tiles = ((int64_t)prefix_pages * pa::kPage + kPrefixKeyTile - 1) / kPrefixKeyTile;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (kPrefixCtaCap + groups - 1) / groups));
+}
+
+struct PrefixLayout {
+  size_t prefix_o, prefix_lse, chunk_o, chunk_lse, total;
+};
+
+PrefixLayout prefix_layout(size_t base, int32_t total_q, int32_t num_q_heads, int32_t head_dim, int32_t prefix_pages) {
+  PrefixLayout w;
+  const int32_t hkv = std::max(std::max(num_q_heads, 0) / PA_GQA_GROUP, 1);
+  const size_t rows = (size_t)std::max(total_q, 0) * (size_t)std::max(num_q_heads, 0);
+  const int cap = prefix_chunk_cap(total_q, hkv, prefix_pages);
+  const size_t chunk_rows = cap > 1 ? (size_t)cap * rows : 0;  // one chunk writes the prefix partial itself
+  w.prefix_o = base;
+  w.prefix_lse = w.prefix_o + align256(rows * (size_t)std::max(head_dim, 0) * 4);
+  w.chunk_o = w.prefix_lse + align256(rows * 4);
+  w.chunk_lse = w.chunk_o + align256(chunk_rows * (size_t)std::max(head_dim, 0) * 4);
+  w.total = w.chunk_lse + align256(chunk_rows * 4);
+  return w;
+}
+
 // Plan one persistent decode launch over decode rows rows[0..n): fills
 // plan, returns the grid size (0 when there is nothing to do, -1 when no
 // valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
-int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, int num_kv_heads, int gcap,
-                pa::DecodePlan& plan) {
+int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, int page_offset, int num_kv_heads,
+                int gcap, pa::DecodePlan& plan) {
   std::vector<int32_t> pages(n);
   int64_t total = 0;  // pages of one kv head's stream
   for (int d = 0; d < n; ++d) {
-    pages[d] = pages_of(seq_lens_host[rows[d]]);
+    pages[d] = pages_of(seq_lens_host[rows[d]]) - page_offset;
     total += pages[d];
   }
   if (total == 0) return 0;
@@ -153,6 +188,11 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, int nu
                                                 (total * num_kv_heads + kMinSegPages - 1) / kMinSegPages /
                                                     num_kv_heads);
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, seg_cap));
+  // a segment holds at most kDecodeMaxPagesPerCta pages; when that forces more
+  // segments than one wave has slots, use whole waves so no wave runs part-empty
+  const int64_t wave = std::max<int64_t>(1, (int64_t)sm_count() * kDecodeCtasPerSm / num_kv_heads);
+  const int64_t need = (total + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta;
+  if (forced <= 0 && need > nseg) nseg = std::min<int64_t>((need + wave - 1) / wave * wave, seg_cap);
   int64_t seg = (total + nseg - 1) / nseg;
   seg = std::max<int64_t>(seg, (total + seg_cap - 1) / seg_cap);
   seg = std::min<int64_t>(seg, pa::kDecodeMaxPagesPerCta);  // more segments if one would be too long
@@ -208,6 +248,200 @@ pa_status pa::set_error(pa_status s, const char* fmt, ...) {
   va_end(ap);
   return s;
 }
+
+namespace {
+
+// Both attention entry points.  prefix_pages > 0: the first prefix_pages
+// pages of every request are one shared prefix, attended once for all
+// queries by the prefix pass and folded into each row's own part.
+pa_status attention(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                    const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* seq_lens,
+                    const int32_t* qo_indptr, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
+                    int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int32_t prefix_pages, float sm_scale, void* out, float* lse, void* workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+  pa_status s = check_shape(num_q_heads, num_kv_heads, head_dim, block_size);
+  if (s != PA_OK) return s;
+  if (num_reqs < 0 || num_reqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_reqs %d outside [0, 65535]", num_reqs);
+  if (total_q < 0) return fail(PA_ERR_INVALID_ARG, "total_q %d < 0", total_q);
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
+  if (!(fabsf(sm_scale) < INFINITY)) return fail(PA_ERR_INVALID_ARG, "sm_scale must be finite");
+  if (!seq_lens_host || !qo_indptr_host) return fail(PA_ERR_INVALID_ARG, "host metadata pointers are required");
+  if (!k_cache || !v_cache || !workspace || !seq_lens || !qo_indptr || (num_reqs > 0 && !block_tables) ||
+      (total_q > 0 && (!q || !out)))
+    return fail(PA_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || !aligned(lse, 4) || !aligned(block_tables, 4))
+    return fail(PA_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned, workspace 256-byte aligned");
+  if (qo_indptr_host[0] != 0) return fail(PA_ERR_INVALID_ARG, "qo_indptr[0] = %d, must be 0", qo_indptr_host[0]);
+  if (qo_indptr_host[num_reqs] != total_q)
+    return fail(PA_ERR_INVALID_ARG, "qo_indptr[num_reqs] = %d != total_q = %d", qo_indptr_host[num_reqs], total_q);
+
+  if (prefix_pages < 0 || prefix_pages > max_blocks_per_req)
+    return fail(PA_ERR_INVALID_ARG, "shared_prefix_pages %d outside [0, max_blocks_per_req %d]", prefix_pages,
+                max_blocks_per_req);
+  // classify rows and collect the plan inputs
+  std::vector<int32_t> decode_rows;
+  int32_t active = 0, first_active = -1;
+  int32_t max_len = 1;
+  std::vector<std::pair<int32_t, int32_t>> tiles;  // (kv extent of the tile, item index) for ordering
+  static thread_local pa::PrefillItems items;
+  std::vector<int32_t> item_req, item_q0;
+  for (int r = 0; r < num_reqs; ++r) {
+    const int32_t qo_len = qo_indptr_host[r + 1] - qo_indptr_host[r];
+    const int32_t L = seq_lens_host[r];
+    if (qo_len < 0) return fail(PA_ERR_INVALID_ARG, "qo_indptr decreases at request %d", r);
+    if (L < 0 || L > PA_MAX_SEQ_LEN)
+      return fail(L < 0 ? PA_ERR_INVALID_ARG : PA_ERR_UNSUPPORTED, "seq_lens[%d] = %d outside [0, %d]", r, L,
+                  PA_MAX_SEQ_LEN);
+    if (qo_len > L) return fail(PA_ERR_INVALID_ARG, "request %d: qo_len %d > seq_len %d", r, qo_len, L);
+    if (pages_of(L) > max_blocks_per_req)
+      return fail(PA_ERR_INVALID_ARG, "request %d: %d pages > max_blocks_per_req %d", r, pages_of(L),
+                  max_blocks_per_req);
+    max_len = std::max(max_len, L);
+    if (qo_len > 0) {
+      if (first_active < 0) first_active = r;
+      ++active;
+      if ((int64_t)L - qo_len < (int64_t)prefix_pages * pa::kPage)
+        return fail(PA_ERR_INVALID_ARG, "request %d: the shared prefix (%d pages) must be cached before its %d queries",
+                    r, prefix_pages, qo_len);
+    }
+    if (qo_len == 1) {
+      decode_rows.push_back(r);
+    } else if (qo_len > 1) {
+      for (int32_t j0 = 0; j0 < qo_len; j0 += pa::kPrefillQTile) {
+        tiles.push_back({L - qo_len + std::min(qo_len, j0 + pa::kPrefillQTile), (int32_t)item_req.size()});
+        item_req.push_back(r);
+        item_q0.push_back(j0);
+      }
+    }
+  }
+  const WorkspaceLayout wl = layout(num_reqs, num_q_heads, head_dim, max_len);
+  const PrefixLayout pl = prefix_layout(wl.total, total_q, num_q_heads, head_dim, prefix_pages);
+  const size_t need = prefix_pages > 0 ? pl.total : wl.total;
+  if (workspace_bytes < need)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, need);
+  if (total_q == 0) return ok();
+  // a prefix read by one request only is not worth a separate pass
+  const int32_t P = active >= 2 ? prefix_pages : 0;
+  if (P > 0 && prefix_qtiles(total_q) > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "total_q %d too large for the shared-prefix pass", total_q);
+
+  char* ws = static_cast<char*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  const float scale_log2 = sm_scale * pa::kLog2e;
+  float* prefix_o = P > 0 ? reinterpret_cast<float*>(ws + pl.prefix_o) : nullptr;
+  float* prefix_lse = P > 0 ? reinterpret_cast<float*>(ws + pl.prefix_lse) : nullptr;
+
+  if (P > 0) {
+    pa::PrefixParams xp;
+    xp.q = static_cast<const uint16_t*>(q);
+    xp.k_cache = static_cast<const uint16_t*>(k_cache);
+    xp.v_cache = static_cast<const uint16_t*>(v_cache);
+    xp.num_blocks = num_blocks;
+    xp.block_tables = block_tables;
+    xp.max_blocks_per_req = max_blocks_per_req;
+    xp.table_row = first_active;
+    xp.total_q = total_q;
+    xp.num_q_heads = num_q_heads;
+    xp.num_kv_heads = num_kv_heads;
+    xp.prefix_keys = P * pa::kPage;
+    // about two CTAs per SM over chunks x kv heads x query tiles
+    const int64_t groups = prefix_qtiles(total_q) * num_kv_heads;
+    int n_chunks = (int)std::min<int64_t>(prefix_chunk_cap(total_q, num_kv_heads, P),
+                                          std::max<int64_t>(1, (2 * sm_count() + groups - 1) / groups));
+    const int64_t tiles = ((int64_t)xp.prefix_keys + kPrefixKeyTile - 1) / kPrefixKeyTile;
+    xp.chunk_keys = (int32_t)((tiles + n_chunks - 1) / n_chunks * kPrefixKeyTile);
+    n_chunks = (int)((xp.prefix_keys + xp.chunk_keys - 1) / xp.chunk_keys);
+    xp.scale_log2 = scale_log2;
+    xp.chunk_o = reinterpret_cast<float*>(ws + pl.chunk_o);
+    xp.chunk_lse = reinterpret_cast<float*>(ws + pl.chunk_lse);
+    xp.prefix_o = prefix_o;
+    xp.prefix_lse = prefix_lse;
+    xp.err = err;
+    s = run_launch(PA_KERNEL_PREFIX, "prefix", stream, [&] { return pa::launch_prefix(xp, n_chunks, stream); });
+    if (s != PA_OK) return s;
+    if (n_chunks > 1) {
+      s = run_launch(PA_KERNEL_PREFIX_MERGE, "prefix_merge", stream,
+                     [&] { return pa::launch_prefix_merge(xp, n_chunks, stream); });
+      if (s != PA_OK) return s;
+    }
+  }
+
+  if (!tiles.empty()) {
+    // longest key extent first, so the big tiles do not form the tail
+    std::stable_sort(tiles.begin(), tiles.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+    pa::PrefillParams pp;
+    pp.q = static_cast<const uint16_t*>(q);
+    pp.k_cache = static_cast<const uint16_t*>(k_cache);
+    pp.v_cache = static_cast<const uint16_t*>(v_cache);
+    pp.num_blocks = num_blocks;
+    pp.block_tables = block_tables;
+    pp.max_blocks_per_req = max_blocks_per_req;
+    pp.seq_lens = seq_lens;
+    pp.qo_indptr = qo_indptr;
+    pp.num_q_heads = num_q_heads;
+    pp.num_kv_heads = num_kv_heads;
+    pp.scale_log2 = scale_log2;
+    pp.kv_key_offset = P * pa::kPage;
+    pp.prefix_o = prefix_o;
+    pp.prefix_lse = prefix_lse;
+    pp.out = static_cast<uint16_t*>(out);
+    pp.lse = lse;
+    pp.err = err;
+    for (size_t base = 0; base < tiles.size(); base += pa::kMaxPrefillItems) {
+      const size_t n = std::min(tiles.size() - base, (size_t)pa::kMaxPrefillItems);
+      items.count = (int32_t)n;
+      for (size_t i = 0; i < n; ++i) {
+        const int32_t idx = tiles[base + i].second;
+        items.req[i] = item_req[idx];
+        items.q_start[i] = item_q0[idx];
+      }
+      s = run_launch(PA_KERNEL_PREFILL, "prefill", stream, [&] { return pa::launch_prefill(pp, items, stream); });
+      if (s != PA_OK) return s;
+    }
+  }
+
+  if (!decode_rows.empty()) {
+    pa::DecodeParams dp;
+    dp.q = static_cast<const uint16_t*>(q);
+    dp.k_cache = static_cast<const uint16_t*>(k_cache);
+    dp.v_cache = static_cast<const uint16_t*>(v_cache);
+    dp.num_blocks = num_blocks;
+    dp.block_tables = block_tables;
+    dp.max_blocks_per_req = max_blocks_per_req;
+    dp.seq_lens = seq_lens;
+    dp.qo_indptr = qo_indptr;
+    dp.num_q_heads = num_q_heads;
+    dp.num_kv_heads = num_kv_heads;
+    dp.scale_log2 = scale_log2;
+    dp.page_offset = P;
+    dp.prefix_o = prefix_o;
+    dp.prefix_lse = prefix_lse;
+    dp.out = static_cast<uint16_t*>(out);
+    dp.lse = lse;
+    dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
+    dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
+    dp.counters = reinterpret_cast<int*>(ws + wl.counters);
+    dp.scratch = reinterpret_cast<float*>(ws + wl.scratch);
+    dp.err = err;
+    static thread_local pa::DecodePlan plan;
+    const int gcap = grid_cap(num_reqs, num_kv_heads, max_len);
+    // one launch per kPlanMaxRows decode rows (the plan travels as kernel
+    // parameters); launches on one stream run in order and reuse the slots
+    for (size_t d0 = 0; d0 < decode_rows.size(); d0 += pa::kPlanMaxRows) {
+      const int n = (int)std::min(decode_rows.size() - d0, (size_t)pa::kPlanMaxRows);
+      const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, P, num_kv_heads, gcap, plan);
+      if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
+      if (grid == 0) continue;
+      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, stream); });
+      if (s != PA_OK) return s;
+    }
+  }
+  return ok();
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -269,125 +503,28 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
                               int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
                               int32_t head_dim, int32_t block_size, float sm_scale, void* out, float* lse,
                               void* workspace, size_t workspace_bytes, pa_stream_t stream) {
-  pa_status s = check_shape(num_q_heads, num_kv_heads, head_dim, block_size);
-  if (s != PA_OK) return s;
-  if (num_reqs < 0 || num_reqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_reqs %d outside [0, 65535]", num_reqs);
-  if (total_q < 0) return fail(PA_ERR_INVALID_ARG, "total_q %d < 0", total_q);
-  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
-  if (!(fabsf(sm_scale) < INFINITY)) return fail(PA_ERR_INVALID_ARG, "sm_scale must be finite");
-  if (!seq_lens_host || !qo_indptr_host) return fail(PA_ERR_INVALID_ARG, "host metadata pointers are required");
-  if (!k_cache || !v_cache || !workspace || !seq_lens || !qo_indptr || (num_reqs > 0 && !block_tables) ||
-      (total_q > 0 && (!q || !out)))
-    return fail(PA_ERR_INVALID_ARG, "null device pointer");
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(workspace, 256) || !aligned(lse, 4) || !aligned(block_tables, 4))
-    return fail(PA_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned, workspace 256-byte aligned");
-  if (qo_indptr_host[0] != 0) return fail(PA_ERR_INVALID_ARG, "qo_indptr[0] = %d, must be 0", qo_indptr_host[0]);
-  if (qo_indptr_host[num_reqs] != total_q)
-    return fail(PA_ERR_INVALID_ARG, "qo_indptr[num_reqs] = %d != total_q = %d", qo_indptr_host[num_reqs], total_q);
+  return attention(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
+                   seq_lens_host, qo_indptr_host, num_reqs, total_q, num_q_heads, num_kv_heads, head_dim, block_size,
+                   0, sm_scale, out, lse, workspace, workspace_bytes, stream);
+}
 
-  // classify rows and collect the plan inputs
-  std::vector<int32_t> decode_rows;
-  int32_t max_len = 1;
-  std::vector<std::pair<int32_t, int32_t>> tiles;  // (kv extent of the tile, item index) for ordering
-  static thread_local pa::PrefillItems items;
-  std::vector<int32_t> item_req, item_q0;
-  for (int r = 0; r < num_reqs; ++r) {
-    const int32_t qo_len = qo_indptr_host[r + 1] - qo_indptr_host[r];
-    const int32_t L = seq_lens_host[r];
-    if (qo_len < 0) return fail(PA_ERR_INVALID_ARG, "qo_indptr decreases at request %d", r);
-    if (L < 0 || L > PA_MAX_SEQ_LEN)
-      return fail(L < 0 ? PA_ERR_INVALID_ARG : PA_ERR_UNSUPPORTED, "seq_lens[%d] = %d outside [0, %d]", r, L,
-                  PA_MAX_SEQ_LEN);
-    if (qo_len > L) return fail(PA_ERR_INVALID_ARG, "request %d: qo_len %d > seq_len %d", r, qo_len, L);
-    if (pages_of(L) > max_blocks_per_req)
-      return fail(PA_ERR_INVALID_ARG, "request %d: %d pages > max_blocks_per_req %d", r, pages_of(L),
-                  max_blocks_per_req);
-    max_len = std::max(max_len, L);
-    if (qo_len == 1) {
-      decode_rows.push_back(r);
-    } else if (qo_len > 1) {
-      for (int32_t j0 = 0; j0 < qo_len; j0 += pa::kPrefillQTile) {
-        tiles.push_back({L - qo_len + std::min(qo_len, j0 + pa::kPrefillQTile), (int32_t)item_req.size()});
-        item_req.push_back(r);
-        item_q0.push_back(j0);
-      }
-    }
-  }
-  const WorkspaceLayout wl = layout(num_reqs, num_q_heads, head_dim, max_len);
-  if (workspace_bytes < wl.total)
-    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, wl.total);
-  if (total_q == 0) return ok();
+size_t pa_shared_prefix_workspace_size(int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
+                                       int32_t max_seq_len, int32_t shared_prefix_pages) {
+  if (num_reqs < 0 || total_q < 0 || num_q_heads < 0 || head_dim < 0 || shared_prefix_pages < 0) return 0;
+  const size_t base = layout(num_reqs, num_q_heads, head_dim, std::max(max_seq_len, 1)).total;
+  if (shared_prefix_pages == 0) return base;
+  return prefix_layout(base, total_q, num_q_heads, head_dim, shared_prefix_pages).total;
+}
 
-  char* ws = static_cast<char*>(workspace);
-  int* err = reinterpret_cast<int*>(ws);
-  const float scale_log2 = sm_scale * pa::kLog2e;
-
-  if (!tiles.empty()) {
-    // longest key extent first, so the big tiles do not form the tail
-    std::stable_sort(tiles.begin(), tiles.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
-    pa::PrefillParams pp;
-    pp.q = static_cast<const uint16_t*>(q);
-    pp.k_cache = static_cast<const uint16_t*>(k_cache);
-    pp.v_cache = static_cast<const uint16_t*>(v_cache);
-    pp.num_blocks = num_blocks;
-    pp.block_tables = block_tables;
-    pp.max_blocks_per_req = max_blocks_per_req;
-    pp.seq_lens = seq_lens;
-    pp.qo_indptr = qo_indptr;
-    pp.num_q_heads = num_q_heads;
-    pp.num_kv_heads = num_kv_heads;
-    pp.scale_log2 = scale_log2;
-    pp.out = static_cast<uint16_t*>(out);
-    pp.lse = lse;
-    pp.err = err;
-    for (size_t base = 0; base < tiles.size(); base += pa::kMaxPrefillItems) {
-      const size_t n = std::min(tiles.size() - base, (size_t)pa::kMaxPrefillItems);
-      items.count = (int32_t)n;
-      for (size_t i = 0; i < n; ++i) {
-        const int32_t idx = tiles[base + i].second;
-        items.req[i] = item_req[idx];
-        items.q_start[i] = item_q0[idx];
-      }
-      s = run_launch(PA_KERNEL_PREFILL, "prefill", stream, [&] { return pa::launch_prefill(pp, items, stream); });
-      if (s != PA_OK) return s;
-    }
-  }
-
-  if (!decode_rows.empty()) {
-    pa::DecodeParams dp;
-    dp.q = static_cast<const uint16_t*>(q);
-    dp.k_cache = static_cast<const uint16_t*>(k_cache);
-    dp.v_cache = static_cast<const uint16_t*>(v_cache);
-    dp.num_blocks = num_blocks;
-    dp.block_tables = block_tables;
-    dp.max_blocks_per_req = max_blocks_per_req;
-    dp.seq_lens = seq_lens;
-    dp.qo_indptr = qo_indptr;
-    dp.num_q_heads = num_q_heads;
-    dp.num_kv_heads = num_kv_heads;
-    dp.scale_log2 = scale_log2;
-    dp.out = static_cast<uint16_t*>(out);
-    dp.lse = lse;
-    dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
-    dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
-    dp.counters = reinterpret_cast<int*>(ws + wl.counters);
-    dp.scratch = reinterpret_cast<float*>(ws + wl.scratch);
-    dp.err = err;
-    static thread_local pa::DecodePlan plan;
-    const int gcap = grid_cap(num_reqs, num_kv_heads, max_len);
-    // one launch per kPlanMaxRows decode rows (the plan travels as kernel
-    // parameters); launches on one stream run in order and reuse the slots
-    for (size_t d0 = 0; d0 < decode_rows.size(); d0 += pa::kPlanMaxRows) {
-      const int n = (int)std::min(decode_rows.size() - d0, (size_t)pa::kPlanMaxRows);
-      const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, num_kv_heads, gcap, plan);
-      if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
-      if (grid == 0) continue;
-      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, stream); });
-      if (s != PA_OK) return s;
-    }
-  }
-  return ok();
+pa_status pa_attention_varlen_shared_prefix(
+    const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks, const int32_t* block_tables,
+    int32_t max_blocks_per_req, const int32_t* seq_lens, const int32_t* qo_indptr, const int32_t* seq_lens_host,
+    const int32_t* qo_indptr_host, int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t block_size, int32_t shared_prefix_pages, float sm_scale, void* out, float* lse,
+    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  return attention(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
+                   seq_lens_host, qo_indptr_host, num_reqs, total_q, num_q_heads, num_kv_heads, head_dim, block_size,
+                   shared_prefix_pages, sm_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_merge_lse(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,

@@ -226,8 +226,11 @@ def sweep_point(batch: int, context: int, *, seed: int = SEED0 + 5) -> dict:
 #   Block table: 4 B per page read.  Append: k_new + v_new read and written
 #   (4 x Hkv x D x 2 B... i.e. 2 x 4096 B per token) plus the 8-byte slot.
 # Split-KV partial results are implementation overhead and are not counted.
+# With prefix_pages > 0 (the shared-prefix call) the decode kernel reads only
+# the pages after the prefix, and the prefix pass reads the prefix pages once
+# plus every query.
 # ---------------------------------------------------------------------------
-def step_bytes(b: Batch) -> dict:
+def step_bytes(b: Batch, prefix_pages: int = 0) -> dict:
     total_q, Hq, D = b.q.shape
     _, Hkv, P, _ = b.k_cache.shape
     per_tok = 2 * Hkv * D * 2
@@ -251,14 +254,15 @@ def step_bytes(b: Batch) -> dict:
     dec_seen = {}
     for r in np.nonzero(decode)[0]:
         L = int(seq[r])
-        for i in range(-(-L // P)):
+        for i in range(prefix_pages, -(-L // P)):
             blk = int(b.block_tables[r, i])
             dec_seen[blk] = max(dec_seen.get(blk, 0), min(P, L - i * P))
     decode_kv_unique = sum(dec_seen.values()) * per_tok
     n_dec = int(decode.sum())
     decode_kernel = decode_kv_unique + n_dec * Hq * D * 2 + int(
-        sum(4 * (-(-int(L) // P)) for L in seq[decode]))
+        sum(4 * (-(-int(L) // P) - prefix_pages) for L in seq[decode]))
+    prefix_kernel = prefix_pages * P * per_tok + total_q * Hq * D * 2 + 4 * prefix_pages if prefix_pages else 0
     return dict(unique=unique_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
                 logical=logical_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
                 unique_kv=unique_kv, logical_kv=logical_kv, decode_kernel=decode_kernel,
-                query_tokens=int(total_q))
+                prefix_kernel=prefix_kernel, query_tokens=int(total_q))

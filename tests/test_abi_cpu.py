@@ -109,3 +109,39 @@ def test_grid_override_bounds():
     assert lib.pa_set_decode_ctas(1025) == b.PA_ERR_INVALID_ARG
     assert lib.pa_set_decode_ctas(-1) == b.PA_ERR_INVALID_ARG
     assert lib.pa_set_decode_ctas(0) == b.PA_OK
+
+
+def test_shared_prefix_workspace_size():
+    base = b.pa_attention_workspace_size(16, 16, 32, 128, 8447)
+    assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 0) == base
+    # + prefix partial (16 x 32 rows of 128 fp32) + its lse
+    # + 64 key-chunk partials (512-CTA bound / 8 kv heads) of the same rows
+    rows = 16 * 32
+    assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 384) == \
+        base + rows * 512 + rows * 4 + 64 * rows * 512 + 64 * rows * 4
+    # a 5-page prefix has two 64-key tiles, so at most two chunks
+    assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 5) == \
+        base + rows * 512 + rows * 4 + 2 * rows * 512 + 2 * rows * 4
+    # 64 query tiles x 8 kv heads fill the CTA bound: one chunk, no chunk partials
+    base2 = b.pa_attention_workspace_size(4, 1024, 32, 128, 3000)
+    assert b.pa_shared_prefix_workspace_size(4, 1024, 32, 128, 3000, 96) == \
+        base2 + 1024 * 32 * 512 + 1024 * 32 * 4
+    assert b.pa_shared_prefix_workspace_size(4, 4, 32, 128, 100, -1) == 0
+
+
+def _attn_prefix(pages, seq=(40, 100), ind=(0, 1, 2), wsb=1 << 30, mb=40):
+    slh = (ctypes.c_int32 * 2)(*seq)
+    qih = (ctypes.c_int32 * 3)(*ind)
+    return lib.pa_attention_varlen_shared_prefix(FAKE, FAKE, FAKE, 64, FAKE, mb, FAKE, FAKE, slh, qih, 2, ind[2],
+                                                 32, 8, 128, 16, pages, 0.088, FAKE, None, FAKE, wsb, None)
+
+
+def test_shared_prefix_validation():
+    assert _attn_prefix(-1) == b.PA_ERR_INVALID_ARG
+    assert _attn_prefix(41) == b.PA_ERR_INVALID_ARG                      # beyond max_blocks_per_req
+    assert _attn_prefix(3) == b.PA_ERR_INVALID_ARG                       # 40 - 1 = 39 cached keys < 48
+    assert _attn_prefix(2, seq=(40, 40), ind=(0, 1, 11)) == b.PA_ERR_INVALID_ARG  # 40 - 10 = 30 < 32
+    # the base workspace is not enough once the prefix pass runs
+    need = b.pa_shared_prefix_workspace_size(2, 2, 32, 128, 100, 2)
+    assert _attn_prefix(2, wsb=need - 256) == b.PA_ERR_WORKSPACE_TOO_SMALL
+    assert "workspace" in lib.pa_last_error_message().decode()
