@@ -1,6 +1,7 @@
 // Host-side interface between the C ABI (pa_api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -62,6 +63,15 @@ struct DecodeParams {
 };
 // per-CTA merge scratch: 4 warps x 4 heads x D sums, then 4 x 4 max and sum
 constexpr int kScratchFloats = 4 * 4 * 128 + 2 * 4 * 4;
+
+// Tiled TMA maps of the tensor-core tile kernels (host-encoded, passed by
+// value): q as [total_q][Hq][D] with 64 x 4 x 32 boxes, the K and V pools as
+// [num_blocks * Hkv * 16][D] rows with 64 x 16 boxes, all 128-byte swizzled.
+struct TcMaps {
+  CUtensorMap q;
+  CUtensorMap k;
+  CUtensorMap v;
+};
 
 // Prefill work items: (request, first query of the tile) pairs, passed by
 // value in the kernel's parameter block.
@@ -136,13 +146,16 @@ pa_status set_error(pa_status s, const char* fmt, ...);
 // Each launcher enqueues one kernel on `stream` and returns its launch error.
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, cudaStream_t stream);
-cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
+                           cudaStream_t stream);
+cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream);
 cudaError_t launch_prefix_merge(const PrefixParams& p, int n_chunks, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
-// Query tile of the prefill kernel (query tokens per CTA).
-constexpr int kPrefillQTile = 16;
+// Query tile of the tensor-core tile kernels (query tokens per CTA: with the
+// 4 heads of a GQA group, 128 rows = the MMA's M) and their key tile.
+constexpr int kPrefillQTile = 32;
+constexpr int kTcKeyTile = 128;
 // Decode kernel: pages a CTA may hold block ids for (bounds the segment).
 constexpr int kDecodeMaxPagesPerCta = 1024;
 

@@ -12,6 +12,8 @@
 #include <mutex>
 #include <vector>
 
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
 #include "common.cuh"
 #include "internal.h"
 #include "pa.h"
@@ -137,10 +139,11 @@ WorkspaceLayout layout(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim, 
 
 // Shared-prefix pass: the chunk count for a call and the workspace region
 // after the base layout: [prefix o (total_q x Hq x D fp32) | prefix lse |
-// chunk o (chunks x total_q x Hq x D) | chunk lse].  Chunks are sized so that chunks x Hkv x query tiles fills
-// about two CTAs per SM; kPrefixCtaCap bounds that for workspace sizing.
+// chunk o (chunks x total_q x Hq x D) | chunk lse].  Chunks are sized so
+// that chunks x Hkv x query tiles gives about one CTA per SM; kPrefixCtaCap
+// bounds that for workspace sizing.
 constexpr int kPrefixCtaCap = 512;
-constexpr int kPrefixKeyTile = 64;  // keys per tensor-core tile
+constexpr int kPrefixKeyTile = pa::kTcKeyTile;  // keys per tensor-core tile
 
 int64_t prefix_qtiles(int32_t total_q) { return ((int64_t)std::max(total_q, 0) + pa::kPrefillQTile - 1) / pa::kPrefillQTile; }
 
@@ -224,6 +227,51 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, int pa
     if (seg == 1) return -1;
     seg = (seg + 1) / 2;  // shorter segments touch fewer rows
   }
+}
+
+// ------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Tiled maps of q ([total_q][Hq][128] bf16, boxes 64 x 4 heads x 32 tokens)
+// and of the K / V pools (rows of 128 bf16, one per (block, kv head, token),
+// boxes 64 x 16 rows), 128-byte swizzled; out-of-range q tokens read as 0.
+pa_status make_tc_maps(const void* q, int32_t total_q, int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                       int64_t num_blocks, int32_t num_kv_heads, pa::TcMaps& m) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int64_t rows = num_blocks * num_kv_heads * pa::kPage;
+  if (rows >= (int64_t(1) << 31)) return fail(PA_ERR_UNSUPPORTED, "pool of %lld rows: too many for the tile kernels",
+                                               (long long)rows);
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t qdims[3] = {(cuuint64_t)pa::kHeadDim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+  const cuuint64_t qstrides[2] = {(cuuint64_t)pa::kHeadDim * 2, (cuuint64_t)num_q_heads * pa::kHeadDim * 2};
+  const cuuint32_t qbox[3] = {64, (cuuint32_t)pa::kGroup, (cuuint32_t)pa::kPrefillQTile};
+  CUresult r = enc(&m.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qdims, qstrides, qbox, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "encoding the q tensor map: CUresult %d", (int)r);
+  const cuuint64_t kdims[2] = {(cuuint64_t)pa::kHeadDim, (cuuint64_t)rows};
+  const cuuint64_t kstrides[1] = {(cuuint64_t)pa::kHeadDim * 2};
+  const cuuint32_t kbox[2] = {64, (cuuint32_t)pa::kPage};
+  r = enc(&m.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k_cache), kdims, kstrides, kbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "encoding the K tensor map: CUresult %d", (int)r);
+  r = enc(&m.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(v_cache), kdims, kstrides, kbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "encoding the V tensor map: CUresult %d", (int)r);
+  return PA_OK;
 }
 
 pa_status check_shape(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
@@ -332,6 +380,11 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
   const float scale_log2 = sm_scale * pa::kLog2e;
   float* prefix_o = P > 0 ? reinterpret_cast<float*>(ws + pl.prefix_o) : nullptr;
   float* prefix_lse = P > 0 ? reinterpret_cast<float*>(ws + pl.prefix_lse) : nullptr;
+  static thread_local pa::TcMaps maps;
+  if (P > 0 || !tiles.empty()) {
+    s = make_tc_maps(q, total_q, num_q_heads, k_cache, v_cache, num_blocks, num_kv_heads, maps);
+    if (s != PA_OK) return s;
+  }
 
   if (P > 0) {
     pa::PrefixParams xp;
@@ -346,10 +399,10 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     xp.num_q_heads = num_q_heads;
     xp.num_kv_heads = num_kv_heads;
     xp.prefix_keys = P * pa::kPage;
-    // about two CTAs per SM over chunks x kv heads x query tiles
+    // about one CTA per SM over chunks x kv heads x query tiles
     const int64_t groups = prefix_qtiles(total_q) * num_kv_heads;
     int n_chunks = (int)std::min<int64_t>(prefix_chunk_cap(total_q, num_kv_heads, P),
-                                          std::max<int64_t>(1, (2 * sm_count() + groups - 1) / groups));
+                                          std::max<int64_t>(1, (sm_count() + groups - 1) / groups));
     const int64_t tiles = ((int64_t)xp.prefix_keys + kPrefixKeyTile - 1) / kPrefixKeyTile;
     xp.chunk_keys = (int32_t)((tiles + n_chunks - 1) / n_chunks * kPrefixKeyTile);
     n_chunks = (int)((xp.prefix_keys + xp.chunk_keys - 1) / xp.chunk_keys);
@@ -359,7 +412,7 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     xp.prefix_o = prefix_o;
     xp.prefix_lse = prefix_lse;
     xp.err = err;
-    s = run_launch(PA_KERNEL_PREFIX, "prefix", stream, [&] { return pa::launch_prefix(xp, n_chunks, stream); });
+    s = run_launch(PA_KERNEL_PREFIX, "prefix", stream, [&] { return pa::launch_prefix(xp, n_chunks, maps, stream); });
     if (s != PA_OK) return s;
     if (n_chunks > 1) {
       s = run_launch(PA_KERNEL_PREFIX_MERGE, "prefix_merge", stream,
@@ -397,7 +450,7 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
         items.req[i] = item_req[idx];
         items.q_start[i] = item_q0[idx];
       }
-      s = run_launch(PA_KERNEL_PREFILL, "prefill", stream, [&] { return pa::launch_prefill(pp, items, stream); });
+      s = run_launch(PA_KERNEL_PREFILL, "prefill", stream, [&] { return pa::launch_prefill(pp, items, maps, stream); });
       if (s != PA_OK) return s;
     }
   }

@@ -1,5 +1,6 @@
-// Tensor-core tiles of paged attention: chunked-prefill rows (qo_len > 1)
-// and the shared-prefix pass of a batch whose requests share leading pages.
+// Tensor-core tiles of paged attention on the 5th-generation tensor cores:
+// chunked-prefill rows (qo_len > 1) and the shared-prefix pass of a batch
+// whose requests share leading pages.
 //
 // What is computed: a chunk of c new tokens after h cached ones; new token j
 // sits at position h + j and attends to keys 0 .. h + j ("Inference
@@ -11,313 +12,487 @@
 // for all queries together (no mask: every prefix key is visible to every
 // query) and merged with each request's own part by log-sum-exp.
 //
-// Design: both products are dense contractions (QK^T and PV), so they run on
-// the tensor cores (mma.sync m16n8k16, bf16 inputs, fp32 accumulators).
-//   * One CTA per (16-query tile, kv head [, key chunk]).  The 4 q heads of
-//     the GQA group are packed into the M dimension: 16 tokens x 4 heads = 64
-//     rows, so every K/V tile staged in shared memory serves all four heads.
-//   * 4 warps x 16 rows; each warp keeps its Q fragments in registers for
-//     the whole key loop.
-//   * K/V tiles of 64 keys (4 pages) are staged with cp.async (16 B per
-//     request) into XOR-swizzled rows (16-byte chunk c of row r lands at
-//     chunk c ^ (r & 7)), double buffered, so ldmatrix reads are
-//     conflict-free.
-//   * Online softmax in the log2 domain on the fp32 S fragments; P is
-//     rounded to bf16 for the PV product.  Only tiles that cross the causal
-//     diagonal or the end of the key range evaluate a mask.
+// Design (QK^T and PV are dense contractions):
+//   * One CTA per (32-query tile, kv head [, key chunk]).  The 4 q heads of
+//     the GQA group are packed into the M dimension: 32 tokens x 4 heads =
+//     128 rows = the M of one tcgen05.mma, so every K/V tile serves all four
+//     heads.  Keys go in tiles of 128 (8 pages).
+//   * Warp roles: warps 4 and 6 issue tiled TMA copies (Q once; per key tile
+//     the two 64-dim halves of each page's K slab, resp. V slab, 128-byte
+//     swizzled, into 2-stage K and V rings: a K stage is refilled as soon as
+//     its S product is done); warp 5 owns the tensor memory and one of its
+//     threads issues the MMAs; warps 0-3 run the softmax, one thread per row
+//     (tensor-memory lane = row).
+//   * Tensor memory: two S buffers of 128 fp32 columns and the O accumulator
+//     (128 columns).  S of tile j + 1 is queued before PV of tile j, so it
+//     runs while the softmax of tile j does; PV of tile j follows the
+//     softmax that wrote its P (bf16, to a double-buffered shared tile in the
+//     layout the MMA reads).
+//   * Online softmax in the log2 domain; the running max is re-based (and O
+//     in tensor memory rescaled) only when it grows by more than 2^8, so P
+//     stays below 256 and the rescale is rare.
+//   * Every wait is bounded; on a timeout the CTA records the error, lets
+//     its copies and MMAs finish (bounded), frees its tensor memory and
+//     returns.
 #include <math.h>
+#include <stddef.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace pa {
 namespace {
 
-constexpr int kQT = kPrefillQTile;     // query tokens per CTA
-constexpr int kRows = kQT * kGroup;    // 64 MMA rows
-constexpr int kKT = 64;                // keys per tile
-constexpr int kThreads = 128;
-constexpr int kChunksPerRow = kHeadDim * 2 / 16;  // 16 chunks of 16 B
+using namespace tc;
 
-struct __align__(128) PrefillSmem {
-  uint16_t q[kRows * kHeadDim];
-  uint16_t k[2][kKT * kHeadDim];
-  uint16_t v[2][kKT * kHeadDim];
+constexpr int kTok = kPrefillQTile;              // 32 query tokens per CTA
+constexpr int kRows = kTok * kGroup;             // 128 MMA rows
+constexpr int kKeys = kTcKeyTile;                // 128 keys per tile
+constexpr int kPagesPerTile = kKeys / kPage;     // 8
+constexpr int kHalf = 128 * 128;                 // 128 rows x 64 bf16 (one 64-column half): 16 KiB
+constexpr int kTileBytes = 2 * kHalf;            // 32 KiB
+constexpr int kPageHalfBytes = kPage * 128;      // one page's rows of one half: 2 KiB
+constexpr int kStages = 2;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kKWarp = 4, kMmaWarp = 5, kVWarp = 6;  // Q/K copies, MMA issue, V copies
+constexpr int kThreads = 7 * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // S buffers at columns 0 and 128
+constexpr uint32_t kColO = 256;  // O accumulator
+constexpr float kRescaleSlack = 8.f;
+constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, kKeys, false);     // Q (K-major) x K^T (K-major)
+constexpr uint32_t kIdescO = idesc_bf16_f32(kRows, kHeadDim, true);   // P (K-major) x V (MN-major)
+static_assert(kRows == 128 && kKeys == 128, "tile shape");
+
+struct __align__(1024) TcSmem {
+  uint8_t q[kTileBytes];
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  uint8_t p[2][kTileBytes];
+  uint64_t bar_q;
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
+  uint64_t k_empty[kStages];
+  uint64_t v_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+};
+constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;  // + slack to align the base to 1024 B
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(offsetof(TcSmem, p) + 2 * kTileBytes <= sizeof(TcSmem), "staging area = both P tiles (64 KiB)");
+
+__device__ __forceinline__ TcSmem& tc_smem() {
+  extern __shared__ uint8_t tc_smem_raw[];
+  return *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+}
+
+// Bounded wait that also gives up once another thread of the CTA has given
+// up (the abort flag).
+__device__ __forceinline__ bool tc_wait(TcSmem& sm, uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*reinterpret_cast<volatile int*>(&sm.abort)) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        record_error(err, PA_ERR_DEVICE_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// One CTA's work: rows = tokens tok0 .. tok0 + nq - 1 of q (4 heads of kv
+// head kvh each) against keys [k_lo, k_hi) of one block-table row; k_lo is a
+// multiple of 16.  Causal: token l (position pos0 + l) sees keys <= pos0 + l.
+struct TcJob {
+  int32_t tok0;
+  int32_t nq;
+  int32_t kvh;
+  int32_t k_lo;
+  int32_t k_hi;
+  int32_t pos0;
+  const int32_t* table;
 };
 
-// element offset of 16-byte chunk `ch` of row `row` in a swizzled tile
-__device__ __forceinline__ int swz(int row, int ch) { return (row * kChunksPerRow + (ch ^ (row & 7))) * 8; }
+// Runs the tile.  Each softmax thread calls `stage(row, o, m, l, smem)` with
+// its row's unnormalised O (4 x 32 fp32), running max (log2 domain) and
+// sum, to leave its output row in the 64 KiB staging area `smem`; after a
+// barrier of the softmax warps each of their threads calls `store(t, smem)`
+// (t = 0 .. 127) to copy the staged rows out with contiguous stores.
+template <bool kCausal, class Stage, class Store>
+__device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, int num_kv_heads, int64_t num_blocks,
+                                         float scale_log2, int* err, Stage&& stage, Store&& store) {
+  TcSmem& sm = tc_smem();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = (job.k_hi - job.k_lo + kKeys - 1) / kKeys;
+  const int first_page = job.k_lo / kPage;
+  const int last_page = (job.k_hi - 1) / kPage;
+  const bool is_producer = warp == kKWarp || warp == kVWarp;
+  const bool is_k = warp == kKWarp;
 
-__device__ __forceinline__ void ldsm_x4(uint32_t* r, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_addr(p)));
-}
-__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// The 64 rows of one CTA (tokens tok0 .. tok0 + nq - 1 of q, 4 heads of kv
-// head kvh) against keys [k_lo, k_hi) of one block table; k_lo is a multiple
-// of 16.  Causal: the row of token l (position pos0 + l) sees keys <= that
-// position.  Leaves per thread the O fragments of its two rows (gq, gq + 8 of
-// the warp's 16) and their running max (log2 domain) and partial sum.
-template <bool kCausal>
-__device__ __forceinline__ void attend_rows(PrefillSmem& sm, const uint16_t* q, int64_t tok0, int nq, int num_q_heads,
-                                            int kvh, const uint16_t* k_cache, const uint16_t* v_cache,
-                                            int num_kv_heads, int64_t num_blocks, const int32_t* table, int k_lo,
-                                            int k_hi, int pos0, float scale_log2, int* err, float (&o)[16][4],
-                                            float (&m_run)[2], float (&l_run)[2]) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = (k_hi - k_lo + kKT - 1) / kKT;
-  const int last_page = (k_hi - 1) / kPage;
-
-  // Q: row m = 4 * token + head-in-group; invalid tokens are zero rows.
-#pragma unroll
-  for (int it = 0; it < kRows * kChunksPerRow / kThreads; ++it) {
-    const int ci = tid + it * kThreads;
-    const int row = ci / kChunksPerRow, ch = ci % kChunksPerRow;
-    const int tokl = row >> 2, g = row & 3;
-    uint16_t* dst = sm.q + swz(row, ch);
-    if (tokl < nq) {
-      cp_async16(dst, q + ((size_t)(tok0 + tokl) * num_q_heads + kvh * kGroup + g) * kHeadDim + ch * 8);
-    } else {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+  // Block ids are read four tiles at a time, one group ahead: lane l of a
+  // producer warp holds the pool row of page l % 8 of tile 4 g + l / 8.
+  auto load_group = [&](int g) -> int {
+    const int t = 4 * g + (lane >> 3);
+    if (t >= n_tiles) return 0;
+    // pages past the range repeat the last page (finite data; masked)
+    const int page = min(first_page + t * kPagesPerTile + (lane & 7), last_page);
+    int32_t b = job.table[page];
+    if (b < 0 || b >= num_blocks) {
+      if (is_k) record_error(err, PA_ERR_DEVICE_INDEX);
+      b = 0;
     }
-  }
-
-  auto load_kv = [&](int kt, int buf) {
-#pragma unroll
-    for (int it = 0; it < kKT * kChunksPerRow / kThreads; ++it) {
-      const int ci = tid + it * kThreads;
-      const int row = ci / kChunksPerRow, ch = ci % kChunksPerRow;
-      // keys past the range read the last page again (finite data, masked)
-      const int page = min((k_lo + kt * kKT) / kPage + row / kPage, last_page);
-      int32_t b = table[page];
-      if (b < 0 || b >= num_blocks) {
-        record_error(err, PA_ERR_DEVICE_INDEX);
-        b = 0;
-      }
-      const size_t src = (((size_t)b * num_kv_heads + kvh) * kPage + (row % kPage)) * kHeadDim + ch * 8;
-      cp_async16(sm.k[buf] + swz(row, ch), k_cache + src);
-      cp_async16(sm.v[buf] + swz(row, ch), v_cache + src);
-    }
+    return (b * num_kv_heads + job.kvh) * kPage;
   };
-  load_kv(0, 0);
-  cp_async_commit();
-
-  uint32_t qa[kHeadDim / 16][4];
-#pragma unroll
-  for (int i = 0; i < kHeadDim / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  m_run[0] = m_run[1] = -INFINITY;
-  l_run[0] = l_run[1] = 0.f;
-  const int gq = lane >> 2, tq = lane & 3;
-  // positions of this thread's two rows (gq and gq + 8 of the warp's 16)
-  const int row_pos[2] = {pos0 + ((warp * 16 + gq) >> 2), pos0 + ((warp * 16 + gq + 8) >> 2)};
-
-  for (int kt = 0; kt < n_tiles; ++kt) {
-    const int buf = kt & 1;
-    if (kt + 1 < n_tiles) load_kv(kt + 1, buf ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (kt == 0) {
-      const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-      for (int kk = 0; kk < kHeadDim / 16; ++kk)
-        ldsm_x4(qa[kk], sm.q + swz(warp * 16 + (mi & 1) * 8 + ri, 2 * kk + (mi >> 1)));
-    }
-
-    // S = Q K^T for 16 rows x 64 keys
-    float s[kKT / 8][4];
-#pragma unroll
-    for (int i = 0; i < kKT / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-    {
-      const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-#pragma unroll
-        for (int np = 0; np < kKT / 16; ++np) {
-          uint32_t b[4];
-          ldsm_x4(b, sm.k[buf] + swz(16 * np + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)));
-          mma16816(s[2 * np], qa[kk], b[0], b[1]);
-          mma16816(s[2 * np + 1], qa[kk], b[2], b[3]);
-        }
-      }
-    }
-
-    // scale, mask (only where the tile crosses the diagonal or the range end)
-    const int kbase = k_lo + kt * kKT;
-    const bool need_mask = (kCausal && kbase + kKT - 1 > pos0) || (kbase + kKT > k_hi);
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < kKT / 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = s[nt][e] * scale_log2;
-        if (need_mask) {
-          const int key = kbase + nt * 8 + 2 * tq + (e & 1);
-          if (key >= k_hi || (kCausal && key > row_pos[e >> 1])) x = -INFINITY;
-        }
-        s[nt][e] = x;
-        mx[e >> 1] = fmaxf(mx[e >> 1], x);
-      }
-    }
-    float corr[2], mref[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-      const float m_new = fmaxf(m_run[h], mx[h]);
-      mref[h] = (m_new == -INFINITY) ? 0.f : m_new;
-      corr[h] = exp2f(m_run[h] - mref[h]);
-      m_run[h] = m_new;
-      l_run[h] *= corr[h];
-    }
-#pragma unroll
-    for (int i = 0; i < kHeadDim / 8; ++i) {
-      o[i][0] *= corr[0];
-      o[i][1] *= corr[0];
-      o[i][2] *= corr[1];
-      o[i][3] *= corr[1];
-    }
-    uint32_t pa[kKT / 16][4];
-#pragma unroll
-    for (int nt = 0; nt < kKT / 8; ++nt) {
-      const float p0 = exp2f(s[nt][0] - mref[0]);
-      const float p1 = exp2f(s[nt][1] - mref[0]);
-      const float p2 = exp2f(s[nt][2] - mref[1]);
-      const float p3 = exp2f(s[nt][3] - mref[1]);
-      l_run[0] += p0 + p1;
-      l_run[1] += p2 + p3;
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
-    }
-
-    // O += P V
-    {
-      const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-      for (int kk = 0; kk < kKT / 16; ++kk) {
-#pragma unroll
-        for (int dp = 0; dp < kHeadDim / 16; ++dp) {
-          uint32_t b[4];
-          ldsm_x4_t(b, sm.v[buf] + swz(16 * kk + (mi & 1) * 8 + ri, 2 * dp + (mi >> 1)));
-          mma16816(o[2 * dp], pa[kk], b[0], b[1]);
-          mma16816(o[2 * dp + 1], pa[kk], b[2], b[3]);
-        }
-      }
-    }
-    __syncthreads();  // buffer `buf` is refilled by the next iteration
+  int grp_cur = 0, grp_next = 0;
+  if (is_producer) {  // in flight during the set-up below
+    grp_cur = load_group(0);
+    grp_next = load_group(1);
   }
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+
+  if (is_k && lane == 0) {
+    mbar_init(&sm.bar_q, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.p_full[b], kSoftmaxWarps * 32);
+    }
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    // Q first: its copy overlaps the rest of the set-up
+    prefetch_tensormap(&maps.q);
+    mbar_arrive_expect_tx(&sm.bar_q, kTileBytes);
+    tma_load_3d(sm.q, &maps.q, 0, job.kvh * kGroup, job.tok0, &sm.bar_q);
+    tma_load_3d(sm.q + kHalf, &maps.q, 64, job.kvh * kGroup, job.tok0, &sm.bar_q);
   }
+  if (warp == kMmaWarp) tmem_alloc(&sm.tmem, kTmemCols);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sm.tmem;
+
+  if (is_producer) {
+    // ----------------------------------------------------------- producers
+    // warp kKWarp: Q (above), then the K ring; warp kVWarp: the V ring.  A K
+    // stage is free once its S product is done, a V stage once its PV is.
+    const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+    uint64_t* full = is_k ? sm.k_full : sm.v_full;
+    uint64_t* empty = is_k ? sm.k_empty : sm.v_empty;
+    int last_issued[kStages] = {-1, -1};
+    if (lane == 0) prefetch_tensormap(map);
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j & (kStages - 1);
+      if (j >= kStages && !__all_sync(0xffffffffu, tc_wait(sm, &empty[s], ((j / kStages) - 1) & 1, err))) break;
+      if (j > 0 && (j & 3) == 0) {
+        grp_cur = grp_next;
+        grp_next = load_group((j >> 2) + 1);
+      }
+      const int row = __shfl_sync(0xffffffffu, grp_cur, ((j & 3) << 3) + (lane & 7));
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], kTileBytes);
+      __syncwarp();
+      uint8_t* dst = is_k ? sm.k[s] : sm.v[s];
+      if (lane < kPagesPerTile) {
+        const int off = lane * kPageHalfBytes;
+        tma_load_2d(dst + off, map, 0, row, &full[s]);
+        tma_load_2d(dst + kHalf + off, map, 64, row, &full[s]);
+      }
+      last_issued[s] = j;
+    }
+    if (*reinterpret_cast<volatile int*>(&sm.abort) && lane == 0) {
+      // let the copies in flight land before the CTA leaves (bounded)
+      if (is_k) mbar_wait_bounded(&sm.bar_q, 0);
+      for (int s = 0; s < kStages; ++s)
+        if (last_issued[s] >= 0) mbar_wait_bounded(&full[s], (last_issued[s] / kStages) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t qb = smem_addr(sm.q);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j & (kStages - 1);
+        if (!tc_wait(sm, &sm.k_full[s], (j / kStages) & 1, err)) return false;
+        fence_after_sync();
+        const uint32_t kb = smem_addr(sm.k[s]);
+        const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * kKeys;
+#pragma unroll
+        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;  // 64-dim half, 16-dim step in it
+          mma_bf16(d, desc_sw128(qb + off, 16, 1024), desc_sw128(kb + off, 16, 1024), kIdescS, ks > 0);
+        }
+        commit(&sm.s_full[j & 1]);
+        commit(&sm.k_empty[s]);
+        return true;
+      };
+      // S runs one tile ahead: S(j + 1) is queued before PV(j), which waits
+      // for the softmax of tile j
+      bool ok = tc_wait(sm, &sm.bar_q, 0, err) && issue_s(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        if (j + 1 < n_tiles && !issue_s(j + 1)) break;
+        const int s = j & (kStages - 1);
+        ok = tc_wait(sm, &sm.p_full[j & 1], (j >> 1) & 1, err) && tc_wait(sm, &sm.v_full[s], (j / kStages) & 1, err);
+        if (!ok) break;
+        fence_after_sync();
+        const uint32_t pb = smem_addr(sm.p[j & 1]), vb = smem_addr(sm.v[s]);
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks) {
+          const uint32_t pa = pb + (ks >> 2) * kHalf + (ks & 3) * 32;  // 64-key half, 16-key step
+          const uint32_t va = vb + ks * 2 * 1024;                      // 16 keys = two 8-row groups
+          mma_bf16(tmem + kColO, desc_sw128(pa, 16, 1024), desc_sw128(va, kHalf, 1024), kIdescO,
+                   (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        commit(&sm.v_empty[s]);
+        commit(&sm.o_done);
+      }
+      // every MMA issued has completed before the CTA frees its tensor memory
+      commit(&sm.drain);
+      mbar_wait_bounded(&sm.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int r = warp * 32 + lane;  // row = 4 * token + head in group
+    const int pos = job.pos0 + (r >> 2);
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.s_full[j & 1], (j >> 1) & 1, err));
+      if (!ok) break;
+      fence_after_sync();
+      // scores of this row, scaled into the log2 domain in pairs
+      float2 x[64];
+      {
+        uint32_t raw[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32_async(lane_base + kColS + (uint32_t)(j & 1) * kKeys + 32 * c, raw[c]);
+        tmem_wait_ld(raw[0], raw[1], raw[2], raw[3]);
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          x[i] = __fmul2_rn(make_float2(__uint_as_float(raw[i >> 4][(2 * i) & 31]),
+                                        __uint_as_float(raw[i >> 4][(2 * i + 1) & 31])),
+                            sc2);
+      }
+      const int kbase = job.k_lo + j * kKeys;
+      const bool need_mask = (kCausal && kbase + kKeys - 1 > job.pos0) || (kbase + kKeys > job.k_hi);
+      if (need_mask) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const int key = kbase + 2 * i;
+          if (key >= job.k_hi || (kCausal && key > pos)) x[i].x = -INFINITY;
+          if (key + 1 >= job.k_hi || (kCausal && key + 1 > pos)) x[i].y = -INFINITY;
+        }
+      }
+      float mx8[8];  // 8 independent max chains
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], fmaxf(x[i].x, x[i].y));
+      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const bool grow = mt > m_run + kRescaleSlack;  // always true for the first finite max
+      float corr = 1.f;
+      if (grow) {
+        corr = exp2f(m_run - mt);  // m_run = -inf -> 0
+        l_run *= corr;
+        m_run = mt;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O holds tiles < j: wait for the PV of tile j - 1, then rescale
+        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.o_done, (j - 1) & 1, err));
+        if (!ok) break;
+        fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(lane_base + kColO + 32 * c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tmem_st32(lane_base + kColO + 32 * c, o);
+        }
+      }
+      const float nm = (m_run == -INFINITY) ? 0.f : -m_run;
+      const float2 nm2 = make_float2(nm, nm);
+      float2 ls4[4];  // 4 independent pair-sum chains
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ls4[i] = make_float2(0.f, 0.f);
+      uint8_t* prow = sm.p[j & 1] + r * 128;
+#pragma unroll
+      for (int c = 0; c < kKeys / 8; ++c) {  // 8 keys = one 16-byte chunk
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 d = __fadd2_rn(x[4 * c + i], nm2);
+          const float2 e = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+          ls4[i] = __fadd2_rn(ls4[i], e);
+          w[i] = pack_bf16x2(e.x, e.y);
+        }
+        // 64-key half c / 8, chunk c % 8 of the row, 128-byte swizzle
+        *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      const float2 l2 = __fadd2_rn(__fadd2_rn(ls4[0], ls4[1]), __fadd2_rn(ls4[2], ls4[3]));
+      l_run += l2.x + l2.y;
+      fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
+      fence_before_sync();       // tensor-memory reads / writes above precede the arrive
+      mbar_arrive(&sm.p_full[j & 1]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.o_done, (n_tiles - 1) & 1, err));
+    if (ok) {
+      fence_after_sync();
+      float o[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kColO + 32 * c, o[c]);
+      // the P tiles are free (every PV is done): they are the staging area
+      stage(r, o, m_run, l_run, sm.p[0]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
+    if (!*reinterpret_cast<volatile int*>(&sm.abort)) store(r, sm.p[0]);
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-    prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillItems items) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw);
+// Chunked-prefill rows: grid (work item, kv head); item = (request, first
+// query of a 32-token tile).  Keys [kv_key_offset, position of the tile's
+// last query] with the causal mask; the shared-prefix partial, if given, is
+// folded in before the bf16 rounding.
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillItems items,
+                   const __grid_constant__ TcMaps maps) {
   const int r = items.req[blockIdx.x];
   const int j0 = items.q_start[blockIdx.x];
-  const int kvh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
   const int qo0 = p.qo_indptr[r];
   const int c = p.qo_indptr[r + 1] - qo0;
   const int L = p.seq_lens[r];
-  const int nq = min(kQT, c - j0);  // valid query tokens in this tile
-  const int pos0 = L - c + j0;      // position of the tile's first query
-  const int kv_end = pos0 + nq;     // keys [0, kv_end) are visible to some row
-  const int32_t* table = p.block_tables + (size_t)r * p.max_blocks_per_req;
-
-  float o[kHeadDim / 8][4], m_run[2], l_run[2];
-  attend_rows<true>(sm, p.q, (int64_t)qo0 + j0, nq, p.num_q_heads, kvh, p.k_cache, p.v_cache, p.num_kv_heads,
-                    p.num_blocks, table, p.kv_key_offset, kv_end, pos0, p.scale_log2, p.err, o, m_run, l_run);
-
-  // normalise, fold in the shared prefix (if any) and write the valid rows
-  const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int row = warp * 16 + gq + 8 * h;
-    const int tokl = row >> 2;
-    if (tokl >= nq) continue;
-    const int head = kvh * kGroup + (row & 3);
-    const size_t orow = (size_t)(qo0 + j0 + tokl) * p.num_q_heads + head;
-    float lse2 = l_run[h] > 0.f ? m_run[h] + log2f(l_run[h]) : -INFINITY;
-    float ws = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f, wp = 0.f;
-    const float* po = nullptr;
-    if (p.prefix_o) {
-      float wo;
-      lse2 = merge2_weights(lse2, p.prefix_lse[orow], wo, wp);
-      ws *= wo;
-      po = p.prefix_o + orow * kHeadDim + 2 * tq;
-    }
-#pragma unroll
-    for (int nt = 0; nt < kHeadDim / 8; ++nt) {
-      float x0 = o[nt][2 * h] * ws, x1 = o[nt][2 * h + 1] * ws;
-      if (po) {
-        const float2 y = *reinterpret_cast<const float2*>(po + nt * 8);
-        x0 = fmaf(wp, y.x, x0);
-        x1 = fmaf(wp, y.y, x1);
-      }
-      *reinterpret_cast<uint32_t*>(p.out + orow * kHeadDim + nt * 8 + 2 * tq) = pack_bf16x2(x0, x1);
-    }
-    if (p.lse && tq == 0) p.lse[orow] = lse2 * kLn2;
+  TcJob job;
+  job.tok0 = qo0 + j0;
+  job.nq = min(kTok, c - j0);
+  job.kvh = blockIdx.y;
+  job.pos0 = L - c + j0;
+  job.k_lo = p.kv_key_offset;
+  job.k_hi = job.pos0 + job.nq;
+  job.table = p.block_tables + (size_t)r * p.max_blocks_per_req;
+  // metadata that differ from the host plan: record and leave (uniformly,
+  // before any barrier or tensor memory is touched)
+  if (job.nq <= 0 || job.k_hi <= job.k_lo || (job.k_hi - 1) / kPage >= p.max_blocks_per_req) {
+    if (threadIdx.x == 0) record_error(p.err, PA_ERR_DEVICE_INDEX);
+    return;
   }
+  // staged bf16 rows: 256 B per row, 16-byte chunk c at c ^ (row & 15)
+  run_tile<true>(
+      job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err,
+      [&](int row, float (&o)[4][32], float m, float l, uint8_t* stg) {
+        const size_t orow = (size_t)(job.tok0 + (row >> 2)) * p.num_q_heads + job.kvh * kGroup + (row & 3);
+        const bool valid = (row >> 2) < job.nq;
+        float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
+        float ws = l > 0.f ? 1.f / l : 0.f, wp = 0.f;
+        const float* po = nullptr;
+        if (p.prefix_o && valid) {
+          float wo;
+          lse2 = merge2_weights(lse2, p.prefix_lse[orow], wo, wp);
+          ws *= wo;
+          po = p.prefix_o + orow * kHeadDim;
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < kHeadDim / 8; ++c8) {
+          float y[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i] = o[c8 >> 2][(c8 & 3) * 8 + i] * ws;
+          if (po) {
+            const float4 a = *reinterpret_cast<const float4*>(po + 8 * c8);
+            const float4 b = *reinterpret_cast<const float4*>(po + 8 * c8 + 4);
+            y[0] = fmaf(wp, a.x, y[0]);
+            y[1] = fmaf(wp, a.y, y[1]);
+            y[2] = fmaf(wp, a.z, y[2]);
+            y[3] = fmaf(wp, a.w, y[3]);
+            y[4] = fmaf(wp, b.x, y[4]);
+            y[5] = fmaf(wp, b.y, y[5]);
+            y[6] = fmaf(wp, b.z, y[6]);
+            y[7] = fmaf(wp, b.w, y[7]);
+          }
+          *reinterpret_cast<uint4*>(stg + row * 256 + ((c8 ^ (row & 15)) << 4)) =
+              make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                         pack_bf16x2(y[6], y[7]));
+        }
+        if (p.lse && valid) p.lse[orow] = lse2 * kLn2;
+      },
+      [&](int t, const uint8_t* stg) {
+        // 16 consecutive threads write one 256-byte row; the 4 rows of a
+        // token are adjacent in out, so a warp writes 2 KiB contiguously
+#pragma unroll 4
+        for (int i = 0; i < kRows * 16 / (kSoftmaxWarps * 32); ++i) {
+          const int L = i * kSoftmaxWarps * 32 + t;
+          const int row = L >> 4, c = L & 15;
+          if ((row >> 2) >= job.nq) continue;
+          const size_t orow = (size_t)(job.tok0 + (row >> 2)) * p.num_q_heads + job.kvh * kGroup + (row & 3);
+          *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * c) =
+              *reinterpret_cast<const uint4*>(stg + row * 256 + ((c ^ (row & 15)) << 4));
+        }
+      });
 }
 
-// Shared-prefix pass: grid (key chunk, kv head, 16-token tile of all the
-// batch's queries).  Each CTA leaves a chunk partial (prefix_merge_kernel
-// merges them); with a single chunk it writes the prefix partial itself.
-__global__ void __launch_bounds__(kThreads, 2) prefix_kernel(const PrefixParams p) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw);
-  const int chunk = blockIdx.x, kvh = blockIdx.y, qt = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tok0 = qt * kQT;
-  const int nq = min(kQT, p.total_q - tok0);
-  const int k_lo = chunk * p.chunk_keys;
-  const int k_hi = min(p.prefix_keys, k_lo + p.chunk_keys);
-  const int32_t* table = p.block_tables + (size_t)p.table_row * p.max_blocks_per_req;
-
-  float o[kHeadDim / 8][4], m_run[2], l_run[2];
-  attend_rows<false>(sm, p.q, tok0, nq, p.num_q_heads, kvh, p.k_cache, p.v_cache, p.num_kv_heads, p.num_blocks,
-                     table, k_lo, k_hi, 0, p.scale_log2, p.err, o, m_run, l_run);
-
-  // chunk partial (normalised o, log2 lse per row); a single chunk is the
-  // prefix partial itself
+// Shared-prefix pass: grid (key chunk, kv head, 32-token tile of all the
+// batch's queries), no mask.  Each CTA leaves a chunk partial (normalised o,
+// log2 lse) for prefix_merge_kernel; with a single chunk it writes the
+// prefix partial itself.
+__global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams p, const __grid_constant__ TcMaps maps) {
+  TcJob job;
+  job.tok0 = blockIdx.z * kTok;
+  job.nq = min(kTok, p.total_q - job.tok0);
+  job.kvh = blockIdx.y;
+  job.pos0 = 0;
+  job.k_lo = blockIdx.x * p.chunk_keys;
+  job.k_hi = min(p.prefix_keys, job.k_lo + p.chunk_keys);
+  job.table = p.block_tables + (size_t)p.table_row * p.max_blocks_per_req;
+  if (job.nq <= 0 || job.k_hi <= job.k_lo) return;  // not planned on the host
   const bool direct = gridDim.x == 1;
-  float* dst_o = direct ? p.prefix_o : p.chunk_o;
-  float* dst_lse = direct ? p.prefix_lse : p.chunk_lse;
-  const int gq = lane >> 2, tq = lane & 3;
-  const size_t chunk_stride = (size_t)p.total_q * p.num_q_heads;
+  float* dst_o = direct ? p.prefix_o : p.chunk_o + (size_t)blockIdx.x * p.total_q * p.num_q_heads * kHeadDim;
+  float* dst_lse = direct ? p.prefix_lse : p.chunk_lse + (size_t)blockIdx.x * p.total_q * p.num_q_heads;
+  // staged fp32 rows: 512 B per row, 16-byte chunk c at c ^ (row & 31)
+  run_tile<false>(
+      job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err,
+      [&](int row, float (&o)[4][32], float m, float l, uint8_t* stg) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int row = warp * 16 + gq + 8 * h;
-    const int tokl = row >> 2;
-    if (tokl >= nq) continue;
-    const size_t orow = (size_t)(tok0 + tokl) * p.num_q_heads + kvh * kGroup + (row & 3);
-    const size_t prow = (size_t)chunk * chunk_stride + orow;
-    const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
-#pragma unroll
-    for (int nt = 0; nt < kHeadDim / 8; ++nt)
-      *reinterpret_cast<float2*>(dst_o + prow * kHeadDim + nt * 8 + 2 * tq) =
-          make_float2(o[nt][2 * h] * inv, o[nt][2 * h + 1] * inv);
-    if (tq == 0) dst_lse[prow] = l_run[h] > 0.f ? m_run[h] + log2f(l_run[h]) : -INFINITY;
-  }
+        for (int c4 = 0; c4 < kHeadDim / 4; ++c4)
+          *reinterpret_cast<float4*>(stg + row * 512 + ((c4 ^ (row & 31)) << 4)) =
+              make_float4(o[c4 >> 3][(c4 & 7) * 4] * inv, o[c4 >> 3][(c4 & 7) * 4 + 1] * inv,
+                          o[c4 >> 3][(c4 & 7) * 4 + 2] * inv, o[c4 >> 3][(c4 & 7) * 4 + 3] * inv);
+        if ((row >> 2) < job.nq) {
+          const size_t orow = (size_t)(job.tok0 + (row >> 2)) * p.num_q_heads + job.kvh * kGroup + (row & 3);
+          dst_lse[orow] = l > 0.f ? m + log2f(l) : -INFINITY;
+        }
+      },
+      [&](int t, const uint8_t* stg) {
+#pragma unroll 4
+        for (int i = 0; i < kRows * 32 / (kSoftmaxWarps * 32); ++i) {
+          const int L = i * kSoftmaxWarps * 32 + t;
+          const int row = L >> 5, c = L & 31;
+          if ((row >> 2) >= job.nq) continue;
+          const size_t orow = (size_t)(job.tok0 + (row >> 2)) * p.num_q_heads + job.kvh * kGroup + (row & 3);
+          *reinterpret_cast<float4*>(dst_o + orow * kHeadDim + 4 * c) =
+              *reinterpret_cast<const float4*>(stg + row * 512 + ((c ^ (row & 31)) << 4));
+        }
+      });
 }
 
 // Merge of the prefix pass's key-chunk partials: one warp per (query token,
@@ -371,34 +546,32 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefix_merge_kernel(const Pr
 bool g_prefill_attr_set[64] = {};
 bool g_prefix_attr_set[64] = {};
 
-}  // namespace
-
-cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, cudaStream_t stream) {
-  if (items.count <= 0) return cudaSuccess;
+cudaError_t set_smem_attr(const void* fn, bool* done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !g_prefill_attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(PrefillSmem));
-    if (e != cudaSuccess) return e;
-    g_prefill_attr_set[dev] = true;
-  }
-  dim3 grid(items.count, p.num_kv_heads);
-  prefill_kernel<<<grid, kThreads, sizeof(PrefillSmem), stream>>>(p, items);
+  if (dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess && dev < 64) done[dev] = true;
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
+                           cudaStream_t stream) {
+  if (items.count <= 0) return cudaSuccess;
+  cudaError_t e = set_smem_attr((const void*)prefill_kernel, g_prefill_attr_set);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<<<dim3(items.count, p.num_kv_heads), kThreads, kSmemBytes, stream>>>(p, items, maps);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, cudaStream_t stream) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream) {
+  cudaError_t e = set_smem_attr((const void*)prefix_kernel, g_prefix_attr_set);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !g_prefix_attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(PrefillSmem));
-    if (e != cudaSuccess) return e;
-    g_prefix_attr_set[dev] = true;
-  }
-  dim3 grid(n_chunks, p.num_kv_heads, (p.total_q + kQT - 1) / kQT);
-  prefix_kernel<<<grid, kThreads, sizeof(PrefillSmem), stream>>>(p);
+  dim3 grid(n_chunks, p.num_kv_heads, (p.total_q + kTok - 1) / kTok);
+  prefix_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, maps);
   return cudaGetLastError();
 }
 

@@ -115,17 +115,20 @@ def test_shared_prefix_workspace_size():
     base = b.pa_attention_workspace_size(16, 16, 32, 128, 8447)
     assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 0) == base
     # + prefix partial (16 x 32 rows of 128 fp32) + its lse
-    # + 64 key-chunk partials (512-CTA bound / 8 kv heads) of the same rows
+    # + 48 key-chunk partials (one per 128-key tile; the 512-CTA bound / 8 kv heads is larger)
     rows = 16 * 32
     assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 384) == \
-        base + rows * 512 + rows * 4 + 64 * rows * 512 + 64 * rows * 4
-    # a 5-page prefix has two 64-key tiles, so at most two chunks
-    assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 5) == \
-        base + rows * 512 + rows * 4 + 2 * rows * 512 + 2 * rows * 4
-    # 64 query tiles x 8 kv heads fill the CTA bound: one chunk, no chunk partials
-    base2 = b.pa_attention_workspace_size(4, 1024, 32, 128, 3000)
+        base + rows * 512 + rows * 4 + 48 * rows * 512 + 48 * rows * 4
+    # a 5-page prefix is one 128-key tile: one chunk, no chunk partials
+    assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 5) == base + rows * 512 + rows * 4
+    # 64 query tiles of 32 tokens x 8 kv heads reach the CTA bound: one chunk
+    base2 = b.pa_attention_workspace_size(4, 2048, 32, 128, 3000)
+    assert b.pa_shared_prefix_workspace_size(4, 2048, 32, 128, 3000, 96) == \
+        base2 + 2048 * 32 * 512 + 2048 * 32 * 4
+    # 32 query tiles x 8 kv heads: two chunks
+    base3 = b.pa_attention_workspace_size(4, 1024, 32, 128, 3000)
     assert b.pa_shared_prefix_workspace_size(4, 1024, 32, 128, 3000, 96) == \
-        base2 + 1024 * 32 * 512 + 1024 * 32 * 4
+        base3 + 3 * (1024 * 32 * 512 + 1024 * 32 * 4)
     assert b.pa_shared_prefix_workspace_size(4, 4, 32, 128, 100, -1) == 0
 
 
