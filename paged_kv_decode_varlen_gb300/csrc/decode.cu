@@ -150,6 +150,10 @@ __device__ __forceinline__ float fold_prefix(float4& o, float lse2, const float*
 
 __global__ void __launch_bounds__(kThreads, 3)
     decode_kernel(const DecodeParams p, const __grid_constant__ DecodePlan plan) {
+  // No early launch of the next kernel: this grid is one wave sized to fill
+  // every SM, and CTAs of a dependent kernel arriving early would take slots
+  // its own CTAs need.  The next kernel is released as the CTAs exit.
+  pdl_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int b = blockIdx.x;
@@ -589,8 +593,7 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int gri
     if (e != cudaSuccess) return e;
     g_decode_attr_set[dev] = true;
   }
-  decode_kernel<<<grid, kThreads, sizeof(DecodeSmem), stream>>>(p, plan);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel, dim3(grid), dim3(kThreads), sizeof(DecodeSmem), stream, p, plan);
 }
 
 }  // namespace pa

@@ -18,6 +18,8 @@ constexpr int kThreads = 256;
 constexpr int kLanesPerRow = kHeadDim * 2 / 16;  // 16 x 16 B = 256 B
 
 __global__ void __launch_bounds__(kThreads) kv_append_kernel(const AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t rows = p.n_tokens * p.num_kv_heads;
   const int64_t stride = (int64_t)gridDim.x * (kThreads / kLanesPerRow);
   const int lane16 = threadIdx.x % kLanesPerRow;
@@ -49,8 +51,7 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
   const int rows_per_cta = kThreads / kLanesPerRow;
   int64_t grid = (rows + rows_per_cta - 1) / rows_per_cta;
   if (grid > 65535) grid = 65535;
-  kv_append_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3((unsigned)grid), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace pa

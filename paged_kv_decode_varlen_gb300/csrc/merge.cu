@@ -17,6 +17,8 @@ namespace {
 constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) merge_kernel(const MergeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int vecs_per_row = p.head_dim / 8;
   const int64_t n = p.rows * p.num_heads * vecs_per_row;
   for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kThreads) {
@@ -72,8 +74,7 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   int64_t grid = (n + kThreads - 1) / kThreads;
   if (grid > 65535 * 4) grid = 65535 * 4;
   if (grid < 1) grid = 1;
-  merge_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3((unsigned)grid), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace pa

@@ -378,6 +378,8 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillItems items,
                    const __grid_constant__ TcMaps maps) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int r = items.req[blockIdx.x];
   const int j0 = items.q_start[blockIdx.x];
   const int qo0 = p.qo_indptr[r];
@@ -455,6 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // log2 lse) for prefix_merge_kernel; with a single chunk it writes the
 // prefix partial itself.
 __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams p, const __grid_constant__ TcMaps maps) {
+  pdl_launch_dependents();
+  pdl_wait();
   TcJob job;
   job.tok0 = blockIdx.z * kTok;
   job.nq = min(kTok, p.total_q - job.tok0);
@@ -501,6 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
 // dims of up to 32 chunks at once and sums them with the broadcast weights.
 constexpr int kMergeWarps = 2;
 __global__ void __launch_bounds__(kMergeWarps * 32) prefix_merge_kernel(const PrefixParams p, int n_chunks) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int64_t rows = (int64_t)p.total_q * p.num_q_heads;
@@ -563,22 +569,21 @@ cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, co
   if (items.count <= 0) return cudaSuccess;
   cudaError_t e = set_smem_attr((const void*)prefill_kernel, g_prefill_attr_set);
   if (e != cudaSuccess) return e;
-  prefill_kernel<<<dim3(items.count, p.num_kv_heads), kThreads, kSmemBytes, stream>>>(p, items, maps);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel, dim3(items.count, p.num_kv_heads), dim3(kThreads), kSmemBytes, stream, p, items,
+                    maps);
 }
 
 cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream) {
   cudaError_t e = set_smem_attr((const void*)prefix_kernel, g_prefix_attr_set);
   if (e != cudaSuccess) return e;
   dim3 grid(n_chunks, p.num_kv_heads, (p.total_q + kTok - 1) / kTok);
-  prefix_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, maps);
-  return cudaGetLastError();
+  return launch_pdl(prefix_kernel, grid, dim3(kThreads), kSmemBytes, stream, p, maps);
 }
 
 cudaError_t launch_prefix_merge(const PrefixParams& p, int n_chunks, cudaStream_t stream) {
   const int64_t rows = (int64_t)p.total_q * p.num_q_heads;
-  prefix_merge_kernel<<<(unsigned)((rows + kMergeWarps - 1) / kMergeWarps), kMergeWarps * 32, 0, stream>>>(p, n_chunks);
-  return cudaGetLastError();
+  return launch_pdl(prefix_merge_kernel, dim3((unsigned)((rows + kMergeWarps - 1) / kMergeWarps)),
+                    dim3(kMergeWarps * 32), 0, stream, p, n_chunks);
 }
 
 }  // namespace pa
