@@ -124,6 +124,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// atomicAdd with acquire-release semantics at GPU scope: writes this thread
+// has made (or observed, e.g. through a CTA barrier) before it are visible to
+// a thread that reads the counter's result after it, and the reads that
+// follow it see what the earlier adders published.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Kernels are launched with programmatic stream serialization: each CTA of
 // the short kernels lets the next kernel of the stream be scheduled as soon

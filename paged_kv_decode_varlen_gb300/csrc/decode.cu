@@ -62,7 +62,7 @@ struct Item {        // one request's pages within this CTA's segment
   int32_t p0;       // row page index of the item's first page in this segment
   int32_t r;        // request
   int32_t L;        // seq_len of the request
-  int32_t pad;
+  int32_t tok;      // its query token
 };
 
 struct __align__(128) DecodeSmem {
@@ -171,11 +171,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
       const int item = plan.first_row[sidx] + k0 + lane;
       const bool exists = item < n_items_all;
-      int r = 0, L = 0, size = 0;
+      int r = 0, L = 0, size = 0, tok = 0;
       const int p0 = (k0 + lane == 0) ? plan.first_page[sidx] : 0;
       if (exists) {
+        // the plan's copies of seq_lens[r] and qo_indptr[r] (no device read)
         r = plan.rows[item];
-        L = p.seq_lens[r];
+        L = plan.seq[item];
+        tok = plan.tok[item];
         size = max((L + kPage - 1) / kPage - p.page_offset - p0, 0);
       }
       int incl = size;
@@ -193,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         it.p0 = p0;
         it.r = r;
         it.L = L;
+        it.tok = tok;
+        // the item's q (4 heads x 256 B) into L2 now; it is read at the item's start
+        bulk_prefetch_l2(p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim,
+                         kGroup * kHeadDim * 2);
       }
       // the table is the leading run of covered items (a gap can only come
       // from metadata that differ from the plan)
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   for (int k = 0; k < n_items && !aborted; ++k) {
     const Item& it = sm.items[k];
-    const int tok = p.qo_indptr[it.r];
+    const int tok = it.tok;
     const int qend = qg + it.n;
     const int pages_abs = (it.L + kPage - 1) / kPage;
     const int pages_r = pages_abs - p.page_offset;  // pages of the row in the stream
@@ -520,37 +526,54 @@ __global__ void __launch_bounds__(kThreads, 3)
     const size_t slot = ((size_t)b * 2 + jslot) * kGroup + g;
     *reinterpret_cast<float4*>(p.piece_o + slot * kHeadDim + d0) = o;
     if (lane == 0) p.piece_lse[slot] = lse2;
-    __threadfence();
-    bar_all();
+    bar_all();  // every piece write of the CTA precedes tid 0's release below
     if (tid == 0) {
       int* cnt = p.counters + (size_t)it.r * Hkv + kvh;
-      const int done = atomicAdd(cnt, 1);
+      const int done = atom_add_acq_rel_gpu(cnt, 1);
       sm.is_last = (done == b1 - b0);
       if (sm.is_last) *cnt = 0;  // every piece has arrived: ready for the next call
     }
-    bar_all();
+    bar_all();  // tid 0's acquire orders the piece reads below
     if (sm.is_last) {
-      __threadfence();
+      // lane-parallel weights, then every piece load in flight at once
+      const int n_pc = b1 - b0 + 1;
       float Mx = -INFINITY;
-      for (int bb = b0; bb <= b1; ++bb) {
-        const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
-        Mx = fmaxf(Mx, __ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g));
+      for (int c0 = 0; c0 < n_pc; c0 += 32) {
+        const int bb = b0 + c0 + lane;
+        if (c0 + lane < n_pc) {
+          const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+          Mx = fmaxf(Mx, __ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g));
+        }
       }
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o2));
       float wsum = 0.f;
       float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
       if (Mx != -INFINITY) {
-        for (int bb = b0; bb <= b1; ++bb) {
-          const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
-          const size_t sl = ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
-          const float ls = __ldcg(p.piece_lse + sl);
-          if (ls == -INFINITY) continue;
-          const float w = fast_exp2(ls - Mx);
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(p.piece_o + sl * kHeadDim + d0));
-          wsum += w;
-          a4.x = fmaf(w, x.x, a4.x);
-          a4.y = fmaf(w, x.y, a4.y);
-          a4.z = fmaf(w, x.z, a4.z);
-          a4.w = fmaf(w, x.w, a4.w);
+        for (int c0 = 0; c0 < n_pc; c0 += 32) {
+          const int nc = min(32, n_pc - c0);
+          float w = 0.f;
+          if (lane < nc) {
+            const int bb = b0 + c0 + lane;
+            const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+            w = fast_exp2(__ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g) - Mx);
+          }
+          float ws = w;
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o2);
+          wsum += ws;
+#pragma unroll 4
+          for (int i = 0; i < nc; ++i) {
+            const int bb = b0 + c0 + i;
+            const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+            const size_t sl = ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
+            const float wi = __shfl_sync(0xffffffffu, w, i);
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(p.piece_o + sl * kHeadDim + d0));
+            a4.x = fmaf(wi, x.x, a4.x);
+            a4.y = fmaf(wi, x.y, a4.y);
+            a4.z = fmaf(wi, x.z, a4.z);
+            a4.w = fmaf(wi, x.w, a4.w);
+          }
         }
       }
       const float winv = wsum > 0.f ? 1.f / wsum : 0.f;

@@ -34,6 +34,8 @@ struct DecodePlan {
   int32_t seg;                        // pages per segment
   int32_t total;                      // pages of one kv head's stream
   int32_t rows[kPlanMaxRows];         // request index of decode row d
+  int32_t seq[kPlanMaxRows];          // its seq_len (from the host copy)
+  int32_t tok[kPlanMaxRows];          // its query token (qo_indptr, from the host copy)
   int32_t first_row[kPlanMaxCtas];    // row (index d) holding a segment's first page
   int32_t first_page[kPlanMaxCtas];   // that page's index within its row
 };

@@ -174,8 +174,8 @@ PrefixLayout prefix_layout(size_t base, int32_t total_q, int32_t num_q_heads, in
 // Plan one persistent decode launch over decode rows rows[0..n): fills
 // plan, returns the grid size (0 when there is nothing to do, -1 when no
 // valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
-int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, int page_offset, int num_kv_heads,
-                int gcap, pa::DecodePlan& plan) {
+int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
+                int page_offset, int num_kv_heads, int gcap, pa::DecodePlan& plan) {
   std::vector<int32_t> pages(n);
   int64_t total = 0;  // pages of one kv head's stream
   for (int d = 0; d < n; ++d) {
@@ -221,7 +221,11 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, int pa
       plan.n_rows = n;
       plan.seg = (int32_t)seg;
       plan.total = (int32_t)total;
-      for (int r = 0; r < n; ++r) plan.rows[r] = rows[r];
+      for (int r = 0; r < n; ++r) {
+        plan.rows[r] = rows[r];
+        plan.seq[r] = seq_lens_host[rows[r]];
+        plan.tok[r] = qo_indptr_host[rows[r]];
+      }
       return ns * num_kv_heads;
     }
     if (seg == 1) return -1;
@@ -484,7 +488,8 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     // parameters); launches on one stream run in order and reuse the slots
     for (size_t d0 = 0; d0 < decode_rows.size(); d0 += pa::kPlanMaxRows) {
       const int n = (int)std::min(decode_rows.size() - d0, (size_t)pa::kPlanMaxRows);
-      const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, P, num_kv_heads, gcap, plan);
+      const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
+                                   plan);
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
       s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, stream); });
