@@ -134,18 +134,44 @@ __device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
 
 __device__ __forceinline__ void bar_all() { __syncthreads(); }
 
-// Folds the shared-prefix partial of this output row (4 dims at po, log2
-// lse plse2) into the normalised partial o with log2 lse lse2; returns the
-// merged lse.
-__device__ __forceinline__ float fold_prefix(float4& o, float lse2, const float* po, float plse2) {
-  float wo, wp;
-  const float l = merge2_weights(lse2, plse2, wo, wp);
-  const float4 y = *reinterpret_cast<const float4*>(po);
-  o.x = fmaf(wp, y.x, o.x * wo);
-  o.y = fmaf(wp, y.y, o.y * wo);
-  o.z = fmaf(wp, y.z, o.z * wo);
-  o.w = fmaf(wp, y.w, o.w * wo);
-  return l;
+// Whole warp (lane = 4 dims at d0): folds the shared-prefix partials of
+// output row orow (p.prefix_n key-chunk partials, or the merged one) into
+// the normalised partial o with log2 lse lse2 by log-sum-exp; returns the
+// merged lse.  Lanes read the partials' lse in parallel, then every partial
+// load is in flight at once.
+__device__ __forceinline__ float fold_prefix(const DecodeParams& p, float4& o, float lse2, size_t orow, int d0,
+                                             int lane) {
+  const int n = p.prefix_n;
+  float M = lse2;
+  for (int c0 = 0; c0 < n; c0 += 32)
+    if (c0 + lane < n) M = fmaxf(M, p.prefix_lse[(size_t)(c0 + lane) * p.prefix_rows + orow]);
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+  if (M == -INFINITY) return -INFINITY;
+  const float wo = exp2f(lse2 - M);  // own part (-inf -> 0)
+  float wsum = wo;
+  float4 a = make_float4(o.x * wo, o.y * wo, o.z * wo, o.w * wo);
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int nc = min(32, n - c0);
+    const float w = lane < nc ? exp2f(p.prefix_lse[(size_t)(c0 + lane) * p.prefix_rows + orow] - M) : 0.f;
+    float ws = w;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s);
+    wsum += ws;
+#pragma unroll 4
+    for (int i = 0; i < nc; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, w, i);
+      const float4 y =
+          *reinterpret_cast<const float4*>(p.prefix_o + ((size_t)(c0 + i) * p.prefix_rows + orow) * kHeadDim + d0);
+      a.x = fmaf(wi, y.x, a.x);
+      a.y = fmaf(wi, y.y, a.y);
+      a.z = fmaf(wi, y.z, a.z);
+      a.w = fmaf(wi, y.w, a.w);
+    }
+  }
+  const float inv = 1.f / wsum;
+  o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+  return M + log2f(wsum);
 }
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -510,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     const size_t orow = (size_t)tok * p.num_q_heads + head;
     const bool complete = (it.p0 == 0) && (it.n == pages_r);
     if (complete) {
-      if (p.prefix_o) lse2 = fold_prefix(o, lse2, p.prefix_o + orow * kHeadDim + d0, p.prefix_lse[orow]);
+      if (p.prefix_o) lse2 = fold_prefix(p, o, lse2, orow, d0, lane);
       uint2 packed;
       packed.x = pack_bf16x2(o.x, o.y);
       packed.y = pack_bf16x2(o.z, o.w);
@@ -582,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       a4.z *= winv;
       a4.w *= winv;
       float l2 = wsum > 0.f ? Mx + log2f(wsum) : -INFINITY;
-      if (p.prefix_o) l2 = fold_prefix(a4, l2, p.prefix_o + orow * kHeadDim + d0, p.prefix_lse[orow]);
+      if (p.prefix_o) l2 = fold_prefix(p, a4, l2, orow, d0, lane);
       uint2 packed;
       packed.x = pack_bf16x2(a4.x, a4.y);
       packed.y = pack_bf16x2(a4.z, a4.w);

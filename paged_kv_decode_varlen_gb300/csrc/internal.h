@@ -53,8 +53,10 @@ struct DecodeParams {
   int32_t num_kv_heads;
   float scale_log2;      // sm_scale * log2(e)
   int32_t page_offset;   // leading pages of every row left out (a shared prefix attended elsewhere)
-  const float* prefix_o;    // fp32 [total_q, Hq, D] normalised partial over those pages, or null
-  const float* prefix_lse;  // fp32 [total_q, Hq] its log2-domain lse (with prefix_o)
+  const float* prefix_o;    // fp32 [prefix_n][total_q, Hq, D] normalised partials over those pages, or null
+  const float* prefix_lse;  // fp32 [prefix_n][total_q, Hq] their log2-domain lse
+  int32_t prefix_n;         // partials to fold in (key chunks of the prefix; 1 once merged)
+  int64_t prefix_rows;      // total_q * Hq: the stride between two partials' rows
   uint16_t* out;         // bf16 [total_q, Hq, D]
   float* lse;            // [total_q, Hq] natural log, or null
   float* piece_o;        // fp32 [2 * grid, 4, D]: a CTA's partial of its first / last item

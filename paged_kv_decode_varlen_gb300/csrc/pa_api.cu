@@ -390,6 +390,11 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     if (s != PA_OK) return s;
   }
 
+  // what the decode kernel folds in: the merged prefix partial, or the key-
+  // chunk partials themselves when there is no prefill row to share them with
+  const float* dec_prefix_o = prefix_o;
+  const float* dec_prefix_lse = prefix_lse;
+  int32_t dec_prefix_n = 1;
   if (P > 0) {
     pa::PrefixParams xp;
     xp.q = static_cast<const uint16_t*>(q);
@@ -407,8 +412,8 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     const int64_t groups = prefix_qtiles(total_q) * num_kv_heads;
     int n_chunks = (int)std::min<int64_t>(prefix_chunk_cap(total_q, num_kv_heads, P),
                                           std::max<int64_t>(1, (sm_count() + groups - 1) / groups));
-    const int64_t tiles = ((int64_t)xp.prefix_keys + kPrefixKeyTile - 1) / kPrefixKeyTile;
-    xp.chunk_keys = (int32_t)((tiles + n_chunks - 1) / n_chunks * kPrefixKeyTile);
+    const int64_t key_tiles = ((int64_t)xp.prefix_keys + kPrefixKeyTile - 1) / kPrefixKeyTile;
+    xp.chunk_keys = (int32_t)((key_tiles + n_chunks - 1) / n_chunks * kPrefixKeyTile);
     n_chunks = (int)((xp.prefix_keys + xp.chunk_keys - 1) / xp.chunk_keys);
     xp.scale_log2 = scale_log2;
     xp.chunk_o = reinterpret_cast<float*>(ws + pl.chunk_o);
@@ -418,7 +423,12 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     xp.err = err;
     s = run_launch(PA_KERNEL_PREFIX, "prefix", stream, [&] { return pa::launch_prefix(xp, n_chunks, maps, stream); });
     if (s != PA_OK) return s;
-    if (n_chunks > 1) {
+    if (n_chunks > 1 && tiles.empty()) {
+      // decode rows only: the decode kernel folds the chunk partials itself
+      dec_prefix_o = xp.chunk_o;
+      dec_prefix_lse = xp.chunk_lse;
+      dec_prefix_n = n_chunks;
+    } else if (n_chunks > 1) {
       s = run_launch(PA_KERNEL_PREFIX_MERGE, "prefix_merge", stream,
                      [&] { return pa::launch_prefix_merge(xp, n_chunks, stream); });
       if (s != PA_OK) return s;
@@ -473,8 +483,10 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     dp.num_kv_heads = num_kv_heads;
     dp.scale_log2 = scale_log2;
     dp.page_offset = P;
-    dp.prefix_o = prefix_o;
-    dp.prefix_lse = prefix_lse;
+    dp.prefix_o = dec_prefix_o;
+    dp.prefix_lse = dec_prefix_lse;
+    dp.prefix_n = dec_prefix_n;
+    dp.prefix_rows = (int64_t)total_q * num_q_heads;
     dp.out = static_cast<uint16_t*>(out);
     dp.lse = lse;
     dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);

@@ -170,15 +170,27 @@ def test_prefix_must_precede_queries():
     assert e.value.status == B.PA_ERR_INVALID_ARG
 
 
+def _kinds(d, pages):
+    B.pa_trace_enable(1)
+    B.pa_trace_read()
+    _shared(d, pages)
+    torch.cuda.synchronize()
+    kinds = [k for k, _ in B.pa_trace_read()]
+    B.pa_trace_enable(0)
+    return kinds
+
+
 def test_launches_prefix_pass():
+    """Decode rows only: the decode kernel folds the prefix pass's key-chunk
+    partials itself; with a prefill row the chunks are merged first and both
+    kernels fold the merged partial."""
     b = W.make_batch([600, 700, 650], [1, 1, 1], num_blocks=200, seed=51, shared_prefix_tokens=512)
     d = DevBatch(b)
     _append(d)
     torch.cuda.synchronize()
-    B.pa_trace_enable(1)
-    B.pa_trace_read()
-    _shared(d, 32)
+    assert _kinds(d, 32) == ["prefix", "decode"]
+    b = W.make_batch([600, 700, 650], [1, 40, 1], num_blocks=200, seed=52, shared_prefix_tokens=512)
+    d = DevBatch(b)
+    _append(d)
     torch.cuda.synchronize()
-    kinds = [k for k, _ in B.pa_trace_read()]
-    B.pa_trace_enable(0)
-    assert kinds == ["prefix", "prefix_merge", "decode"]
+    assert _kinds(d, 32) == ["prefix", "prefix_merge", "prefill", "decode"]

@@ -52,9 +52,14 @@ def oracle_step(b):
 def compare(out_gpu: torch.Tensor, out_ref: np.ndarray, lse_gpu=None, lse_ref=None, what=""):
     got = oracle.bf16_to_f64(bf16_host(out_gpu))
     err = np.abs(got - out_ref)
-    assert np.all(np.isfinite(got)), f"{what}: non-finite outputs"
+    if not np.all(np.isfinite(got)):
+        bad = np.argwhere(~np.isfinite(got).all(axis=-1))
+        raise AssertionError(f"{what}: non-finite outputs at {len(bad)} (row, head) pairs, first {bad[:12].tolist()}")
     mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
-    assert mx <= MAX_ABS, f"{what}: max abs err {mx:.3e} > {MAX_ABS}"
+    if mx > MAX_ABS:
+        bad = np.argwhere((err > MAX_ABS).any(axis=-1))
+        raise AssertionError(f"{what}: max abs err {mx:.3e} > {MAX_ABS} at {len(bad)} (row, head) pairs, "
+                             f"first {bad[:12].tolist()}")
     assert mean <= MEAN_ABS, f"{what}: mean abs err {mean:.3e} > {MEAN_ABS}"
     if lse_gpu is not None:
         le = np.abs(lse_gpu.detach().cpu().double().numpy() - lse_ref)
