@@ -99,6 +99,8 @@ class Oracle:
         lib.oracle_attention_sampled.restype = i32
         lib.oracle_attention_sampled.argtypes = [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, f64,
                                                  i32, P, P, P, P, P, i32, i32]
+        lib.oracle_copy_blocks.restype = i64
+        lib.oracle_copy_blocks.argtypes = [P, P, i64, i32, i32, i32, P, P, i64]
         lib.oracle_merge_lse.restype = i32
         lib.oracle_merge_lse.argtypes = [P, P, P, P, P, P, i64, i32, i32]
         self.lib = lib
@@ -125,6 +127,20 @@ class Oracle:
         nb, _, P, _ = k_cache.shape
         _check(self.lib.oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache),
                                          _ptr(v_cache), nb, P, Hkv, D), "kv_append")
+
+    def copy_blocks(self, k_cache, v_cache, src, dst):
+        """Copy whole blocks src[i] -> dst[i] (K and V, every kv head), in
+        order, in place.  Returns the number of pairs skipped for an id
+        outside the pool."""
+        for c in (k_cache, v_cache):
+            if not (c.flags.c_contiguous and c.dtype == np.uint16):
+                raise TypeError("caches must be C-contiguous uint16")
+        src, dst = _c(src, np.int32), _c(dst, np.int32)
+        if src.shape != dst.shape or src.ndim != 1:
+            raise ValueError("src and dst must be 1-D and of equal length")
+        nb, Hkv, P, D = k_cache.shape
+        return int(self.lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), nb, P, Hkv, D, _ptr(src), _ptr(dst),
+                                               src.shape[0]))
 
     def _common(self, q, k_cache, v_cache, block_tables, seq_lens, qo_indptr):
         q = _c(q, np.uint16)
@@ -212,6 +228,10 @@ def round_bf16(x):
 
 def kv_append(*a, **kw):
     return default().kv_append(*a, **kw)
+
+
+def copy_blocks(*a, **kw):
+    return default().copy_blocks(*a, **kw)
 
 
 def attention_varlen(*a, **kw):

@@ -127,6 +127,36 @@ int oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int64_t
   return ORACLE_OK;
 }
 
+/*
+ * Block copy (copy-on-write): before a branch writes into a block it shares
+ * with another request, it gets its own copy of that block; the filled
+ * read-only blocks stay shared ("Inference optimisation", AI-infra book
+ * ch. 8, §8.3.2 and Fig. 8-15: the shared tail block holding a, b, c is
+ * copied, then each branch appends its own token).  For pair i the whole
+ * block src[i] (every kv head, every token slot, K and V) is written into
+ * block dst[i]; pairs are applied in order.  A pair with an id outside the
+ * pool is skipped; the return value is the number of skipped pairs.
+ */
+int64_t oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int64_t num_blocks, int block_size,
+                           int num_kv_heads, int head_dim, const int32_t* src, const int32_t* dst, int64_t n_pairs) {
+  int64_t skipped = 0;
+  for (int64_t i = 0; i < n_pairs; ++i) {
+    if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) {
+      ++skipped;
+      continue;
+    }
+    for (int h = 0; h < num_kv_heads; ++h)
+      for (int off = 0; off < block_size; ++off)
+        for (int d = 0; d < head_dim; ++d) {
+          size_t from = kv_offset(src[i], h, off, d, num_kv_heads, block_size, head_dim);
+          size_t to = kv_offset(dst[i], h, off, d, num_kv_heads, block_size, head_dim);
+          k_cache[to] = k_cache[from];
+          v_cache[to] = v_cache[from];
+        }
+  }
+  return skipped;
+}
+
 /* Shared argument bundle for the attention definition. */
 typedef struct {
   const uint16_t* q;

@@ -382,6 +382,51 @@ def pin_append_then_read(o):
         raise AssertionError("slot beyond the pool was accepted")
 
 
+def pin_copy_on_write(o):
+    """Copy-on-write of a shared tail block ("Inference optimisation"
+    §8.3.2, Fig. 8-15): two branches share every block, the last one only
+    partly filled; branch B copies that tail block, then each branch appends
+    its own next token.  Each branch must then attend exactly as if it had
+    private copies of every block, and the shared blocks are untouched.
+    Pairs naming a block outside the pool are skipped and counted."""
+    Hq, Hkv, P, D = 8, 2, 16, 32
+    rng = np.random.default_rng(19)
+    nb = 12
+    k = workloads.normal_bf16(rng, (nb, Hkv, P, D))
+    v = workloads.normal_bf16(rng, (nb, Hkv, P, D))
+    shared = np.array([3, 7, 1, 9], np.int32)          # 3 full pages + a tail page holding 2 tokens
+    L0 = 3 * P + 2
+    k_ref, v_ref = k.copy(), v.copy()
+    # B gets its own tail: copy block 9 into free block 5
+    assert o.copy_blocks(k, v, np.array([9, 9], np.int32), np.array([5, nb + 3], np.int32)) == 1
+    assert np.array_equal(k[5], k[9]) and np.array_equal(v[5], v[9])
+    assert np.array_equal(np.delete(k, 5, 0), np.delete(k_ref, 5, 0))
+    ta = shared.copy()
+    tb = shared.copy()
+    tb[3] = 5
+    new_a = workloads.normal_bf16(rng, (2, Hkv, D))       # (K, V) of A's token, then B's
+    new_b = workloads.normal_bf16(rng, (2, Hkv, D))
+    o.kv_append(new_a[:1], new_a[1:], np.array([9 * P + 2], np.int64), k, v)
+    o.kv_append(new_b[:1], new_b[1:], np.array([5 * P + 2], np.int64), k, v)
+    q = workloads.normal_bf16(rng, (2, Hq, D))
+    tables = np.stack([ta, tb]).astype(np.int32)
+    seq = np.array([L0 + 1, L0 + 1], np.int32)
+    ind = np.array([0, 1, 2], np.int32)
+    out, lse = o.attention_varlen(q, k, v, tables, seq, ind, 1 / math.sqrt(D))
+    for r, new in ((0, new_a), (1, new_b)):
+        # private copies: blocks 0..3 of a fresh pool, the appended token at L0
+        kp = np.zeros((4, Hkv, P, D), np.uint16)
+        vp = np.zeros((4, Hkv, P, D), np.uint16)
+        kp[:] = k_ref[shared]
+        vp[:] = v_ref[shared]
+        kp[3, :, 2] = new[0]
+        vp[3, :, 2] = new[1]
+        po, pl = o.attention_varlen(q[r:r + 1], kp, vp, np.arange(4, dtype=np.int32)[None], seq[r:r + 1],
+                                    np.array([0, 1], np.int32), 1 / math.sqrt(D))
+        assert np.array_equal(out[r], po[0]) and np.array_equal(lse[r], pl[0]), r
+    assert not np.array_equal(out[0], out[1])
+
+
 def pin_brute_force(o):
     """Cross-check against the pure-Python fp64 restatement (oracle/brute.py)
     on a tiny mixed batch (decode rows and a chunk)."""
@@ -407,7 +452,7 @@ def pin_sampled_matches_full(o):
 ALL_PINS = [pin_page_arithmetic, pin_round_bf16, pin_single_key, pin_one_hot_score, pin_two_key_sigmoid,
             pin_uniform_scores, pin_gqa_grouping, pin_scipy_dense, pin_page_permutation,
             pin_shared_equals_duplicated, pin_chunked_equals_oneshot, pin_merge_identity, pin_append_then_read,
-            pin_brute_force, pin_sampled_matches_full]
+            pin_copy_on_write, pin_brute_force, pin_sampled_matches_full]
 
 
 def run_all(o) -> list:

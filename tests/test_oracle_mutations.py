@@ -30,6 +30,10 @@ MUTANTS = {
     "merge_lse_dropped": ("lse_out[i] = M + log(wa + wb);", "lse_out[i] = M;"),
     "normalise_dropped": ("for (int d = 0; d < a->D; ++d) o[d] /= l;", ""),
     "round_truncates": ("double r = ldexp(rint(ldexp(m, 8)), e - 8);", "double r = ldexp(trunc(ldexp(m, 8)), e - 8);"),
+    "copy_keys_only": ("          v_cache[to] = v_cache[from];\n", ""),
+    "copy_one_head": ("    for (int h = 0; h < num_kv_heads; ++h)\n      for (int off = 0; off < block_size; ++off)",
+                      "    for (int h = 0; h < 1; ++h)\n      for (int off = 0; off < block_size; ++off)"),
+    "copy_reversed": ("          k_cache[to] = k_cache[from];", "          k_cache[from] = k_cache[to];"),
 }
 
 
