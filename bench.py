@@ -49,6 +49,8 @@ WORKLOADS = {
     "mixed": "mixed chunked-prefill batch: one 512-token chunk at offset 1536 + 63 decode rows seq_len "
              "U[2048,8192], 24,576-block pool, GQA 32/8, head_dim 128, bf16, 1 layer, kv_append of 575 tokens",
     "tiny": "tiny decode: 4 decode rows seq_len {17,100,256,513}, 64-block pool, GQA 32/8, head_dim 128, bf16",
+    "verify": "speculative-verify step: 64 rows of 5 query tokens (4-token drafts) over seq_len U[2048,2303], "
+              "10,922-block pool, GQA 32/8, head_dim 128, bf16, 1 layer, kv_append of 320 tokens",
 }
 
 
@@ -58,6 +60,13 @@ def load_peaks():
         d = json.load(open(path))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def load_tflops_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return float(json.load(open(path))["bf16_tflops"])
+    return 1900.0
 
 
 def kernel_source_hash():
@@ -490,15 +499,32 @@ def main():
     value = bytes_all / (t_step * 1e-3) / 1e9
     e2e_value = bytes_all / (t_e2e * 1e-3) / 1e9
 
-    dec = [ms for k_, ms in trace if k_ == "decode"]
     peak, peak_kind = load_peaks()
-    dec_ms = sum(dec) / len(dec) if dec else None
-    achieved = sb["decode_kernel"] / (dec_ms * 1e-3) / 1e9 if dec_ms else None
+    tflops_peak = load_tflops_peak()
     pre = [ms for k_, ms in trace if k_ == "prefix"]
     pre_ms = sum(pre) / len(pre) if pre else None
     kernel_share = {}
     for k_, ms in trace:
         kernel_share[k_] = kernel_share.get(k_, 0.0) + ms
+    # roofline of the kernel with the largest share of the step: the decode
+    # kernel (HBM-bound), or the tensor-core tile kernel of rows with
+    # qo_len > 1, bound by HBM or by the tensor pipe by its arithmetic intensity
+    dom = max(("decode", "prefill"), key=lambda k_: kernel_share.get(k_, 0.0))
+    dom_ms_list = [ms for k_, ms in trace if k_ == dom]
+    dom_ms = sum(dom_ms_list) / len(dom_ms_list) if dom_ms_list else None
+    if dom == "decode":
+        bound, dom_bytes, dom_flops = "hbm", sb["decode_kernel"], None
+    else:
+        dom_bytes, dom_flops = sb["prefill_kernel"], sb["prefill_flops"]
+        bound = "tensor" if dom_flops / max(dom_bytes, 1) > tflops_peak * 1e12 / (peak * 1e9) else "hbm"
+    if bound == "hbm":
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else None
+        r_peak, r_unit = peak, "GB/s"
+        r_source = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s"
+    else:
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12 if dom_ms else None
+        r_peak, r_unit = tflops_peak, "TFLOP/s"
+        r_source = "measured (MEASURED_PEAKS.json bf16_tflops)"
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -516,14 +542,14 @@ def main():
                    "query_tokens_per_step": sb["query_tokens"]},
         "tokens_per_layer_step_per_s": round(sb["query_tokens"] * world / (t_step * 1e-3), 1),
         "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
-        "roofline": {"bound": "hbm", "kernel": "decode", "achieved": round(achieved, 2) if achieved else None,
-                     "peak": peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if
-                     peak_kind == "measured" else "fallback 6.8 TB/s", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4) if achieved else None,
-                     "traffic": profiled_traffic(args.workload),
-                     "algorithmic_bytes_per_launch": sb["decode_kernel"],
-                     "avg_launch_ms": round(dec_ms, 5) if dec_ms else None,
-                     "timing": f"CUDA events around each decode launch, {trace_steps} steps after the timed pass",
+        "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2) if achieved else None,
+                     "peak": r_peak, "peak_source": r_source, "unit": r_unit,
+                     "frac": round(achieved / r_peak, 4) if achieved else None,
+                     "traffic": profiled_traffic(args.workload) if dom == "decode" else None,
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     **({"algorithmic_flops_per_launch": dom_flops} if dom_flops else {}),
+                     "avg_launch_ms": round(dom_ms, 5) if dom_ms else None,
+                     "timing": f"CUDA events around each {dom} launch, {trace_steps} steps after the timed pass",
                      "kernel_time_share": {k_: round(v / sum(kernel_share.values()), 4)
                                            for k_, v in kernel_share.items()}},
         **({"prefix_pass": {"algorithmic_bytes_per_launch": sb["prefix_kernel"],

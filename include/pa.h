@@ -100,6 +100,27 @@ pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot
                        int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_copy_blocks -- copy-on-write block copy ("Inference optimisation",
+ * AI-infra book ch. 8, §8.3.2 and Fig. 8-15: before a branch writes into a
+ * block it shares with another request, it gets its own copy of that block,
+ * and the filled read-only blocks stay shared).
+ *   For pair i, the whole block src_blocks[i] -- every kv head and token
+ *   slot, of k_cache and of v_cache -- is copied into block dst_blocks[i].
+ * src_blocks, dst_blocks  [n_pairs] int32, device.  The dst ids must be
+ *                distinct and none may also be a src id of the call;
+ *                otherwise which copy lands is undefined (no fault).
+ * k_cache, v_cache  HND pools as for pa_kv_append, modified in place.
+ * workspace      device, >= PA_ERROR_WORD_BYTES bytes; a pair naming a block
+ *                outside [0, num_blocks) is skipped and PA_ERR_DEVICE_INDEX
+ *                is recorded in its error word.
+ * Errors: PA_ERR_INVALID_ARG (n_pairs < 0, null or misaligned pointers),
+ *   PA_ERR_UNSUPPORTED (shape), PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_CUDA.
+ */
+pa_status pa_copy_blocks(const int32_t* src_blocks, const int32_t* dst_blocks, int64_t n_pairs, void* k_cache,
+                         void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_attention_workspace_size -- bytes of device workspace that
  * pa_attention_varlen needs for a batch with at most these sizes.  The
  * workspace holds the error word and the split-KV partial results.
@@ -284,7 +305,8 @@ typedef enum {
   PA_KERNEL_PREFILL = 4,
   PA_KERNEL_MERGE = 5,
   PA_KERNEL_PREFIX = 6,      /* shared-prefix pass of pa_attention_varlen_shared_prefix */
-  PA_KERNEL_PREFIX_MERGE = 7 /* merge of that pass's key-chunk partials */
+  PA_KERNEL_PREFIX_MERGE = 7, /* merge of that pass's key-chunk partials */
+  PA_KERNEL_COPY_BLOCKS = 8   /* pa_copy_blocks */
 } pa_kernel_kind;
 
 pa_status pa_set_decode_ctas(int32_t n);

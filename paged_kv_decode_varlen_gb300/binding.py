@@ -27,7 +27,7 @@ PA_ERR_CUDA = 4
 PA_ERR_DEVICE_INDEX = 5
 PA_ERR_DEVICE_TIMEOUT = 6
 PA_ERROR_WORD_BYTES = 256
-KERNEL_KINDS = {1: "kv_append", 2: "decode", 3: "combine", 4: "prefill", 5: "merge", 6: "prefix", 7: "prefix_merge"}
+KERNEL_KINDS = {1: "kv_append", 2: "decode", 3: "combine", 4: "prefill", 5: "merge", 6: "prefix", 7: "prefix_merge", 8: "copy_blocks"}
 
 
 class PAError(RuntimeError):
@@ -48,6 +48,7 @@ _SIGS = {
     "pa_status_string": (ctypes.c_char_p, [_i32]),
     "pa_last_error_message": (ctypes.c_char_p, []),
     "pa_kv_append": (_i32, [_P, _P, _P, _i64, _P, _P, _i64, _i32, _i32, _i32, _P, _sz, _P]),
+    "pa_copy_blocks": (_i32, [_P, _P, _i64, _P, _P, _i64, _i32, _i32, _i32, _P, _sz, _P]),
     "pa_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pa_attention_varlen": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _f32, _P, _P, _P, _sz, _P]),
@@ -128,6 +129,23 @@ def pa_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, workspace=None, s
         workspace = new_workspace(PA_ERROR_WORD_BYTES, k_cache.device)
     _check(_lib.pa_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache), _ptr(v_cache), nb, P,
                              Hkv, D, _ptr(workspace), workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def pa_copy_blocks(src_blocks, dst_blocks, k_cache, v_cache, workspace=None, stream=None):
+    """Copy whole blocks src_blocks[i] -> dst_blocks[i] of both HND pools
+    (int32 [n] device ids; copy-on-write of shared blocks)."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(src_blocks, torch.int32, "src_blocks")
+    _need(dst_blocks, torch.int32, "dst_blocks")
+    if src_blocks.shape != dst_blocks.shape or src_blocks.dim() != 1 or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    nb, Hkv, P, D = k_cache.shape
+    if workspace is None:
+        workspace = new_workspace(PA_ERROR_WORD_BYTES, k_cache.device)
+    _check(_lib.pa_copy_blocks(_ptr(src_blocks), _ptr(dst_blocks), src_blocks.shape[0], _ptr(k_cache),
+                               _ptr(v_cache), nb, P, Hkv, D, _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
 
 

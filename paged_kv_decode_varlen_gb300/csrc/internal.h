@@ -21,6 +21,17 @@ struct AppendParams {
   int* err;
 };
 
+struct CopyParams {
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  int64_t num_blocks;
+  const int32_t* src;
+  const int32_t* dst;
+  int64_t n_pairs;
+  int64_t block_vecs;  // 16-byte words in one block of one cache
+  int* err;
+};
+
 // Persistent decode launch plan (host-made, passed by value).  For each kv
 // head the decode rows' pages are laid end to end as one stream (row d of
 // the launch, then row d + 1, ...); every stream is cut into n_seg equal
@@ -149,6 +160,7 @@ pa_status set_error(pa_status s, const char* fmt, ...);
 
 // Each launcher enqueues one kernel on `stream` and returns its launch error.
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
                            cudaStream_t stream);

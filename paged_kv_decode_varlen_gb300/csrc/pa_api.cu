@@ -561,6 +561,34 @@ pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot
   return s == PA_OK ? ok() : s;
 }
 
+pa_status pa_copy_blocks(const int32_t* src_blocks, const int32_t* dst_blocks, int64_t n_pairs, void* k_cache,
+                         void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (n_pairs < 0) return fail(PA_ERR_INVALID_ARG, "n_pairs %lld < 0", (long long)n_pairs);
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
+  pa_status s = check_shape(PA_GQA_GROUP * num_kv_heads, num_kv_heads, head_dim, block_size);
+  if (s != PA_OK) return s;
+  if (!k_cache || !v_cache || !workspace) return fail(PA_ERR_INVALID_ARG, "null cache or workspace pointer");
+  if (n_pairs > 0 && (!src_blocks || !dst_blocks)) return fail(PA_ERR_INVALID_ARG, "null block id pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_blocks, 4) || !aligned(dst_blocks, 4) ||
+      !aligned(workspace, 4))
+    return fail(PA_ERR_INVALID_ARG, "caches must be 16-byte aligned (block ids and workspace 4)");
+  if (workspace_bytes < PA_ERROR_WORD_BYTES)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %d bytes", workspace_bytes, PA_ERROR_WORD_BYTES);
+  if (n_pairs == 0) return ok();
+  pa::CopyParams p;
+  p.k_cache = static_cast<uint16_t*>(k_cache);
+  p.v_cache = static_cast<uint16_t*>(v_cache);
+  p.num_blocks = num_blocks;
+  p.src = src_blocks;
+  p.dst = dst_blocks;
+  p.n_pairs = n_pairs;
+  p.block_vecs = (int64_t)num_kv_heads * block_size * head_dim * 2 / 16;
+  p.err = static_cast<int*>(workspace);
+  s = run_launch(PA_KERNEL_COPY_BLOCKS, "copy_blocks", stream, [&] { return pa::launch_copy_blocks(p, stream); });
+  return s == PA_OK ? ok() : s;
+}
+
 size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t head_dim,
                                    int32_t max_seq_len) {
   if (num_reqs < 0 || total_q < 0 || num_q_heads < 0 || head_dim < 0) return 0;

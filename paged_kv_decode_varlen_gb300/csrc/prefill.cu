@@ -73,12 +73,9 @@ struct __align__(1024) TcSmem {
   uint64_t bar_q;
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
-  uint64_t k_empty[kStages];
-  uint64_t v_empty[kStages];
+  uint64_t pv_done[2];  // PV of tile j done: phase j / 2 of pv_done[j % 2]
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_done;
-  uint64_t drain;
   uint32_t tmem;
   int abort;
 };
@@ -163,15 +160,13 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
+
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_full[b], kSoftmaxWarps * 32);
+      mbar_init(&sm.pv_done[b], 1);
     }
-    mbar_init(&sm.o_done, 1);
-    mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
     // Q first: its copy overlaps the rest of the set-up
@@ -189,10 +184,12 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
   if (is_producer) {
     // ----------------------------------------------------------- producers
     // warp kKWarp: Q (above), then the K ring; warp kVWarp: the V ring.  A K
-    // stage is free once its S product is done, a V stage once its PV is.
+    // stage is free once its S product is done (s_full), a V stage once its
+    // PV product is (pv_done); stage s serves tiles s, s + 2, ..., and so do
+    // both barrier pairs, so tile j waits for phase (j - 2) / 2.
     const CUtensorMap* map = is_k ? &maps.k : &maps.v;
     uint64_t* full = is_k ? sm.k_full : sm.v_full;
-    uint64_t* empty = is_k ? sm.k_empty : sm.v_empty;
+    uint64_t* empty = is_k ? sm.s_full : sm.pv_done;
     int last_issued[kStages] = {-1, -1};
     if (lane == 0) prefetch_tensormap(map);
     for (int j = 0; j < n_tiles; ++j) {
@@ -223,10 +220,12 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t qb = smem_addr(sm.q);
+      int last_s = -1, last_pv = -1;  // last S / PV issued
       auto issue_s = [&](int j) -> bool {
         const int s = j & (kStages - 1);
         if (!tc_wait(sm, &sm.k_full[s], (j / kStages) & 1, err)) return false;
         fence_after_sync();
+        last_s = j;
         const uint32_t kb = smem_addr(sm.k[s]);
         const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * kKeys;
 #pragma unroll
@@ -234,8 +233,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
           const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;  // 64-dim half, 16-dim step in it
           mma_bf16(d, desc_sw128(qb + off, 16, 1024), desc_sw128(kb + off, 16, 1024), kIdescS, ks > 0);
         }
-        commit(&sm.s_full[j & 1]);
-        commit(&sm.k_empty[s]);
+        commit(&sm.s_full[j & 1]);  // one commit per MMA group
         return true;
       };
       // S runs one tile ahead: S(j + 1) is queued before PV(j), which waits
@@ -255,12 +253,14 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
           mma_bf16(tmem + kColO, desc_sw128(pa, 16, 1024), desc_sw128(va, kHalf, 1024), kIdescO,
                    (j > 0 || ks > 0) ? 1u : 0u);
         }
-        commit(&sm.v_empty[s]);
-        commit(&sm.o_done);
+        commit(&sm.pv_done[j & 1]);
+        last_pv = j;
       }
-      // every MMA issued has completed before the CTA frees its tensor memory
-      commit(&sm.drain);
-      mbar_wait_bounded(&sm.drain, 0);
+      // every MMA issued has completed before the CTA frees its tensor memory:
+      // the PVs form one chain on O, and the S products were each waited for
+      // by the softmax unless it gave up
+      if (last_pv >= 0) mbar_wait_bounded(&sm.pv_done[last_pv & 1], (last_pv >> 1) & 1);
+      if (last_s >= 0) mbar_wait_bounded(&sm.s_full[last_s & 1], (last_s >> 1) & 1);
     }
     __syncwarp();
   } else {
@@ -312,11 +312,16 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
         l_run *= corr;
         m_run = mt;
       }
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O holds tiles < j: wait for the PV of tile j - 1, then rescale
-        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.o_done, (j - 1) & 1, err));
+      if (j > 0) {
+        // PV of tile j - 1 done (and with it every earlier PV: they form one
+        // chain on O): O is stable and the P tile of tile j - 2 is free.  S
+        // products go to other accumulators and may finish before it.
+        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err));
         if (!ok) break;
         fence_after_sync();
+      }
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // rescale the rows of O whose running max grew
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
@@ -352,7 +357,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       fence_before_sync();       // tensor-memory reads / writes above precede the arrive
       mbar_arrive(&sm.p_full[j & 1]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.o_done, (n_tiles - 1) & 1, err));
+    if (ok) ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, err));
     if (ok) {
       fence_after_sync();
       float o[4][32];

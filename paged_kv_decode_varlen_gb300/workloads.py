@@ -174,12 +174,13 @@ def make_batch(seq_lens, qo_lens, *, num_blocks: int, seed: int, num_q_heads: in
 # ---------------------------------------------------------------------------
 SEED0 = 20261202
 POOL_12GIB_PER_LAYER = 5461
+_WL_SEED = {"tiny": 1, "short": 2, "shared": 3, "mixed": 4, "verify": 6}
 
 
 def workload(name: str, *, scale: float = 1.0, seed_offset: int = 0) -> dict:
     """Length recipe of a named workload.  `scale` < 1 shrinks request
     counts for quick parity runs while keeping the length mix."""
-    rng = np.random.default_rng(SEED0 + {"tiny": 1, "short": 2, "shared": 3, "mixed": 4}[name] + seed_offset)
+    rng = np.random.default_rng(SEED0 + _WL_SEED[name] + seed_offset)
     if name == "tiny":
         seq = [17, 100, 256, 513]
         return dict(seq_lens=seq, qo_lens=[1] * 4, num_blocks=64, shared_prefix_tokens=0)
@@ -195,12 +196,19 @@ def workload(name: str, *, scale: float = 1.0, seed_offset: int = 0) -> dict:
         n = max(1, int(round(63 * scale)))
         seq = [2048] + rng.integers(2048, 8192 + 1, n).tolist()
         return dict(seq_lens=seq, qo_lens=[512] + [1] * n, num_blocks=24576, shared_prefix_tokens=0)
+    if name == "verify":
+        # speculative verification ("Inference optimisation" §8.5.1): each of
+        # the short-dialogue requests checks a 4-token draft, i.e. 5 query
+        # tokens (the 4 drafts and the token after them) over its context
+        n = max(1, int(round(64 * scale)))
+        seq = rng.integers(2048, 2303 + 1, n).tolist()
+        return dict(seq_lens=seq, qo_lens=[5] * n, num_blocks=2 * POOL_12GIB_PER_LAYER, shared_prefix_tokens=0)
     raise KeyError(name)
 
 
 def workload_batch(name: str, *, scale: float = 1.0, seed_offset: int = 0, **kw) -> Batch:
     spec = workload(name, scale=scale, seed_offset=seed_offset)
-    seed = SEED0 + 100 + {"tiny": 1, "short": 2, "shared": 3, "mixed": 4}[name] + seed_offset
+    seed = SEED0 + 100 + _WL_SEED[name] + seed_offset
     return make_batch(spec["seq_lens"], spec["qo_lens"], num_blocks=spec["num_blocks"], seed=seed,
                       shared_prefix_tokens=spec["shared_prefix_tokens"], **kw)
 
@@ -262,7 +270,20 @@ def step_bytes(b: Batch, prefix_pages: int = 0) -> dict:
     decode_kernel = decode_kv_unique + n_dec * Hq * D * 2 + int(
         sum(4 * (-(-int(L) // P) - prefix_pages) for L in seq[decode]))
     prefix_kernel = prefix_pages * P * per_tok + total_q * Hq * D * 2 + 4 * prefix_pages if prefix_pages else 0
+    # tensor-core tile kernel (rows with qo_len > 1): the keys each row reads
+    # once per kv head (after the prefix), its q, its table entries; flops
+    # of the causal QK^T and PV products (2 x 2 flop per pair, head and dim)
+    pre_kv, pre_q, pre_tab, pre_flops = 0, 0, 0, 0
+    for r in np.nonzero(qo > 1)[0]:
+        L, c = int(seq[r]), int(qo[r])
+        h = L - c
+        pre_kv += (L - prefix_pages * P) * per_tok
+        pre_q += c * Hq * D * 2
+        pre_tab += 4 * (-(-L // P) - prefix_pages)
+        pre_flops += (c * h + c * (c + 1) // 2) * Hq * D * 4
+    prefill_kernel = pre_kv + pre_q + pre_tab
     return dict(unique=unique_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
                 logical=logical_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
                 unique_kv=unique_kv, logical_kv=logical_kv, decode_kernel=decode_kernel,
-                prefix_kernel=prefix_kernel, query_tokens=int(total_q))
+                prefix_kernel=prefix_kernel, prefill_kernel=prefill_kernel, prefill_flops=pre_flops,
+                query_tokens=int(total_q))

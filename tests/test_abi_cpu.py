@@ -148,3 +148,18 @@ def test_shared_prefix_validation():
     need = b.pa_shared_prefix_workspace_size(2, 2, 32, 128, 100, 2)
     assert _attn_prefix(2, wsb=need - 256) == b.PA_ERR_WORKSPACE_TOO_SMALL
     assert "workspace" in lib.pa_last_error_message().decode()
+
+
+def test_copy_blocks_validation():
+    ws = FAKE
+    assert lib.pa_copy_blocks(FAKE, FAKE, -1, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(None, FAKE, 2, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(FAKE, FAKE, 2, FAKE, FAKE, 0, 16, 8, 128, ws, 256, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(FAKE, FAKE, 2, FAKE, FAKE, 64, 8, 8, 128, ws, 256, None) == b.PA_ERR_UNSUPPORTED
+    assert lib.pa_copy_blocks(FAKE, FAKE, 2, FAKE, FAKE, 64, 16, 8, 128, ws, 64, None) == \
+        b.PA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.pa_copy_blocks(FAKE, FAKE, 2, ctypes.c_void_p((1 << 20) + 8), FAKE, 64, 16, 8, 128, ws, 256,
+                              None) == b.PA_ERR_INVALID_ARG
+    n0 = lib.pa_launch_count()
+    assert lib.pa_copy_blocks(None, None, 0, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == b.PA_OK
+    assert lib.pa_launch_count() == n0

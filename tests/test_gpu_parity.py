@@ -72,7 +72,7 @@ def test_kv_append_skip_and_out_of_range():
 
 # ------------------------------------------------------- attention: workloads
 @pytest.mark.parametrize("name,scale", [("tiny", 1.0), ("short", 1.0), ("shared", 1.0), ("mixed", 0.25),
-                                        ("mixed", 1.0)])
+                                        ("mixed", 1.0), ("verify", 0.25), ("verify", 1.0)])
 def test_workload_parity(name, scale):
     b = W.workload_batch(name, scale=scale)
     d = DevBatch(b)
