@@ -99,6 +99,17 @@ class Oracle:
         lib.oracle_attention_sampled.restype = i32
         lib.oracle_attention_sampled.argtypes = [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, f64,
                                                  i32, P, P, P, P, P, i32, i32]
+        lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+        lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.oracle_f16_value.restype = f64
+        lib.oracle_f16_value.argtypes = [ctypes.c_uint16]
+        lib.oracle_quantize_q8.restype = None
+        lib.oracle_quantize_q8.argtypes = [P, i64, P, P]
+        lib.oracle_kv_append_q8.restype = i32
+        lib.oracle_kv_append_q8.argtypes = [P, P, P, i64, P, P, i64, i32, i32, i32]
+        lib.oracle_attention_varlen_q8.restype = i32
+        lib.oracle_attention_varlen_q8.argtypes = [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32, f64,
+                                                   P, P, P, i32, i32]
         lib.oracle_copy_blocks.restype = i64
         lib.oracle_copy_blocks.argtypes = [P, P, i64, i32, i32, i32, P, P, i64]
         lib.oracle_merge_lse.restype = i32
@@ -174,6 +185,60 @@ class Oracle:
                                                 nt), "attention_varlen")
         return out, lse
 
+    # ---------------------------------------------------------------- q8_0
+    def f32_to_f16(self, x: float) -> int:
+        """binary16 bits of a binary32 value (round to nearest even)."""
+        return int(self.lib.oracle_f32_to_f16(float(x)))
+
+    def f16_value(self, h: int) -> float:
+        return float(self.lib.oracle_f16_value(int(h)))
+
+    def quantize_q8(self, x):
+        """q8_0 of bf16 values x (uint16 [..., 32 k]): int8 codes of x's shape
+        and uint16 binary16 scales [..., k]."""
+        x = _c(x, np.uint16)
+        if x.shape[-1] % 32:
+            raise ValueError("the last dimension must be a multiple of 32")
+        codes = np.zeros(x.shape, np.int8)
+        scales = np.zeros(x.shape[:-1] + (x.shape[-1] // 32,), np.uint16)
+        self.lib.oracle_quantize_q8(_ptr(x), x.size // 32, _ptr(codes), _ptr(scales))
+        return codes, scales
+
+    def kv_append_q8(self, k_new, v_new, slot_mapping, k_cache, v_cache):
+        """kv_append into q8_0 pages, in place: caches uint8
+        [num_blocks, Hkv, q8_slab_bytes(P, D)]."""
+        k_new, v_new = _c(k_new, np.uint16), _c(v_new, np.uint16)
+        slot_mapping = _c(slot_mapping, np.int64)
+        for c in (k_cache, v_cache):
+            if not (c.flags.c_contiguous and c.dtype == np.uint8):
+                raise TypeError("q8 caches must be C-contiguous uint8")
+        N, Hkv, D = k_new.shape
+        nb = k_cache.shape[0]
+        P = q8_page_tokens(k_cache.shape[2], D)
+        _check(self.lib.oracle_kv_append_q8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache),
+                                            _ptr(v_cache), nb, P, Hkv, D), "kv_append_q8")
+
+    def attention_varlen_q8(self, q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, sm_scale, n_threads=None):
+        """attention_varlen over q8_0 pages (uint8 [num_blocks, Hkv, slab])."""
+        q = _c(q, np.uint16)
+        k_cache, v_cache = _c(k_cache, np.uint8), _c(v_cache, np.uint8)
+        block_tables = _c(block_tables, np.int32)
+        seq_lens, qo_indptr = _c(seq_lens, np.int32), _c(qo_indptr, np.int32)
+        total_q, Hq, D = q.shape
+        nb, Hkv, slab = k_cache.shape
+        P = q8_page_tokens(slab, D)
+        R = seq_lens.shape[0]
+        nt = n_threads or host_threads()
+        max_len = max(int(seq_lens.max()) if R else 1, 1)
+        out = np.zeros((total_q, Hq, D), np.float64)
+        lse = np.zeros((total_q, Hq), np.float64)
+        scratch = np.zeros(nt * max_len, np.float64)
+        _check(self.lib.oracle_attention_varlen_q8(_ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                                                   block_tables.shape[1], _ptr(seq_lens), _ptr(qo_indptr), R, Hq,
+                                                   Hkv, D, P, float(sm_scale), _ptr(out), _ptr(lse), _ptr(scratch),
+                                                   max_len, nt), "attention_varlen_q8")
+        return out, lse
+
     def attention_sampled(self, q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, sm_scale, sample_tok,
                           sample_head, n_threads=None):
         """The same definition at a list of (query token, q head) samples.
@@ -232,6 +297,30 @@ def kv_append(*a, **kw):
 
 def copy_blocks(*a, **kw):
     return default().copy_blocks(*a, **kw)
+
+
+def q8_slab_bytes(page_tokens: int, head_dim: int) -> int:
+    """Bytes of one (block, kv head) q8_0 slab: codes, then binary16 scales."""
+    return page_tokens * head_dim + page_tokens * (head_dim // 32) * 2
+
+
+def q8_page_tokens(slab_bytes: int, head_dim: int) -> int:
+    per_token = head_dim + (head_dim // 32) * 2
+    if slab_bytes % per_token:
+        raise ValueError("slab size does not match the head dimension")
+    return slab_bytes // per_token
+
+
+def quantize_q8(*a, **kw):
+    return default().quantize_q8(*a, **kw)
+
+
+def kv_append_q8(*a, **kw):
+    return default().kv_append_q8(*a, **kw)
+
+
+def attention_varlen_q8(*a, **kw):
+    return default().attention_varlen_q8(*a, **kw)
 
 
 def attention_varlen(*a, **kw):

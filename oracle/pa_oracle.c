@@ -93,6 +93,87 @@ void oracle_round_bf16_array(const double* x, uint16_t* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(x[i]);
 }
 
+/* binary16 bit pattern -> exact value. */
+static double f16_to_double(uint16_t h) {
+  int e = (h >> 10) & 0x1f, m = h & 0x3ff;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);                      /* zero, subnormal */
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp((double)(m | 0x400), e - 25);                 /* 1.m * 2^(e-15) */
+  return (h & 0x8000) ? -v : v;
+}
+
+/* binary32 value -> binary16 bits, round to nearest even, gradual underflow,
+ * overflow to infinity: rounded with rint() at the value's binary16 quantum
+ * (2^(e-11) for normal numbers, 2^-24 below 2^-14), then encoded. */
+static uint16_t f32_to_f16(float f) {
+  double x = (double)f;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return 0x7e00;
+  double r;
+  if (a < ldexp(1.0, -14)) {
+    r = ldexp(rint(ldexp(a, 24)), -24);
+  } else {
+    int e;
+    double m = frexp(a, &e);
+    r = ldexp(rint(ldexp(m, 11)), e - 11);
+  }
+  if (r >= 65520.0 || isinf(a)) return sign | 0x7c00;
+  if (r < ldexp(1.0, -14)) return sign | (uint16_t)ldexp(r, 24);   /* subnormal (or 0) */
+  int e;
+  double m = frexp(r, &e);                                          /* r = m 2^e, 0.5 <= m < 1 */
+  return sign | (uint16_t)((e + 14) << 10) | (uint16_t)(ldexp(m, 11) - 1024.0);
+}
+
+uint16_t oracle_f32_to_f16(float f) { return f32_to_f16(f); }
+double oracle_f16_value(uint16_t h) { return f16_to_double(h); }
+
+/*
+ * q8_0 ("Inference optimisation", AI-infra book ch. 8, §8.4.2 and Fig.
+ * 8-23): 32 values share one 2-byte scale and each keeps an 8-bit code, 34
+ * bytes instead of 64.  The pages fix the grouping and the sizes, not the
+ * arithmetic; the reading used here: the scale is d = max|x| / 127 in
+ * binary32, stored as binary16 (round to nearest even); each code is
+ * rint(x / d16) in binary32 with d16 the stored scale, clamped to
+ * [-127, 127]; a group whose stored scale is 0 gets all-zero codes.  The
+ * value a code stands for is code * d16 (exact in binary32).
+ */
+static void quantize_group_q8(const uint16_t* x, int8_t* codes, uint16_t* scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < 32; ++i) {
+    float v = (float)fabs(bf16_to_double(x[i]));
+    if (v > amax) amax = v;
+  }
+  float d = amax / 127.0f;
+  uint16_t h = f32_to_f16(d);
+  float d16 = (float)f16_to_double(h);
+  for (int i = 0; i < 32; ++i) {
+    int c = 0;
+    if (d16 != 0.0f) {
+      float t = rintf((float)bf16_to_double(x[i]) / d16);
+      c = t > 127.0f ? 127 : (t < -127.0f ? -127 : (int)t);
+    }
+    codes[i] = (int8_t)c;
+  }
+  *scale = h;
+}
+
+void oracle_quantize_q8(const uint16_t* x, int64_t n_groups, int8_t* codes, uint16_t* scales) {
+  for (int64_t g = 0; g < n_groups; ++g) quantize_group_q8(x + 32 * g, codes + 32 * g, scales + g);
+}
+
+/* q8_0 pages: one (block, kv head) slab of p tokens is p * D code bytes
+ * (token t, dim d at t * D + d) followed by p * D / 32 little-endian
+ * binary16 scales (token t, group g at 2 * (t * D / 32 + g)). */
+static size_t q8_slab_bytes(int p, int D) { return (size_t)p * (size_t)D + (size_t)p * (size_t)(D / 32) * 2; }
+
+static double q8_elem(const uint8_t* cache, int64_t block, int kvh, int off, int d, int Hkv, int p, int D) {
+  const uint8_t* slab = cache + ((size_t)block * (size_t)Hkv + (size_t)kvh) * q8_slab_bytes(p, D);
+  const uint8_t* sc = slab + (size_t)p * D + 2 * ((size_t)off * (D / 32) + d / 32);
+  return (double)(int8_t)slab[(size_t)off * D + d] * f16_to_double((uint16_t)(sc[0] | (sc[1] << 8)));
+}
+
 /* Element offset of (physical block, kv head, token-in-block, dim) in one
  * HND pool [num_blocks, Hkv, p, D]. */
 static size_t kv_offset(int64_t block, int kvh, int off, int d, int Hkv, int p, int D) {
@@ -121,6 +202,38 @@ int oracle_kv_append(const uint16_t* k_new, const uint16_t* v_new, const int64_t
         size_t dst = kv_offset(block, h, off, d, num_kv_heads, block_size, head_dim);
         k_cache[dst] = k_new[src];
         v_cache[dst] = v_new[src];
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* KV append into q8_0 pages: the same scatter as oracle_kv_append, each
+ * (token, head) row of D values quantized in groups of 32 on the way in. */
+int oracle_kv_append_q8(const uint16_t* k_new, const uint16_t* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                        uint8_t* k_cache, uint8_t* v_cache, int64_t num_blocks, int block_size, int num_kv_heads,
+                        int head_dim) {
+  if (block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 32 || n_tokens < 0) return ORACLE_ERR_ARG;
+  const size_t slab = q8_slab_bytes(block_size, head_dim);
+  for (int64_t i = 0; i < n_tokens; ++i) {
+    int64_t slot = slot_mapping[i];
+    if (slot < 0) continue;
+    int64_t block = slot / block_size;
+    int off = (int)(slot % block_size);
+    if (block >= num_blocks) return ORACLE_ERR_INDEX;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      for (int which = 0; which < 2; ++which) {
+        const uint16_t* row = (which ? v_new : k_new) + ((size_t)i * num_kv_heads + h) * head_dim;
+        uint8_t* s = (which ? v_cache : k_cache) + ((size_t)block * num_kv_heads + h) * slab;
+        for (int g = 0; g < head_dim / 32; ++g) {
+          int8_t codes[32];
+          uint16_t scale;
+          quantize_group_q8(row + 32 * g, codes, &scale);
+          memcpy(s + (size_t)off * head_dim + 32 * g, codes, 32);
+          uint8_t* sc = s + (size_t)block_size * head_dim + 2 * ((size_t)off * (head_dim / 32) + g);
+          sc[0] = (uint8_t)(scale & 0xff);
+          sc[1] = (uint8_t)(scale >> 8);
+        }
       }
     }
   }
@@ -169,7 +282,18 @@ typedef struct {
   const int32_t* qo_indptr;
   int num_reqs, Hq, Hkv, D, p;
   double sm_scale;
+  const uint8_t* kq;  /* q8_0 pages instead of k_cache / v_cache, or NULL */
+  const uint8_t* vq;
 } attn_args;
+
+/* Element d of token `off` of block `block`, kv head kvh, of the K
+ * (which = 0) or V (which = 1) cache: a bf16 value, or a q8_0 code times
+ * its group's scale. */
+static double kv_elem(const attn_args* a, int which, int64_t block, int kvh, int off, int d) {
+  if (a->kq) return q8_elem(which ? a->vq : a->kq, block, kvh, off, d, a->Hkv, a->p, a->D);
+  const uint16_t* c = which ? a->v_cache : a->k_cache;
+  return bf16_to_double(c[kv_offset(block, kvh, off, d, a->Hkv, a->p, a->D)]);
+}
 
 /*
  * One output element set: query token `tok` (global index into q) of
@@ -194,7 +318,7 @@ static int attend_one(const attn_args* a, int r, int tok, int h, double* s, doub
     if (block < 0 || block >= a->num_blocks) return ORACLE_ERR_INDEX;
     double dot = 0.0;
     for (int d = 0; d < a->D; ++d)
-      dot += bf16_to_double(qv[d]) * bf16_to_double(a->k_cache[kv_offset(block, kvh, t % a->p, d, a->Hkv, a->p, a->D)]);
+      dot += bf16_to_double(qv[d]) * kv_elem(a, 0, block, kvh, t % a->p, d);
     s[t] = a->sm_scale * dot;
     if (s[t] > m) m = s[t];
   }
@@ -206,7 +330,7 @@ static int attend_one(const attn_args* a, int r, int tok, int h, double* s, doub
     double w = exp(s[t] - m);
     l += w;
     for (int d = 0; d < a->D; ++d)
-      o[d] += w * bf16_to_double(a->v_cache[kv_offset(block, kvh, t % a->p, d, a->Hkv, a->p, a->D)]);
+      o[d] += w * kv_elem(a, 1, block, kvh, t % a->p, d);
   }
   for (int d = 0; d < a->D; ++d) o[d] /= l;
   *lse = m + log(l);
@@ -237,30 +361,25 @@ static int request_of(const attn_args* a, int tok) {
  * n_threads * max_seq_len doubles for the scores; the caller provides it so
  * this file allocates nothing.
  */
-int oracle_attention_varlen(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_blocks,
-                            const int32_t* block_tables, int max_blocks_per_req, const int32_t* seq_lens,
-                            const int32_t* qo_indptr, int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
-                            int block_size, double sm_scale, double* out, double* lse, double* scratch,
-                            int max_seq_len, int n_threads) {
-  attn_args a = {q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
-                 num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, sm_scale};
-  int rc = check_args(&a);
+static int attention_all(const attn_args* a, double* out, double* lse, double* scratch, int max_seq_len,
+                         int n_threads) {
+  int rc = check_args(a);
   if (rc) return rc;
-  for (int r = 0; r < num_reqs; ++r)
-    if (seq_lens[r] > max_seq_len) return ORACLE_ERR_ARG;
-  int total_q = num_reqs > 0 ? qo_indptr[num_reqs] : 0;
-  long n_items = (long)total_q * num_q_heads;
+  for (int r = 0; r < a->num_reqs; ++r)
+    if (a->seq_lens[r] > max_seq_len) return ORACLE_ERR_ARG;
+  int total_q = a->num_reqs > 0 ? a->qo_indptr[a->num_reqs] : 0;
+  long n_items = (long)total_q * a->Hq;
   int err = ORACLE_OK;
 #pragma omp parallel for schedule(dynamic, 4) num_threads(n_threads)
   for (long it = 0; it < n_items; ++it) {
-    int tok = (int)(it / num_q_heads), h = (int)(it % num_q_heads);
+    int tok = (int)(it / a->Hq), h = (int)(it % a->Hq);
 #ifdef _OPENMP
     double* s = scratch + (size_t)omp_get_thread_num() * (size_t)max_seq_len;
 #else
     double* s = scratch;
 #endif
     double l_out;
-    int e = attend_one(&a, request_of(&a, tok), tok, h, s, out + (size_t)it * (size_t)head_dim, &l_out);
+    int e = attend_one(a, request_of(a, tok), tok, h, s, out + (size_t)it * (size_t)a->D, &l_out);
     if (lse) lse[it] = l_out;
     if (e) {
 #pragma omp atomic write
@@ -268,6 +387,29 @@ int oracle_attention_varlen(const uint16_t* q, const uint16_t* k_cache, const ui
     }
   }
   return err;
+}
+
+int oracle_attention_varlen(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_blocks,
+                            const int32_t* block_tables, int max_blocks_per_req, const int32_t* seq_lens,
+                            const int32_t* qo_indptr, int num_reqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, double sm_scale, double* out, double* lse, double* scratch,
+                            int max_seq_len, int n_threads) {
+  attn_args a = {q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
+                 num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, sm_scale, NULL, NULL};
+  return attention_all(&a, out, lse, scratch, max_seq_len, n_threads);
+}
+
+/* The same definition over q8_0 pages (each K and V element is its code
+ * times its group's scale). */
+int oracle_attention_varlen_q8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache, int64_t num_blocks,
+                               const int32_t* block_tables, int max_blocks_per_req, const int32_t* seq_lens,
+                               const int32_t* qo_indptr, int num_reqs, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, double sm_scale, double* out, double* lse,
+                               double* scratch, int max_seq_len, int n_threads) {
+  if (head_dim % 32) return ORACLE_ERR_ARG;
+  attn_args a = {q, NULL, NULL, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
+                 num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, sm_scale, k_cache, v_cache};
+  return attention_all(&a, out, lse, scratch, max_seq_len, n_threads);
 }
 
 /*
@@ -282,7 +424,7 @@ int oracle_attention_sampled(const uint16_t* q, const uint16_t* k_cache, const u
                              const int32_t* sample_head, double* out, double* lse, double* scratch, int max_seq_len,
                              int n_threads) {
   attn_args a = {q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
-                 num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, sm_scale};
+                 num_reqs, num_q_heads, num_kv_heads, head_dim, block_size, sm_scale, NULL, NULL};
   int rc = check_args(&a);
   if (rc) return rc;
   for (int r = 0; r < num_reqs; ++r)

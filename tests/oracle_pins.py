@@ -427,6 +427,125 @@ def pin_copy_on_write(o):
     assert not np.array_equal(out[0], out[1])
 
 
+def pin_f16_conversion(o):
+    """The oracle's binary32 -> binary16 rounding (used for the q8_0 scales)
+    agrees with numpy's IEEE conversion on random values across the range
+    and on the edge cases (ties, subnormals, the largest finite, overflow)."""
+    rng = np.random.default_rng(21)
+    x = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * np.float32(2.0) ** rng.integers(-30, 17, 4000),
+        np.array([0.0, -0.0, 1.0, 65504.0, 65519.0, 65520.0, 1e30, 2 ** -24, 2 ** -25, 3 * 2 ** -26,
+                  2 ** -14, 2 ** -14 * 0.9995, 1 + 2 ** -11, 1 + 3 * 2 ** -11, -2.5e-6], np.float32)])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([o.f32_to_f16(v) for v in x], np.uint16)
+    assert np.array_equal(got, ref), x[got != ref][:5]
+    for h in (0x0001, 0x03ff, 0x0400, 0x3c00, 0x7bff, 0xc248):
+        assert o.f16_value(h) == float(np.array([h], np.uint16).view(np.float16)[0])
+
+
+def pin_q8_layout_arithmetic(o=None):
+    """The q8_0 page layout reproduces the pages' byte counts: 34 bytes per
+    32 values (8.5 bits), so one 8K context drops from 1152 MiB to 612 MiB,
+    the 1188 MiB block-allocated long request to 631.125 MiB, and 16 such
+    requests need 9.86 GiB of the 12 GiB reserve."""
+    g = json.load(open(os.path.join(HERE, "golden", "q8_arithmetic.json")))
+    D, P = 128, 16
+    slab = oracle.q8_slab_bytes(P, D)
+    bf16_slab = P * D * 2
+    assert slab * 64 == bf16_slab * g["group"]["q8_bytes"]
+    assert slab * 8 / (P * D) == g["group"]["q8_bits_per_value"]
+    assert (P * D // 2 + P * (D // 32) * 2) * 8 / (P * D) == g["group"]["q4_bits_per_value"]
+    per_tok_bf16 = paging.kv_bytes_per_token(36, 8, 128, 2)
+    per_tok_q8 = 2 * 36 * 8 * (slab // P)
+    c = g["context_8k_mib"]
+    assert per_tok_bf16 * 8192 / 2 ** 20 == c["bf16"]
+    assert per_tok_q8 * 8192 / 2 ** 20 == c["q8"]
+    assert c["bf16"] - c["q8"] == c["q8_saved"] and c["bf16"] - c["q4"] == c["q8_saved"] + 288
+    lr = g["long_request_after_generation"]
+    assert per_tok_q8 * paging.reserved_tokens(8447, 16) / 2 ** 20 == lr["q8_mib"]
+    assert round(lr["requests"] * lr["q8_mib"] / 1024, 2) == lr["total_gib"] <= lr["reserve_gib"]
+
+
+def pin_q8_quantization(o):
+    """q8_0 codes and scales by their closed forms: the scale is the
+    binary16 of max|x| / 127 (numpy's conversion), the largest element of a
+    group gets code +-127, every value is within half a scale step of its
+    dequantized code, codes stay in [-127, 127], an all-zero group is zero."""
+    rng = np.random.default_rng(22)
+    x = workloads.normal_bf16(rng, (64, 128))
+    x[3, 32:64] = 0                                        # an all-zero group
+    x[5, :32] = bits(0.0)
+    x[5, 7] = bits(-3.0)                                    # one nonzero element
+    codes, scales = o.quantize_q8(x)
+    xv = oracle.bf16_to_f64(x).reshape(64, 4, 32)
+    cg = codes.astype(np.float64).reshape(64, 4, 32)
+    amax = np.abs(xv).max(axis=2)
+    ref_scale = (amax.astype(np.float32) / np.float32(127)).astype(np.float16)
+    assert np.array_equal(scales, ref_scale.view(np.uint16))
+    d16 = ref_scale.astype(np.float64)
+    assert np.all(np.abs(codes.astype(np.int32)) <= 127)
+    assert np.all(np.abs(xv - cg * d16[..., None]) <= d16[..., None] * (0.5 + 2 ** -20))
+    top = np.abs(xv).argmax(axis=2)
+    for i in range(64):
+        for gi in range(4):
+            if amax[i, gi] > 0:
+                assert cg[i, gi, top[i, gi]] == 127 * np.sign(xv[i, gi, top[i, gi]])
+    assert scales[3, 1] == 0 and not codes[3, 32:64].any()
+    assert codes[5, 7] == -127 and np.count_nonzero(codes[5, :32]) == 1
+
+
+def _q8_values(cache, P, D):
+    """Dequantized values [nb, Hkv, P, D] of q8_0 pages, decoded here from
+    the slab bytes (codes, then little-endian binary16 scales)."""
+    nb, Hkv, slab = cache.shape
+    codes = cache[:, :, :P * D].view(np.int8).reshape(nb, Hkv, P, D // 32, 32).astype(np.float64)
+    sc = cache[:, :, P * D:].copy().view(np.float16).reshape(nb, Hkv, P, D // 32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # never-written slots may hold NaN scales; they are not read
+        return (codes * sc[..., None]).reshape(nb, Hkv, P, D)
+
+
+def pin_q8_attention(o):
+    """q8_0 pages: kv_append_q8 stores what quantize_q8 gives, and attention
+    over q8_0 pages equals a numpy fp64 softmax attention over the values
+    decoded from the slab bytes (gathered through the block tables)."""
+    Hq, Hkv, P, D = 8, 2, 16, 64
+    b = workloads.make_batch([40, 17, 70], [1, 5, 1], num_blocks=16, seed=23, num_q_heads=Hq, num_kv_heads=Hkv,
+                             head_dim=D)
+    slab = oracle.q8_slab_bytes(P, D)
+    rng = np.random.default_rng(24)
+    kq = rng.integers(0, 256, (16, Hkv, slab)).astype(np.uint8)   # junk, then fill every token used
+    vq = kq.copy()
+    for r in range(b.num_reqs):
+        toks = workloads.normal_bf16(rng, (int(b.seq_lens[r]), 2, Hkv, D))
+        slots = np.array([b.block_tables[r, t // P] * P + t % P for t in range(int(b.seq_lens[r]))], np.int64)
+        o.kv_append_q8(toks[:, 0], toks[:, 1], slots, kq, vq)
+    one = workloads.normal_bf16(rng, (1, Hkv, D))
+    ck, sk = o.quantize_q8(one)
+    s0 = int(b.block_tables[0, 0]) * P
+    o.kv_append_q8(one, one, np.array([s0], np.int64), kq, vq)
+    got_codes = kq[s0 // P, :, :P * D].view(np.int8).reshape(Hkv, P, D)[:, 0]
+    got_scales = kq[s0 // P, :, P * D:].copy().view(np.uint16).reshape(Hkv, P, D // 32)[:, 0]
+    assert np.array_equal(got_codes, ck[0]) and np.array_equal(got_scales, sk[0])
+    out, lse = o.attention_varlen_q8(b.q, kq, vq, b.block_tables, b.seq_lens, b.qo_indptr, b.sm_scale)
+    Kv, Vv = _q8_values(kq, P, D), _q8_values(vq, P, D)
+    qv = oracle.bf16_to_f64(b.q)
+    for r in range(b.num_reqs):
+        L = int(b.seq_lens[r])
+        c = int(b.qo_indptr[r + 1] - b.qo_indptr[r])
+        Kr = np.stack([Kv[b.block_tables[r, t // P], :, t % P] for t in range(L)])   # [L, Hkv, D]
+        Vr = np.stack([Vv[b.block_tables[r, t // P], :, t % P] for t in range(L)])
+        for j in range(c):
+            tok = int(b.qo_indptr[r]) + j
+            n = L - c + j + 1
+            for h in range(Hq):
+                sc = b.sm_scale * Kr[:n, h // (Hq // Hkv)] @ qv[tok, h]
+                w = np.exp(sc - sc.max())
+                ref = w @ Vr[:n, h // (Hq // Hkv)] / w.sum()
+                assert np.allclose(out[tok, h], ref, rtol=1e-10, atol=1e-12), (r, j, h)
+                assert abs(lse[tok, h] - (sc.max() + np.log(w.sum()))) < 1e-10
+
+
 def pin_brute_force(o):
     """Cross-check against the pure-Python fp64 restatement (oracle/brute.py)
     on a tiny mixed batch (decode rows and a chunk)."""
@@ -452,7 +571,8 @@ def pin_sampled_matches_full(o):
 ALL_PINS = [pin_page_arithmetic, pin_round_bf16, pin_single_key, pin_one_hot_score, pin_two_key_sigmoid,
             pin_uniform_scores, pin_gqa_grouping, pin_scipy_dense, pin_page_permutation,
             pin_shared_equals_duplicated, pin_chunked_equals_oneshot, pin_merge_identity, pin_append_then_read,
-            pin_copy_on_write, pin_brute_force, pin_sampled_matches_full]
+            pin_copy_on_write, pin_f16_conversion, pin_q8_layout_arithmetic, pin_q8_quantization, pin_q8_attention,
+            pin_brute_force, pin_sampled_matches_full]
 
 
 def run_all(o) -> list:

@@ -20,12 +20,17 @@ MUTANTS = {
     "gqa_interleaved": ("int kvh = h / G;", "int kvh = h % a->Hkv;"),
     "scale_dropped": ("s[t] = a->sm_scale * dot;", "s[t] = dot;"),
     "softmax_sign": ("double w = exp(s[t] - m);", "double w = exp(m - s[t]);"),
-    "values_from_keys": ("o[d] += w * bf16_to_double(a->v_cache[", "o[d] += w * bf16_to_double(a->k_cache["),
+    "values_from_keys": ("o[d] += w * kv_elem(a, 1,", "o[d] += w * kv_elem(a, 0,"),
     "page_index_mod": ("int64_t block = table[t / a->p];\n    if", "int64_t block = table[(t / a->p) % 2];\n    if"),
     "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
     "nhd_layout": ("return (((size_t)block * (size_t)Hkv + (size_t)kvh) * (size_t)p + (size_t)off) * (size_t)D",
                    "return (((size_t)block * (size_t)p + (size_t)off) * (size_t)Hkv + (size_t)kvh) * (size_t)D"),
-    "append_offset": ("int off = (int)(slot % block_size);", "int off = (int)((slot + 1) % block_size);"),
+    "append_offset": ("    int off = (int)(slot % block_size);\n    if (block >= num_blocks) return ORACLE_ERR_INDEX;\n"
+                      "    for (int h = 0; h < num_kv_heads; ++h) {\n      for (int d = 0;",
+                      "    int off = (int)((slot + 1) % block_size);\n    if (block >= num_blocks) return ORACLE_ERR_INDEX;\n"
+                      "    for (int h = 0; h < num_kv_heads; ++h) {\n      for (int d = 0;"),
+    "q8_append_offset": ("          memcpy(s + (size_t)off * head_dim + 32 * g, codes, 32);",
+                         "          memcpy(s + (size_t)((off + 1) % block_size) * head_dim + 32 * g, codes, 32);"),
     "merge_weight_sign": ("double wa = exp(la - M), wb = exp(lb - M);", "double wa = exp(M - la), wb = exp(lb - M);"),
     "merge_lse_dropped": ("lse_out[i] = M + log(wa + wb);", "lse_out[i] = M;"),
     "normalise_dropped": ("for (int d = 0; d < a->D; ++d) o[d] /= l;", ""),
@@ -34,6 +39,11 @@ MUTANTS = {
     "copy_one_head": ("    for (int h = 0; h < num_kv_heads; ++h)\n      for (int off = 0; off < block_size; ++off)",
                       "    for (int h = 0; h < 1; ++h)\n      for (int off = 0; off < block_size; ++off)"),
     "copy_reversed": ("          k_cache[to] = k_cache[from];", "          k_cache[from] = k_cache[to];"),
+    "q8_scale_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "q8_code_trunc": ("float t = rintf((float)bf16_to_double(x[i]) / d16);",
+                      "float t = truncf((float)bf16_to_double(x[i]) / d16);"),
+    "q8_scale_index": ("2 * ((size_t)off * (D / 32) + d / 32)", "2 * ((size_t)off * (D / 32) + d / 64)"),
+    "f16_round_trunc": ("r = ldexp(rint(ldexp(m, 11)), e - 11);", "r = ldexp(trunc(ldexp(m, 11)), e - 11);"),
 }
 
 
