@@ -362,6 +362,8 @@ def main():
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--contexts", default="2048,8192", help="sweep contexts")
     ap.add_argument("--batches", default="1,8,32,64,128", help="sweep decode batch sizes")
+    ap.add_argument("--kv", choices=["bf16", "q8"], default="bf16",
+                    help="KV page format: bf16, or q8_0 (decode workloads only)")
     ap.add_argument("--no-cascade", action="store_true",
                     help="run shared-prefix batches through pa_attention_varlen instead of the shared-prefix call")
     args = ap.parse_args()
@@ -388,8 +390,11 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     batch = W.workload_batch(args.workload, seed_offset=rank)
-    ppages = 0 if args.no_cascade else batch.meta["shared_prefix_tokens"] // 16
-    sb = W.step_bytes(batch, ppages)
+    q8 = args.kv == "q8"
+    if q8 and np.any(np.diff(batch.qo_indptr) > 1):
+        raise SystemExit("--kv q8 serves decode rows only; this workload has rows with qo_len > 1")
+    ppages = 0 if (args.no_cascade or q8) else batch.meta["shared_prefix_tokens"] // 16
+    sb = W.step_bytes(batch, ppages, kv=args.kv)
 
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
@@ -402,8 +407,21 @@ def main():
         "qo_indptr": torch.from_numpy(batch.qo_indptr).pin_memory(),
     }
     d = {k: v.to(dev) for k, v in host.items()}
-    k_cache = bf(batch.k_cache).to(dev)
-    v_cache = bf(batch.v_cache).to(dev)
+    if q8:
+        # q8_0 pools: every cached token quantized into its slot once, on the GPU
+        nb, Hkv = batch.k_cache.shape[:2]
+        k_cache = B.new_q8_pool(nb, Hkv, dev)
+        v_cache = B.new_q8_pool(nb, Hkv, dev)
+        for r in range(batch.num_reqs):
+            L = int(batch.seq_lens[r]) - int(batch.qo_indptr[r + 1] - batch.qo_indptr[r])
+            t = np.arange(L)
+            blk = batch.block_tables[r, t // 16].astype(np.int64)
+            B.pa_kv_append_q8(bf(batch.k_cache[blk, :, t % 16]).to(dev), bf(batch.v_cache[blk, :, t % 16]).to(dev),
+                              torch.from_numpy(blk * 16 + t % 16).to(dev), k_cache, v_cache)
+        torch.cuda.synchronize()
+    else:
+        k_cache = bf(batch.k_cache).to(dev)
+        v_cache = bf(batch.v_cache).to(dev)
     out = torch.empty_like(d["q"])
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     R, total_q = batch.num_reqs, batch.total_q
@@ -419,6 +437,12 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step(src):
+        if q8:
+            B.pa_kv_append_q8(src["k_new"], src["v_new"], src["slot_mapping"], k_cache, v_cache, workspace=ws_app)
+            B.pa_attention_varlen_q8(src["q"], k_cache, v_cache, src["block_tables"], src["seq_lens"],
+                                     src["qo_indptr"], batch.sm_scale, seq_lens_host=seq_h, qo_indptr_host=ind_h,
+                                     out=out, workspace=ws)
+            return
         B.pa_kv_append(src["k_new"], src["v_new"], src["slot_mapping"], k_cache, v_cache, workspace=ws_app)
         attention(B, ppages, src["q"], k_cache, v_cache, src["block_tables"], src["seq_lens"], src["qo_indptr"],
                   batch.sm_scale, seq_h, ind_h, out, ws)
@@ -536,6 +560,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(t_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": f"replicas x{world}",
+                   "kv_format": "q8_0 (34 of 64 bytes per 32 values)" if q8 else "bf16",
                    "l2": "flushed between timed steps (256 MiB read outside the events)",
                    "attention_call": call_name(ppages),
                    "bytes_per_step": sb["unique"], "logical_bytes_per_step": sb["logical"],
@@ -545,7 +570,7 @@ def main():
         "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2) if achieved else None,
                      "peak": r_peak, "peak_source": r_source, "unit": r_unit,
                      "frac": round(achieved / r_peak, 4) if achieved else None,
-                     "traffic": profiled_traffic(args.workload) if dom == "decode" else None,
+                     "traffic": profiled_traffic(args.workload) if dom == "decode" and not q8 else None,
                      "algorithmic_bytes_per_launch": dom_bytes,
                      **({"algorithmic_flops_per_launch": dom_flops} if dom_flops else {}),
                      "avg_launch_ms": round(dom_ms, 5) if dom_ms else None,

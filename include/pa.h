@@ -100,6 +100,50 @@ pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot
                        int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * q8_0 KV pages ("Inference optimisation", AI-infra book ch. 8, §8.4.2 and
+ * Fig. 8-23: every 32 values share one 2-byte scale next to their 8-bit
+ * codes, 34 bytes instead of 64).  A q8_0 pool is
+ * [num_blocks, num_kv_heads, PA_Q8_SLAB_BYTES] bytes: one (block, kv head)
+ * slab holds block_size x head_dim int8 codes (token t, dim d at
+ * t * head_dim + d), then block_size x head_dim / 32 little-endian binary16
+ * scales (token t, group g = d / 32 at byte block_size * head_dim +
+ * 2 * (t * head_dim / 32 + g)).  Per group: d = max|x| / 127 in binary32,
+ * stored as binary16 rounded to nearest even; code = rint(x / d16) in
+ * binary32 with d16 the stored scale, clamped to [-127, 127]; all codes 0
+ * when d16 is 0.  A code stands for code * d16.  Inputs must be finite.
+ */
+#define PA_Q8_SLAB_BYTES (PA_BLOCK_SIZE * PA_HEAD_DIM + PA_BLOCK_SIZE * (PA_HEAD_DIM / 32) * 2) /* 2176 */
+
+/*
+ * pa_kv_append_q8 -- pa_kv_append into q8_0 pools: each (token, kv head)
+ * row of k_new / v_new is quantized in groups of 32 as described above and
+ * stored with its scales in the slot's page.  Same arguments, validation and
+ * error word as pa_kv_append; k_cache and v_cache are q8_0 pools
+ * (16-byte aligned).
+ */
+pa_status pa_kv_append_q8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                          void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                          int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_attention_varlen_q8 -- pa_attention_varlen over q8_0 pools, for decode
+ * rows: every K and V element is its code times its group's scale, the rest
+ * of the definition is unchanged (fp32 arithmetic, bf16 out, natural-log
+ * lse).  Rows with qo_len > 1 give PA_ERR_UNSUPPORTED; rows with qo_len = 0
+ * are skipped.  Workspace as pa_attention_varlen
+ * (pa_attention_workspace_size).  Reading 34 instead of 64 bytes per 32
+ * values shortens the HBM-bound decode when the saved read time exceeds
+ * the added dequantization (the pages' Delta T = Delta D / beta - T_c).
+ */
+pa_status pa_attention_varlen_q8(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                                 const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* seq_lens,
+                                 const int32_t* qo_indptr, const int32_t* seq_lens_host,
+                                 const int32_t* qo_indptr_host, int32_t num_reqs, int32_t total_q,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 float sm_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 pa_stream_t stream);
+
+/*
  * pa_copy_blocks -- copy-on-write block copy ("Inference optimisation",
  * AI-infra book ch. 8, §8.3.2 and Fig. 8-15: before a branch writes into a
  * block it shares with another request, it gets its own copy of that block,

@@ -49,6 +49,9 @@ _SIGS = {
     "pa_last_error_message": (ctypes.c_char_p, []),
     "pa_kv_append": (_i32, [_P, _P, _P, _i64, _P, _P, _i64, _i32, _i32, _i32, _P, _sz, _P]),
     "pa_copy_blocks": (_i32, [_P, _P, _i64, _P, _P, _i64, _i32, _i32, _i32, _P, _sz, _P]),
+    "pa_kv_append_q8": (_i32, [_P, _P, _P, _i64, _P, _P, _i64, _i32, _i32, _i32, _P, _sz, _P]),
+    "pa_attention_varlen_q8": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32,
+                                      _i32, _f32, _P, _P, _P, _sz, _P]),
     "pa_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pa_attention_varlen": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _f32, _P, _P, _P, _sz, _P]),
@@ -130,6 +133,69 @@ def pa_kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, workspace=None, s
     _check(_lib.pa_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache), _ptr(v_cache), nb, P,
                              Hkv, D, _ptr(workspace), workspace.numel(), _stream(stream)))
     return workspace
+
+
+PA_Q8_SLAB_BYTES = 16 * 128 + 16 * (128 // 32) * 2
+
+
+def new_q8_pool(num_blocks, num_kv_heads, device):
+    """An empty q8_0 pool [num_blocks, Hkv, PA_Q8_SLAB_BYTES] (uint8)."""
+    return torch.zeros((num_blocks, num_kv_heads, PA_Q8_SLAB_BYTES), dtype=torch.uint8, device=device)
+
+
+def pa_kv_append_q8(k_new, v_new, slot_mapping, k_cache, v_cache, workspace=None, stream=None):
+    """Quantize k_new / v_new [N, Hkv, D] bf16 into q8_0 pools (uint8
+    [num_blocks, Hkv, PA_Q8_SLAB_BYTES]) at slot_mapping (int64 [N])."""
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    N, Hkv, D = k_new.shape
+    nb = k_cache.shape[0]
+    if v_new.shape != k_new.shape or v_cache.shape != k_cache.shape or k_cache.shape[1:] != (Hkv, PA_Q8_SLAB_BYTES) \
+            or slot_mapping.shape != (N,):
+        raise ValueError("inconsistent shapes")
+    if workspace is None:
+        workspace = new_workspace(PA_ERROR_WORD_BYTES, k_cache.device)
+    _check(_lib.pa_kv_append_q8(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache), _ptr(v_cache), nb,
+                                16, Hkv, D, _ptr(workspace), workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def pa_attention_varlen_q8(q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, sm_scale, *, seq_lens_host=None,
+                           qo_indptr_host=None, out=None, lse=None, workspace=None, stream=None, return_lse=False):
+    """pa_attention_varlen over q8_0 pools (decode rows)."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(qo_indptr, torch.int32, "qo_indptr")
+    total_q, Hq, D = q.shape
+    nb, Hkv, slab = k_cache.shape
+    R = seq_lens.shape[0]
+    if v_cache.shape != k_cache.shape or slab != PA_Q8_SLAB_BYTES or qo_indptr.shape != (R + 1,) \
+            or block_tables.dim() != 2 or block_tables.shape[0] != R:
+        raise ValueError("inconsistent shapes")
+    slh = _host_i32(seq_lens if seq_lens_host is None else seq_lens_host)
+    qih = _host_i32(qo_indptr if qo_indptr_host is None else qo_indptr_host)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    if workspace is None:
+        max_len = int(slh.max()) if R else 1
+        workspace = new_workspace(pa_attention_workspace_size(R, total_q, Hq, D, max_len), q.device)
+    _check(_lib.pa_attention_varlen_q8(_ptr(q), _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables),
+                                       block_tables.shape[1], _ptr(seq_lens), _ptr(qo_indptr),
+                                       ctypes.c_void_p(slh.data_ptr()), ctypes.c_void_p(qih.data_ptr()), R, total_q,
+                                       Hq, Hkv, D, 16, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       workspace.numel(), _stream(stream)))
+    return (out, lse) if (return_lse or lse is not None) else out
 
 
 def pa_copy_blocks(src_blocks, dst_blocks, k_cache, v_cache, workspace=None, stream=None):

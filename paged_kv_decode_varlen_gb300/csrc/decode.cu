@@ -65,9 +65,15 @@ struct Item {        // one request's pages within this CTA's segment
   int32_t tok;      // its query token
 };
 
+// Bytes of one (page, kv head) slab: bf16 pages, or q8_0 pages (16 x 128
+// int8 codes, then 16 x 4 binary16 group scales).
+constexpr int kQ8SlabBytes = kPage * kHeadDim + kPage * (kHeadDim / 32) * 2;  // 2176
+static_assert(kQ8SlabBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+
+template <int kSlab>
 struct __align__(128) DecodeSmem {
-  uint8_t k[kStages][kSlabBytes];
-  uint8_t v[kStages][kSlabBytes];
+  uint8_t k[kStages][kSlab];
+  uint8_t v[kStages][kSlab];
   uint64_t full[kStages];   // TMA landed
   int readers[kStages];     // warps done reading the stage's current page
   int32_t ids[kDecodeMaxPagesPerCta];
@@ -114,6 +120,75 @@ __device__ __forceinline__ void qk16(const float2 (&qp)[2][16], const uint4& ka,
   }
   s01 = __fadd2_rn(a0, a1);
   s23 = __fadd2_rn(c0, c1);
+}
+
+// q8_0 pages: 8 int8 codes (dims 8c..8c+7 or 64+8c..) -> 8 floats.
+__device__ __forceinline__ void codes8(const uint2& w, float* f) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[i] = (float)(int8_t)((w.x >> (8 * i)) & 0xffu);
+    f[4 + i] = (float)(int8_t)((w.y >> (8 * i)) & 0xffu);
+  }
+}
+
+// qk16 over q8_0 codes: the dims of ka lie in one 32-value group (scale
+// dA), those of kb in another (dB); each group's partial dot product is
+// scaled once.
+__device__ __forceinline__ void qk16_q8(const float2 (&qp)[2][16], const uint2& ka, const uint2& kb, float dA,
+                                        float dB, float2& s01, float2& s23) {
+  float kf[16];
+  codes8(ka, kf);
+  codes8(kb, kf + 8);
+  float2 a0 = __fmul2_rn(qp[0][0], make_float2(kf[0], kf[0]));
+  float2 a1 = __fmul2_rn(qp[0][1], make_float2(kf[1], kf[1]));
+  float2 c0 = __fmul2_rn(qp[1][0], make_float2(kf[0], kf[0]));
+  float2 c1 = __fmul2_rn(qp[1][1], make_float2(kf[1], kf[1]));
+  float2 e0 = __fmul2_rn(qp[0][8], make_float2(kf[8], kf[8]));
+  float2 e1 = __fmul2_rn(qp[0][9], make_float2(kf[9], kf[9]));
+  float2 g0 = __fmul2_rn(qp[1][8], make_float2(kf[8], kf[8]));
+  float2 g1 = __fmul2_rn(qp[1][9], make_float2(kf[9], kf[9]));
+#pragma unroll
+  for (int i = 2; i < 8; i += 2) {
+    a0 = __ffma2_rn(qp[0][i], make_float2(kf[i], kf[i]), a0);
+    a1 = __ffma2_rn(qp[0][i + 1], make_float2(kf[i + 1], kf[i + 1]), a1);
+    c0 = __ffma2_rn(qp[1][i], make_float2(kf[i], kf[i]), c0);
+    c1 = __ffma2_rn(qp[1][i + 1], make_float2(kf[i + 1], kf[i + 1]), c1);
+    e0 = __ffma2_rn(qp[0][8 + i], make_float2(kf[8 + i], kf[8 + i]), e0);
+    e1 = __ffma2_rn(qp[0][9 + i], make_float2(kf[9 + i], kf[9 + i]), e1);
+    g0 = __ffma2_rn(qp[1][8 + i], make_float2(kf[8 + i], kf[8 + i]), g0);
+    g1 = __ffma2_rn(qp[1][9 + i], make_float2(kf[9 + i], kf[9 + i]), g1);
+  }
+  const float2 dA2 = make_float2(dA, dA), dB2 = make_float2(dB, dB);
+  s01 = __ffma2_rn(dA2, __fadd2_rn(a0, a1), __fmul2_rn(dB2, __fadd2_rn(e0, e1)));
+  s23 = __ffma2_rn(dA2, __fadd2_rn(c0, c1), __fmul2_rn(dB2, __fadd2_rn(g0, g1)));
+}
+
+// pv16 over q8_0 codes: each head's weight is scaled by the group scale of
+// the dims it multiplies.
+__device__ __forceinline__ void pv16_q8(float2 (&acc)[kGroup][8], const float (&pg)[kGroup], const uint2& va,
+                                        const uint2& vb, float dA, float dB) {
+  float vf[16];
+  codes8(va, vf);
+  codes8(vb, vf + 8);
+#pragma unroll
+  for (int g = 0; g < kGroup; ++g) {
+    const float2 pa2 = make_float2(pg[g] * dA, pg[g] * dA), pb2 = make_float2(pg[g] * dB, pg[g] * dB);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[g][j] = __ffma2_rn(pa2, make_float2(vf[2 * j], vf[2 * j + 1]), acc[g][j]);
+      acc[g][4 + j] = __ffma2_rn(pb2, make_float2(vf[8 + 2 * j], vf[9 + 2 * j]), acc[g][4 + j]);
+    }
+  }
+}
+
+// The group scales of token slot ts of a q8_0 slab that thread chunk c
+// needs: dims 8c.. lie in group c / 4, dims 64 + 8c.. in group 2 + c / 4.
+__device__ __forceinline__ void q8_scales(const uint8_t* slab, int ts, int c, float& dA, float& dB) {
+  const uint2 w = *reinterpret_cast<const uint2*>(slab + kPage * kHeadDim + ts * 8);
+  const uint32_t lo = (c >> 2) ? (w.x >> 16) : (w.x & 0xffffu);
+  const uint32_t hi = (c >> 2) ? (w.y >> 16) : (w.y & 0xffffu);
+  dA = __half2float(__ushort_as_half((unsigned short)lo));
+  dB = __half2float(__ushort_as_half((unsigned short)hi));
 }
 
 __device__ __forceinline__ void pv16(float2 (&acc)[kGroup][8], const float (&pg)[kGroup], const uint4& va,
@@ -174,14 +249,17 @@ __device__ __forceinline__ float fold_prefix(const DecodeParams& p, float4& o, f
   return M + log2f(wsum);
 }
 
+template <bool kQ8>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_kernel(const DecodeParams p, const __grid_constant__ DecodePlan plan) {
+  constexpr int kSlab = kQ8 ? kQ8SlabBytes : kSlabBytes;
+  using Smem = DecodeSmem<kSlab>;
   // No early launch of the next kernel: this grid is one wave sized to fill
   // every SM, and CTAs of a dependent kernel arriving early would take slots
   // its own CTAs need.  The next kernel is released as the CTAs exit.
   pdl_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.num_kv_heads;
@@ -281,14 +359,15 @@ __global__ void __launch_bounds__(kThreads, 3)
   const bool ids_ok = __syncthreads_and(ok) != 0;
   const int n_cov = sm.n_cov;
 
-  const size_t slab_elems = (size_t)kPage * kHeadDim;
+  const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_cache);
+  const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v_cache);
   // segment page i -> stage i % kStages (K and V slabs of kv head kvh)
   auto issue = [&](int i) {
     const int s = i & (kStages - 1);
-    const size_t off = ((size_t)max(sm.ids[i], 0) * Hkv + kvh) * slab_elems;
-    mbar_arrive_expect_tx(&sm.full[s], 2 * kSlabBytes);
-    bulk_g2s(sm.k[s], p.k_cache + off, kSlabBytes, &sm.full[s]);
-    bulk_g2s(sm.v[s], p.v_cache + off, kSlabBytes, &sm.full[s]);
+    const size_t off = ((size_t)max(sm.ids[i], 0) * Hkv + kvh) * kSlab;
+    mbar_arrive_expect_tx(&sm.full[s], 2 * kSlab);
+    bulk_g2s(sm.k[s], kbase + off, kSlab, &sm.full[s]);
+    bulk_g2s(sm.v[s], vbase + off, kSlab, &sm.full[s]);
     sm.stage_page[s] = i;  // one issuer per stage at a time
   };
   if (tid == 0) {
@@ -372,7 +451,20 @@ __global__ void __launch_bounds__(kThreads, 3)
       // a missing second page reads whatever stage sb holds; its scores are
       // masked below and its V is not read
       float2 sA01, sA23, sB01, sB23;
-      {
+      float vdA0 = 0.f, vdB0 = 0.f, vdA1 = 0.f, vdB1 = 0.f;  // q8_0: V group scales of the two pages
+      if constexpr (kQ8) {
+        const uint8_t* kr0 = sm.k[sa] + ts * kHeadDim;
+        const uint8_t* kr1 = sm.k[sb] + ts * kHeadDim;
+        float kdA0, kdB0, kdA1, kdB1;
+        q8_scales(sm.k[sa], ts, c, kdA0, kdB0);
+        q8_scales(sm.k[sb], ts, c, kdA1, kdB1);
+        q8_scales(sm.v[sa], ts, c, vdA0, vdB0);
+        q8_scales(sm.v[sb], ts, c, vdA1, vdB1);
+        qk16_q8(qp, *reinterpret_cast<const uint2*>(kr0 + 8 * c), *reinterpret_cast<const uint2*>(kr0 + 64 + 8 * c),
+                kdA0, kdB0, sA01, sA23);
+        qk16_q8(qp, *reinterpret_cast<const uint2*>(kr1 + 8 * c), *reinterpret_cast<const uint2*>(kr1 + 64 + 8 * c),
+                kdA1, kdB1, sB01, sB23);
+      } else {
         const uint8_t* kr0 = sm.k[sa] + ts * (kHeadDim * 2);
         const uint8_t* kr1 = sm.k[sb] + ts * (kHeadDim * 2);
         const uint4 ka0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
@@ -420,15 +512,28 @@ __global__ void __launch_bounds__(kThreads, 3)
         pA[g] = __shfl_sync(0xffffffffu, pown, src);
         pB[g] = __shfl_sync(0xffffffffu, pown, src + 1);
       }
-      if (valid0) {
-        const uint8_t* vr = sm.v[sa] + ts * (kHeadDim * 2);
-        pv16(acc, pA, *reinterpret_cast<const uint4*>(vr + 16 * c),
-             *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
-      }
-      if (valid1) {
-        const uint8_t* vr = sm.v[sb] + ts * (kHeadDim * 2);
-        pv16(acc, pB, *reinterpret_cast<const uint4*>(vr + 16 * c),
-             *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
+      if constexpr (kQ8) {
+        if (valid0) {
+          const uint8_t* vr = sm.v[sa] + ts * kHeadDim;
+          pv16_q8(acc, pA, *reinterpret_cast<const uint2*>(vr + 8 * c),
+                  *reinterpret_cast<const uint2*>(vr + 64 + 8 * c), vdA0, vdB0);
+        }
+        if (valid1) {
+          const uint8_t* vr = sm.v[sb] + ts * kHeadDim;
+          pv16_q8(acc, pB, *reinterpret_cast<const uint2*>(vr + 8 * c),
+                  *reinterpret_cast<const uint2*>(vr + 64 + 8 * c), vdA1, vdB1);
+        }
+      } else {
+        if (valid0) {
+          const uint8_t* vr = sm.v[sa] + ts * (kHeadDim * 2);
+          pv16(acc, pA, *reinterpret_cast<const uint4*>(vr + 16 * c),
+               *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
+        }
+        if (valid1) {
+          const uint8_t* vr = sm.v[sb] + ts * (kHeadDim * 2);
+          pv16(acc, pB, *reinterpret_cast<const uint4*>(vr + 16 * c),
+               *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
+        }
       }
       __syncwarp();
       if (lane == 0) {  // this warp is done with the iteration's pages
@@ -629,20 +734,26 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-bool g_decode_attr_set[64] = {};
+bool g_decode_attr_set[2][64] = {};
 
-}  // namespace
-
-cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream) {
+template <bool kQ8>
+cudaError_t launch_decode_as(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream) {
+  constexpr size_t kSmem = sizeof(DecodeSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !g_decode_attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(DecodeSmem));
+  if (dev < 64 && !g_decode_attr_set[kQ8][dev]) {
+    e = cudaFuncSetAttribute(decode_kernel<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
-    g_decode_attr_set[dev] = true;
+    g_decode_attr_set[kQ8][dev] = true;
   }
-  return launch_pdl(decode_kernel, dim3(grid), dim3(kThreads), sizeof(DecodeSmem), stream, p, plan);
+  return launch_pdl(decode_kernel<kQ8>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, cudaStream_t stream) {
+  return q8 ? launch_decode_as<true>(p, plan, grid, stream) : launch_decode_as<false>(p, plan, grid, stream);
 }
 
 }  // namespace pa

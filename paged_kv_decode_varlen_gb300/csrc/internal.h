@@ -160,8 +160,9 @@ pa_status set_error(pa_status s, const char* fmt, ...);
 
 // Each launcher enqueues one kernel on `stream` and returns its launch error.
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_kv_append_q8(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
                            cudaStream_t stream);
 cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream);

@@ -303,15 +303,16 @@ pa_status pa::set_error(pa_status s, const char* fmt, ...) {
 
 namespace {
 
-// Both attention entry points.  prefix_pages > 0: the first prefix_pages
+// The attention entry points.  prefix_pages > 0: the first prefix_pages
 // pages of every request are one shared prefix, attended once for all
-// queries by the prefix pass and folded into each row's own part.
+// queries by the prefix pass and folded into each row's own part.  q8: the
+// pools hold q8_0 pages (decode rows only).
 pa_status attention(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
                     const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* seq_lens,
                     const int32_t* qo_indptr, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
                     int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t block_size, int32_t prefix_pages, float sm_scale, void* out, float* lse, void* workspace,
-                    size_t workspace_bytes, cudaStream_t stream) {
+                    size_t workspace_bytes, cudaStream_t stream, bool q8 = false) {
   pa_status s = check_shape(num_q_heads, num_kv_heads, head_dim, block_size);
   if (s != PA_OK) return s;
   if (num_reqs < 0 || num_reqs > 65535) return fail(PA_ERR_INVALID_ARG, "num_reqs %d outside [0, 65535]", num_reqs);
@@ -351,6 +352,8 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
       return fail(PA_ERR_INVALID_ARG, "request %d: %d pages > max_blocks_per_req %d", r, pages_of(L),
                   max_blocks_per_req);
     max_len = std::max(max_len, L);
+    if (q8 && qo_len > 1)
+      return fail(PA_ERR_UNSUPPORTED, "request %d: q8_0 pages serve decode rows only (qo_len %d)", r, qo_len);
     if (qo_len > 0) {
       if (first_active < 0) first_active = r;
       ++active;
@@ -504,12 +507,16 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
                                    plan);
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
-      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, stream); });
+      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, q8, stream); });
       if (s != PA_OK) return s;
     }
   }
   return ok();
 }
+
+pa_status append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens, void* k_cache,
+                 void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                 void* workspace, size_t workspace_bytes, pa_stream_t stream, bool q8);
 
 }  // namespace
 
@@ -535,6 +542,36 @@ const char* pa_last_error_message(void) { return g_msg; }
 pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
                        void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                        int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  return append(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
+                head_dim, workspace, workspace_bytes, stream, false);
+}
+
+pa_status pa_kv_append_q8(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens,
+                          void* k_cache, void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                          int32_t head_dim, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  return append(k_new, v_new, slot_mapping, n_tokens, k_cache, v_cache, num_blocks, block_size, num_kv_heads,
+                head_dim, workspace, workspace_bytes, stream, true);
+}
+
+pa_status pa_attention_varlen_q8(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
+                                 const int32_t* block_tables, int32_t max_blocks_per_req, const int32_t* seq_lens,
+                                 const int32_t* qo_indptr, const int32_t* seq_lens_host,
+                                 const int32_t* qo_indptr_host, int32_t num_reqs, int32_t total_q,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 float sm_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 pa_stream_t stream) {
+  return attention(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
+                   seq_lens_host, qo_indptr_host, num_reqs, total_q, num_q_heads, num_kv_heads, head_dim, block_size,
+                   0, sm_scale, out, lse, workspace, workspace_bytes, stream, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+pa_status append(const void* k_new, const void* v_new, const int64_t* slot_mapping, int64_t n_tokens, void* k_cache,
+                 void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                 void* workspace, size_t workspace_bytes, pa_stream_t stream, bool q8) {
   if (n_tokens < 0) return fail(PA_ERR_INVALID_ARG, "n_tokens %lld < 0", (long long)n_tokens);
   if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
   pa_status s = check_shape(PA_GQA_GROUP * num_kv_heads, num_kv_heads, head_dim, block_size);
@@ -557,9 +594,14 @@ pa_status pa_kv_append(const void* k_new, const void* v_new, const int64_t* slot
   p.num_blocks = num_blocks;
   p.num_kv_heads = num_kv_heads;
   p.err = static_cast<int*>(workspace);
-  s = run_launch(PA_KERNEL_KV_APPEND, "kv_append", stream, [&] { return pa::launch_kv_append(p, stream); });
+  s = run_launch(PA_KERNEL_KV_APPEND, q8 ? "kv_append_q8" : "kv_append", stream,
+                 [&] { return q8 ? pa::launch_kv_append_q8(p, stream) : pa::launch_kv_append(p, stream); });
   return s == PA_OK ? ok() : s;
 }
+
+}  // namespace
+
+extern "C" {
 
 pa_status pa_copy_blocks(const int32_t* src_blocks, const int32_t* dst_blocks, int64_t n_pairs, void* k_cache,
                          void* v_cache, int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,

@@ -238,10 +238,13 @@ def sweep_point(batch: int, context: int, *, seed: int = SEED0 + 5) -> dict:
 # the pages after the prefix, and the prefix pass reads the prefix pages once
 # plus every query.
 # ---------------------------------------------------------------------------
-def step_bytes(b: Batch, prefix_pages: int = 0) -> dict:
+def step_bytes(b: Batch, prefix_pages: int = 0, kv: str = "bf16") -> dict:
+    """kv = "q8": the pools hold q8_0 pages ("Inference optimisation"
+    §8.4.2): 34 bytes per 32 values instead of 64."""
     total_q, Hq, D = b.q.shape
     _, Hkv, P, _ = b.k_cache.shape
-    per_tok = 2 * Hkv * D * 2
+    per_tok = 2 * Hkv * D * 2 if kv == "bf16" else 2 * Hkv * (D + D // 32 * 2)
+    new_tok = 2 * Hkv * D * 2           # the step's new K/V arrive as bf16
     qo = np.diff(b.qo_indptr)
     active = qo > 0
     seq = b.seq_lens.astype(np.int64)
@@ -258,7 +261,7 @@ def step_bytes(b: Batch, prefix_pages: int = 0) -> dict:
     qo_bytes = 2 * total_q * Hq * D * 2
     table_bytes = int(sum(4 * (-(-int(L) // P)) for L in seq[active]))
     meta_bytes = 8 * len(seq) + 4
-    append_bytes = int((b.slot_mapping >= 0).sum()) * (2 * per_tok + 8)
+    append_bytes = int((b.slot_mapping >= 0).sum()) * (new_tok + per_tok + 8)
     dec_seen = {}
     for r in np.nonzero(decode)[0]:
         L = int(seq[r])

@@ -163,3 +163,16 @@ def test_copy_blocks_validation():
     n0 = lib.pa_launch_count()
     assert lib.pa_copy_blocks(None, None, 0, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == b.PA_OK
     assert lib.pa_launch_count() == n0
+
+
+def test_q8_validation():
+    ws = FAKE
+    assert lib.pa_kv_append_q8(FAKE, FAKE, FAKE, -1, FAKE, FAKE, 64, 16, 8, 128, ws, 256, None) == \
+        b.PA_ERR_INVALID_ARG
+    assert lib.pa_kv_append_q8(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 64, 16, 8, 64, ws, 256, None) == \
+        b.PA_ERR_UNSUPPORTED
+    slh = (ctypes.c_int32 * 2)(40, 100)
+    qih = (ctypes.c_int32 * 3)(0, 1, 5)      # request 1 has 4 queries: not a decode row
+    assert lib.pa_attention_varlen_q8(FAKE, FAKE, FAKE, 64, FAKE, 40, FAKE, FAKE, slh, qih, 2, 5, 32, 8, 128, 16,
+                                      0.088, FAKE, None, FAKE, 1 << 30, None) == b.PA_ERR_UNSUPPORTED
+    assert "q8_0" in lib.pa_last_error_message().decode()
