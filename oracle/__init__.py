@@ -112,6 +112,8 @@ class Oracle:
                                                    P, P, P, i32, i32]
         lib.oracle_copy_blocks.restype = i64
         lib.oracle_copy_blocks.argtypes = [P, P, i64, i32, i32, i32, P, P, i64]
+        lib.oracle_decode_step_slots.restype = i32
+        lib.oracle_decode_step_slots.argtypes = [P, i32, P, i32, i32, i32, P]
         lib.oracle_merge_lse.restype = i32
         lib.oracle_merge_lse.argtypes = [P, P, P, P, P, P, i64, i32, i32]
         self.lib = lib
@@ -138,6 +140,39 @@ class Oracle:
         nb, _, P, _ = k_cache.shape
         _check(self.lib.oracle_kv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), N, _ptr(k_cache),
                                          _ptr(v_cache), nb, P, Hkv, D), "kv_append")
+
+    def decode_step_slots(self, block_tables, seq_lens, block_size, max_seq_len):
+        """Slot of each decode row's new token (position seq_len - 1), -1 for
+        padding and invalid rows.  Returns (slots int64 [R], invalid rows)."""
+        block_tables = _c(block_tables, np.int32)
+        seq_lens = _c(seq_lens, np.int32)
+        R = seq_lens.shape[0]
+        slots = np.full(R, -1, np.int64)
+        bad = self.lib.oracle_decode_step_slots(_ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), R,
+                                                block_size, max_seq_len, _ptr(slots))
+        return slots, int(bad)
+
+    def decode_step(self, q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, sm_scale, max_seq_len,
+                    n_threads=None):
+        """One decode step of a padded batch: row r's new token is appended
+        at position seq_lens[r] - 1 (slots from decode_step_slots; the
+        caches change in place), then every valid row attends over its
+        seq_len keys.  Padding and invalid rows get out = 0, lse = -inf.
+        Returns (out fp64 [R, Hq, D], lse fp64 [R, Hq], invalid rows)."""
+        q = _c(q, np.uint16)
+        R, Hq, D = q.shape
+        P = k_cache.shape[2]
+        slots, bad = self.decode_step_slots(block_tables, seq_lens, P, max_seq_len)
+        self.kv_append(k_new, v_new, slots, k_cache, v_cache)
+        out = np.zeros((R, Hq, D), np.float64)
+        lse = np.full((R, Hq), -np.inf, np.float64)
+        rows = np.flatnonzero(slots >= 0)
+        if len(rows):
+            o, l = self.attention_varlen(q[rows], k_cache, v_cache, _c(block_tables, np.int32)[rows],
+                                         _c(seq_lens, np.int32)[rows], np.arange(len(rows) + 1, dtype=np.int32),
+                                         sm_scale, n_threads=n_threads)
+            out[rows], lse[rows] = o, l
+        return out, lse, bad
 
     def copy_blocks(self, k_cache, v_cache, src, dst):
         """Copy whole blocks src[i] -> dst[i] (K and V, every kv head), in
@@ -297,6 +332,14 @@ def kv_append(*a, **kw):
 
 def copy_blocks(*a, **kw):
     return default().copy_blocks(*a, **kw)
+
+
+def decode_step_slots(*a, **kw):
+    return default().decode_step_slots(*a, **kw)
+
+
+def decode_step(*a, **kw):
+    return default().decode_step(*a, **kw)
 
 
 def q8_slab_bytes(page_tokens: int, head_dim: int) -> int:

@@ -181,6 +181,34 @@ static size_t kv_offset(int64_t block, int kvh, int off, int d, int Hkv, int p, 
 }
 
 /*
+ * Decode-step slots.  A decode row with L = seq_lens[r] keys after the step
+ * holds its new token at position L - 1, the last of its sequence; that
+ * position lives in logical block (L - 1) / p at offset (L - 1) % p, and the
+ * block table maps the logical block to its physical one (§8.3.1 and Fig.
+ * 8-10: tokens fill the table's blocks in order, a new block being taken
+ * when the last one is full).  Rows with L = 0 are padding (slot -1), and so
+ * are rows with L < 0, L > max_seq_len or more than max_blocks_per_req
+ * blocks, which are counted.  Returns the count of such invalid rows.
+ */
+int oracle_decode_step_slots(const int32_t* block_tables, int max_blocks_per_req, const int32_t* seq_lens,
+                             int num_reqs, int block_size, int max_seq_len, int64_t* slots) {
+  int bad = 0;
+  for (int r = 0; r < num_reqs; ++r) {
+    int64_t L = seq_lens[r];
+    slots[r] = -1;
+    if (L == 0) continue;
+    if (L < 0 || L > max_seq_len || (L + block_size - 1) / block_size > max_blocks_per_req) {
+      ++bad;
+      continue;
+    }
+    int64_t pos = L - 1;
+    int64_t block = block_tables[(size_t)r * (size_t)max_blocks_per_req + (size_t)(pos / block_size)];
+    slots[r] = block * block_size + pos % block_size;
+  }
+  return bad;
+}
+
+/*
  * KV append: for new token i with slot s = slot_mapping[i] >= 0, write
  * k_new[i, h, :] and v_new[i, h, :] into block s / p, offset s % p, for
  * every kv head h.  Negative slots are skipped.  A slot beyond the pool is

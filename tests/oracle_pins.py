@@ -427,6 +427,57 @@ def pin_copy_on_write(o):
     assert not np.array_equal(out[0], out[1])
 
 
+def pin_decode_step(o):
+    """A decode step ("Inference optimisation" §8.3.1 and Fig. 8-10) puts
+    each row's new token at the end of its sequence, position seq_len - 1,
+    in the block the table gives for it, and the row then attends over its
+    old keys followed by that token.  Checked against the cache bytes and a
+    dense softmax over [old keys gathered by numpy; the new token appended
+    by hand].  Padding rows (seq_len 0) write nothing and give out 0, lse
+    -inf; rows past max_seq_len are counted and treated as padding."""
+    rng = np.random.default_rng(23)
+    Hq, Hkv, P, D = 8, 2, 16, 32
+    nb = 24
+    lens = [1, 16, 17, 40, 0, 33]
+    k, v = _pool(nb, Hkv, P, D, rng)
+    tab = _tables(rng, nb, [max(L, 1) for L in lens], P)
+    R = len(lens)
+    q = workloads.normal_bf16(rng, (R, Hq, D))
+    kn = workloads.normal_bf16(rng, (R, Hkv, D))
+    vn = workloads.normal_bf16(rng, (R, Hkv, D))
+    k2, v2 = k.copy(), v.copy()
+    seq = np.array(lens, np.int32)
+    out, lse, bad = o.decode_step(q, kn, vn, k2, v2, tab, seq, 0.21, 64)
+    assert bad == 0
+    expect = set()
+    for r, L in enumerate(lens):
+        if L == 0:
+            continue
+        blk, off = int(tab[r, (L - 1) // P]), (L - 1) % P
+        for h in range(Hkv):
+            expect.add((blk, h, off))
+            assert np.array_equal(k2[blk, h, off], kn[r, h]) and np.array_equal(v2[blk, h, off], vn[r, h]), (r, h)
+    changed = set(tuple(x) for x in np.argwhere((k2 != k).any(axis=-1) | (v2 != v).any(axis=-1)).tolist())
+    assert changed == expect, (sorted(changed - expect), sorted(expect - changed))
+    G = Hq // Hkv
+    for r, L in enumerate(lens):
+        if L == 0:
+            assert np.all(out[r] == 0) and np.all(lse[r] == -np.inf)
+            continue
+        for h in range(Hq):
+            g = h // G
+            K = np.concatenate([f64(_gather(k, tab[r], g, L - 1, P)), f64(kn[r, g])[None]])
+            V = np.concatenate([f64(_gather(v, tab[r], g, L - 1, P)), f64(vn[r, g])[None]])
+            S = 0.21 * (K @ f64(q[r, h]))
+            assert np.allclose(out[r, h], special.softmax(S) @ V, rtol=1e-12, atol=1e-12), (r, h)
+            assert abs(lse[r, h] - special.logsumexp(S)) <= 1e-12, (r, h)
+    # a row longer than the call's bound is counted and left as padding
+    k3, v3 = k.copy(), v.copy()
+    out3, lse3, bad3 = o.decode_step(q, kn, vn, k3, v3, tab, seq, 0.21, 39)
+    assert bad3 == 1 and np.all(out3[3] == 0) and np.all(lse3[3] == -np.inf)
+    assert not np.array_equal(out3[5], np.zeros_like(out3[5]))
+
+
 def pin_f16_conversion(o):
     """The oracle's binary32 -> binary16 rounding (used for the q8_0 scales)
     agrees with numpy's IEEE conversion on random values across the range
@@ -572,7 +623,7 @@ ALL_PINS = [pin_page_arithmetic, pin_round_bf16, pin_single_key, pin_one_hot_sco
             pin_uniform_scores, pin_gqa_grouping, pin_scipy_dense, pin_page_permutation,
             pin_shared_equals_duplicated, pin_chunked_equals_oneshot, pin_merge_identity, pin_append_then_read,
             pin_copy_on_write, pin_f16_conversion, pin_q8_layout_arithmetic, pin_q8_quantization, pin_q8_attention,
-            pin_brute_force, pin_sampled_matches_full]
+            pin_brute_force, pin_sampled_matches_full, pin_decode_step]
 
 
 def run_all(o) -> list:

@@ -43,6 +43,11 @@ MUTANTS = {
     "q8_code_trunc": ("float t = rintf((float)bf16_to_double(x[i]) / d16);",
                       "float t = truncf((float)bf16_to_double(x[i]) / d16);"),
     "q8_scale_index": ("2 * ((size_t)off * (D / 32) + d / 32)", "2 * ((size_t)off * (D / 32) + d / 64)"),
+    "step_slot_next": ("int64_t pos = L - 1;", "int64_t pos = L;"),
+    "step_slot_offset": ("slots[r] = block * block_size + pos % block_size;",
+                         "slots[r] = block * block_size + pos / block_size;"),
+    "step_padding_written": ("    if (L == 0) continue;\n    if (L < 0 ||", "    if (L < 0 ||"),
+    "step_bound_ignored": ("if (L < 0 || L > max_seq_len ||", "if (L < 0 ||"),
     "f16_round_trunc": ("r = ldexp(rint(ldexp(m, 11)), e - 11);", "r = ldexp(trunc(ldexp(m, 11)), e - 11);"),
 }
 
