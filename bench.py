@@ -287,7 +287,10 @@ def run_sweep(args):
         for batch in [int(x) for x in args.batches.split(",")]:
             spec = W.sweep_point(batch, context)
             b, pools = device_batch(spec, dev, layers)
-            ppages = 0 if args.no_cascade else spec["shared_prefix_tokens"] // 16
+            # the decode step has no shared-prefix pass: points whose rows share
+            # a prefix keep the cascade call
+            use_step = args.api == "step" and (args.no_cascade or spec["shared_prefix_tokens"] == 0)
+            ppages = 0 if (args.no_cascade or use_step) else spec["shared_prefix_tokens"] // 16
             sb = W.step_bytes(b, ppages)
 
             def bf(a):
@@ -301,8 +304,15 @@ def run_sweep(args):
             ws = B.new_workspace(B.pa_shared_prefix_workspace_size(b.num_reqs, b.total_q, 32, 128,
                                                                    int(b.seq_lens.max()), ppages), dev)
             ws_app = B.new_workspace(B.PA_ERROR_WORD_BYTES, dev)
+            if use_step:
+                ws = B.new_workspace(B.pa_decode_step_workspace_size(batch, 32, 128, context), dev)
 
             def step():
+                if use_step:
+                    for kc, vc in pools:
+                        B.pa_decode_step(q, k_new, v_new, kc, vc, tables, seq, b.sm_scale, context, out=out,
+                                         workspace=ws)
+                    return
                 for kc, vc in pools:
                     B.pa_kv_append(k_new, v_new, slots, kc, vc, workspace=ws_app)
                     attention(B, ppages, q, kc, vc, tables, seq, ind, b.sm_scale, b.seq_lens, b.qo_indptr, out, ws)
@@ -336,10 +346,12 @@ def run_sweep(args):
                     "frac_of_measured_hbm": round(sb["unique"] / (per_layer * 1e-3) / 1e9 / peak, 4),
                     "tokens_per_layer_step_per_s": round(batch / (per_layer * 1e-3), 1),
                     "bytes_per_layer": sb["unique"], "pool_blocks": spec["num_blocks"],
-                    "attention_call": call_name(ppages),
+                    "attention_call": ("pa_decode_step (append + attention in one launch, max_seq_len %d)" % context
+                                       if use_step else call_name(ppages)),
                     "l2": "not flushed (36 layers x distinct pools stream %.1f GB per step)" %
                           (sb["unique"] * layers / 1e9),
-                    "graph": "36 x (kv_append + attention) in one CUDA graph"}
+                    "graph": ("36 x pa_decode_step" if use_step else "36 x (kv_append + attention)")
+                    + " in one CUDA graph"}
             print(json.dumps(line), flush=True)
             del pools, graph
             torch.cuda.empty_cache()
@@ -364,6 +376,9 @@ def main():
     ap.add_argument("--batches", default="1,8,32,64,128", help="sweep decode batch sizes")
     ap.add_argument("--kv", choices=["bf16", "q8"], default="bf16",
                     help="KV page format: bf16, or q8_0 (decode workloads only)")
+    ap.add_argument("--api", choices=["varlen", "step"], default="varlen",
+                    help="varlen: pa_kv_append + the attention call; step: pa_decode_step (append and attention in "
+                         "one self-planned launch; decode-only bf16 batches)")
     ap.add_argument("--no-cascade", action="store_true",
                     help="run shared-prefix batches through pa_attention_varlen instead of the shared-prefix call")
     args = ap.parse_args()
@@ -393,7 +408,10 @@ def main():
     q8 = args.kv == "q8"
     if q8 and np.any(np.diff(batch.qo_indptr) > 1):
         raise SystemExit("--kv q8 serves decode rows only; this workload has rows with qo_len > 1")
-    ppages = 0 if (args.no_cascade or q8) else batch.meta["shared_prefix_tokens"] // 16
+    use_step = args.api == "step"
+    if use_step and (q8 or np.any(np.diff(batch.qo_indptr) != 1)):
+        raise SystemExit("--api step serves bf16 batches of decode rows only")
+    ppages = 0 if (args.no_cascade or q8 or use_step) else batch.meta["shared_prefix_tokens"] // 16
     sb = W.step_bytes(batch, ppages, kv=args.kv)
 
     def bf(a):
@@ -406,6 +424,8 @@ def main():
         "seq_lens": torch.from_numpy(batch.seq_lens).pin_memory(),
         "qo_indptr": torch.from_numpy(batch.qo_indptr).pin_memory(),
     }
+    if use_step:  # the step plans on the device: no slot_mapping, no qo_indptr
+        del host["slot_mapping"], host["qo_indptr"]
     d = {k: v.to(dev) for k, v in host.items()}
     if q8:
         # q8_0 pools: every cached token quantized into its slot once, on the GPU
@@ -425,18 +445,26 @@ def main():
     out = torch.empty_like(d["q"])
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     R, total_q = batch.num_reqs, batch.total_q
-    ws = B.new_workspace(B.pa_shared_prefix_workspace_size(R, total_q, 32, 128, int(batch.seq_lens.max()), ppages),
-                         dev)
+    max_len = int(batch.seq_lens.max())
+    if use_step:
+        ws = B.new_workspace(B.pa_decode_step_workspace_size(R, 32, 128, max_len), dev)
+    else:
+        ws = B.new_workspace(B.pa_shared_prefix_workspace_size(R, total_q, 32, 128, max_len, ppages), dev)
     ws_app = B.new_workspace(B.PA_ERROR_WORD_BYTES, dev)
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush_l2():
         torch.sum(flush, dim=0, out=flush_sink)
-    seq_h, ind_h = host["seq_lens"], host["qo_indptr"]
+    seq_h = host["seq_lens"]
+    ind_h = host.get("qo_indptr")
     stream = torch.cuda.current_stream()
 
     def step(src):
+        if use_step:
+            B.pa_decode_step(src["q"], src["k_new"], src["v_new"], k_cache, v_cache, src["block_tables"],
+                             src["seq_lens"], batch.sm_scale, max_len, out=out, workspace=ws)
+            return
         if q8:
             B.pa_kv_append_q8(src["k_new"], src["v_new"], src["slot_mapping"], k_cache, v_cache, workspace=ws_app)
             B.pa_attention_varlen_q8(src["q"], k_cache, v_cache, src["block_tables"], src["seq_lens"],
@@ -533,11 +561,13 @@ def main():
     # roofline of the kernel with the largest share of the step: the decode
     # kernel (HBM-bound), or the tensor-core tile kernel of rows with
     # qo_len > 1, bound by HBM or by the tensor pipe by its arithmetic intensity
-    dom = max(("decode", "prefill"), key=lambda k_: kernel_share.get(k_, 0.0))
+    dom = max(("decode", "prefill", "decode_step"), key=lambda k_: kernel_share.get(k_, 0.0))
     dom_ms_list = [ms for k_, ms in trace if k_ == dom]
     dom_ms = sum(dom_ms_list) / len(dom_ms_list) if dom_ms_list else None
     if dom == "decode":
         bound, dom_bytes, dom_flops = "hbm", sb["decode_kernel"], None
+    elif dom == "decode_step":
+        bound, dom_bytes, dom_flops = "hbm", sb["step_kernel"], None
     else:
         dom_bytes, dom_flops = sb["prefill_kernel"], sb["prefill_flops"]
         bound = "tensor" if dom_flops / max(dom_bytes, 1) > tflops_peak * 1e12 / (peak * 1e9) else "hbm"
@@ -562,7 +592,8 @@ def main():
         "config": {"workload": WORKLOADS[args.workload], "parallelism": f"replicas x{world}",
                    "kv_format": "q8_0 (34 of 64 bytes per 32 values)" if q8 else "bf16",
                    "l2": "flushed between timed steps (256 MiB read outside the events)",
-                   "attention_call": call_name(ppages),
+                   "attention_call": ("pa_decode_step (append + attention in one launch)" if use_step
+                                      else call_name(ppages)),
                    "bytes_per_step": sb["unique"], "logical_bytes_per_step": sb["logical"],
                    "query_tokens_per_step": sb["query_tokens"]},
         "tokens_per_layer_step_per_s": round(sb["query_tokens"] * world / (t_step * 1e-3), 1),

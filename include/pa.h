@@ -223,6 +223,77 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
                               void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * Decode step for CUDA graphs ("Inference optimisation", AI-infra book ch. 8,
+ * §8.2.4: graphs captured in advance for a few row counts, inputs padded up
+ * to the next captured size; "Continuous batching architecture", section
+ * "CUDA graphs": one recorded launch sequence replayed for batches whose
+ * padded shape matches, which removes the per-step CPU launch work).
+ *
+ * pa_decode_step -- the KV append and the attention of a decode-only batch
+ * in one kernel launch whose launch shape depends only on the scalars
+ * (num_reqs, num_kv_heads, max_seq_len), and which reads no array on the
+ * host.  A launch captured in a CUDA graph is therefore valid for every
+ * batch within those scalars: between replays the caller rewrites q, k_new,
+ * v_new, block_tables and seq_lens in place.
+ *   Row r (0 <= r < num_reqs) is one decode request with L = seq_lens[r]
+ *   keys after this step (L >= 1), its new token at position L - 1 and
+ *   query q[r].  The call writes k_new[r, h, :] / v_new[r, h, :] into
+ *   k_cache / v_cache at the slot of position L - 1 (block
+ *   block_tables[r, (L-1) / 16], offset (L-1) % 16; no slot_mapping is
+ *   taken) and computes, for every q head, the attention of
+ *   pa_attention_varlen with qo_len = 1 over the L keys, the new token
+ *   included (out bf16, lse natural log).
+ *   Rows with L = 0 are padding: nothing is written to the cache, their out
+ *   rows are zero and lse is -inf.  Padding a batch to a captured size
+ *   means L = 0 for the extra rows (KV lengths need no padding: the kernel
+ *   reads the exact lengths).
+ *   A row with L < 0, L > max_seq_len or more than max_blocks_per_req pages
+ *   is treated as padding and recorded as PA_ERR_DEVICE_INDEX; a block id
+ *   outside the pool is masked and recorded as in pa_attention_varlen.
+ *   Requirement (copy-on-write, §8.3.2): the block receiving a row's new
+ *   token is read by no other row of the call.  The appending CTA uses the
+ *   new K/V directly, so the result equals pa_kv_append followed by
+ *   pa_attention_varlen whenever that holds.
+ * q              [num_reqs, num_q_heads, head_dim] bf16, 16-byte aligned.
+ * k_new, v_new   [num_reqs, num_kv_heads, head_dim] bf16, 16-byte aligned.
+ * k_cache, v_cache  HND bf16 pools, modified in place (the new tokens).
+ * block_tables   [num_reqs, max_blocks_per_req] int32, device.
+ * seq_lens       [num_reqs] int32, device only.
+ * num_reqs       rows of the padded batch, 0 .. 1024 (see pa_decode_step_bucket).
+ * max_seq_len    largest L any replay will use, 1 .. PA_MAX_SEQ_LEN.
+ * out, lse       as pa_attention_varlen with total_q = num_reqs.
+ * workspace      device, >= pa_decode_step_workspace_size(num_reqs,
+ *                num_q_heads, head_dim, max_seq_len) bytes, 256-byte aligned,
+ *                zero-filled before first use, left reusable by every call.
+ *                Calls sharing a workspace must not run concurrently.
+ * Errors: PA_ERR_INVALID_ARG (null or misaligned pointers, max_seq_len
+ *   outside its range), PA_ERR_UNSUPPORTED (shape, num_reqs > 1024, or
+ *   num_reqs x max_seq_len too large for one launch),
+ *   PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_CUDA.  num_reqs = 0 launches nothing.
+ */
+pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_req,
+                         const int32_t* seq_lens, int32_t num_reqs, int32_t max_seq_len, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size, float sm_scale, void* out,
+                         float* lse, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode_step_workspace_size -- bytes of workspace pa_decode_step needs
+ * for these scalars; 0 when no launch exists for them (num_reqs outside
+ * 0 .. 1024, max_seq_len outside 1 .. PA_MAX_SEQ_LEN, num_q_heads < 4, or
+ * num_reqs x max_seq_len too large).
+ */
+size_t pa_decode_step_workspace_size(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim, int32_t max_seq_len);
+
+/*
+ * pa_decode_step_bucket -- the padded row count for a batch of num_reqs
+ * decode rows: the smallest power of two >= num_reqs (1 for 0), so that a
+ * handful of captured graphs cover 1 .. 1024 rows with less than 2x rows of
+ * padding (padding rows cost no key reads).  -1 outside 0 .. 1024.
+ */
+int32_t pa_decode_step_bucket(int32_t num_reqs);
+
+/*
  * pa_shared_prefix_workspace_size -- bytes of device workspace that
  * pa_attention_varlen_shared_prefix needs for a batch with at most these
  * sizes: the pa_attention_workspace_size() layout followed by the prefix
@@ -333,7 +404,9 @@ pa_status pa_clear_device_error(void* workspace, pa_stream_t stream);
  * Tuning and diagnostics.
  *   pa_set_decode_ctas(n): n > 0 asks for a persistent decode grid of n CTAs
  *     (capped by the plan limits and the workspace bound), 0 restores the
- *     automatic plan (3 CTAs per SM).  Process-wide.
+ *     automatic plan (3 CTAs per SM).  Process-wide.  pa_decode_step and
+ *     pa_decode_step_workspace_size use it too (rounded up to whole kv
+ *     heads, and raised where a segment would exceed 1024 pages).
  *   pa_launch_count(): kernels this library has launched in this process.
  *   pa_trace_enable(1): from now on every launch records a CUDA event before
  *     and after itself on its stream (at most 16384 launches are kept; the
@@ -350,7 +423,8 @@ typedef enum {
   PA_KERNEL_MERGE = 5,
   PA_KERNEL_PREFIX = 6,      /* shared-prefix pass of pa_attention_varlen_shared_prefix */
   PA_KERNEL_PREFIX_MERGE = 7, /* merge of that pass's key-chunk partials */
-  PA_KERNEL_COPY_BLOCKS = 8   /* pa_copy_blocks */
+  PA_KERNEL_COPY_BLOCKS = 8,  /* pa_copy_blocks */
+  PA_KERNEL_DECODE_STEP = 9   /* pa_decode_step */
 } pa_kernel_kind;
 
 pa_status pa_set_decode_ctas(int32_t n);

@@ -27,7 +27,8 @@ PA_ERR_CUDA = 4
 PA_ERR_DEVICE_INDEX = 5
 PA_ERR_DEVICE_TIMEOUT = 6
 PA_ERROR_WORD_BYTES = 256
-KERNEL_KINDS = {1: "kv_append", 2: "decode", 3: "combine", 4: "prefill", 5: "merge", 6: "prefix", 7: "prefix_merge", 8: "copy_blocks"}
+KERNEL_KINDS = {1: "kv_append", 2: "decode", 3: "combine", 4: "prefill", 5: "merge", 6: "prefix", 7: "prefix_merge", 8: "copy_blocks",
+                9: "decode_step"}
 
 
 class PAError(RuntimeError):
@@ -55,6 +56,10 @@ _SIGS = {
     "pa_attention_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pa_attention_varlen": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _f32, _P, _P, _P, _sz, _P]),
+    "pa_decode_step": (_i32, [_P, _P, _P, _P, _P, _i64, _P, _i32, _P, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _P,
+                              _P, _P, _sz, _P]),
+    "pa_decode_step_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
+    "pa_decode_step_bucket": (_i32, [_i32]),
     "pa_shared_prefix_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_attention_varlen_shared_prefix": (_i32, [_P, _P, _P, _i64, _P, _i32, _P, _P, _P, _P, _i32, _i32, _i32, _i32,
                                                  _i32, _i32, _i32, _f32, _P, _P, _P, _sz, _P]),
@@ -267,6 +272,53 @@ def pa_attention_varlen(q, k_cache, v_cache, block_tables, seq_lens, qo_indptr, 
                                     ctypes.c_void_p(slh.data_ptr()), ctypes.c_void_p(qih.data_ptr()), R, total_q, Hq,
                                     Hkv, D, P, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                     workspace.numel(), _stream(stream)))
+    return (out, lse) if (return_lse or lse is not None) else out
+
+
+def pa_decode_step_workspace_size(num_reqs, num_q_heads, head_dim, max_seq_len) -> int:
+    return int(_lib.pa_decode_step_workspace_size(num_reqs, num_q_heads, head_dim, max_seq_len))
+
+
+def pa_decode_step_bucket(num_reqs) -> int:
+    return int(_lib.pa_decode_step_bucket(num_reqs))
+
+
+def pa_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, sm_scale, max_seq_len, *, out=None,
+                   lse=None, workspace=None, stream=None, return_lse=False):
+    """KV append + attention of a padded decode-only batch in one launch (see
+    include/pa.h).  q [R, Hq, D] bf16; k_new / v_new [R, Hkv, D] bf16; caches
+    [num_blocks, Hkv, 16, D] bf16 (the new tokens are written into them);
+    block_tables int32 [R, max_blocks]; seq_lens int32 [R] on the device (0 =
+    padding row).  Nothing is read back to the host, so the call can be
+    captured in a CUDA graph and replayed with new contents of the same
+    tensors.  Returns out (and lse when return_lse or lse is given)."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(seq_lens, torch.int32, "seq_lens")
+    R, Hq, D = q.shape
+    nb, Hkv, P, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or k_new.shape != (R, Hkv, D) or v_new.shape != (R, Hkv, D) \
+            or seq_lens.shape != (R,) or block_tables.dim() != 2 or block_tables.shape[0] != R:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if lse is None and return_lse:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+    if workspace is None:
+        workspace = new_workspace(pa_decode_step_workspace_size(R, Hq, D, max_seq_len), q.device)
+    _check(_lib.pa_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), nb,
+                               _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), R, int(max_seq_len), Hq,
+                               Hkv, D, P, float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                               _stream(stream)))
     return (out, lse) if (return_lse or lse is not None) else out
 
 

@@ -42,6 +42,7 @@
 //     workspace, and the last of those CTAs to finish (a counter it resets)
 //     merges them into out / lse.
 #include <math.h>
+#include <stddef.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -63,6 +64,7 @@ struct Item {        // one request's pages within this CTA's segment
   int32_t r;        // request
   int32_t L;        // seq_len of the request
   int32_t tok;      // its query token
+  int32_t A;        // stream position of the row's start (its cost units, then its pages)
 };
 
 // Bytes of one (page, kv head) slab: bf16 pages, or q8_0 pages (16 x 128
@@ -78,12 +80,24 @@ struct __align__(128) DecodeSmem {
   int readers[kStages];     // warps done reading the stage's current page
   int32_t ids[kDecodeMaxPagesPerCta];
   Item items[kDecodeMaxItemsPerCta];
-  int n_items;
-  int n_cov;                 // pages covered by the items (exactly these are issued)
+  int n_cov;                 // end of the pages the current window's items cover
+  int seg_pages;             // pages of the segment (self-planned)
+  int n_items;               // items of the current window
+  int n_items_all;           // items of the segment
+  int seg_cost;              // segment length in stream units (self-planned)
+  int scan[kThreads / 32];   // per-warp totals of the planning scans
+  alignas(16) uint8_t knew[kHeadDim * 2];  // decode step: the appended token's K row (16-byte accesses)
+  alignas(16) uint8_t vnew[kHeadDim * 2];  // and V row
   int stage_page[kStages];   // last page issued into each stage (-1: none)
   int abort_flag;
   int is_last;
 };
+
+static_assert(offsetof(DecodeSmem<kSlabBytes>, knew) % 16 == 0 && offsetof(DecodeSmem<kSlabBytes>, vnew) % 16 == 0,
+              "the appended rows are read and written with 16-byte accesses");
+static_assert(offsetof(DecodeSmem<kSlabBytes>, k) % 128 == 0 && offsetof(DecodeSmem<kSlabBytes>, v) % 128 == 0 &&
+                  offsetof(DecodeSmem<kQ8SlabBytes>, v) % 16 == 0,
+              "bulk copies land on 16-byte boundaries");
 
 // 8 packed bf16 pairs (two 16-byte loads) -> 8 float2
 __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float2* f) {
@@ -249,9 +263,139 @@ __device__ __forceinline__ float fold_prefix(const DecodeParams& p, float4& o, f
   return M + log2f(wsum);
 }
 
-template <bool kQ8>
+// Decode step: each CTA plans its own segment from the device seq_lens.
+// Row r of the padded batch costs pages_r + kStepItemCost units (0 for a
+// padding row: seq_len 0, or a length outside the call's bounds), the rows'
+// costs are laid end to end and cut into n_eff equal segments of C units;
+// a row's pages sit after its fixed cost, and segment s holds the pages
+// whose units fall in [s C, (s + 1) C).  The fixed cost stands for the item-
+// end merge work, so segments with many short rows hold fewer pages.  Fills
+// the items win0 .. win0 + kDecodeMaxItemsPerCta - 1 of this CTA's segment
+// (all threads call it; it ends with a barrier).  Also writes the outputs of
+// padding rows (zero, lse -inf) and records rows outside the bounds.
+template <class Smem>
+__device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& sm, int kvh, int sidx, int nseg_grid,
+                            int win0) {
+  constexpr int kRows = kPlanMaxRows / kThreads;  // rows per thread, consecutive
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hkv = p.num_kv_heads;
+  int pg[kRows], len[kRows];
+  int tsum = 0;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int r = tid * kRows + i;
+    const int L = r < plan.n_rows ? __ldg(p.seq_lens + r) : 0;
+    const int pages = (L + kPage - 1) / kPage;
+    const bool bad = r < plan.n_rows && (L < 0 || L > plan.max_seq_len || pages > p.max_blocks_per_req);
+    len[i] = L;
+    pg[i] = (bad || L <= 0) ? 0 : pages;
+    tsum += pg[i] > 0 ? pg[i] + kStepItemCost : 0;
+    if (win0 == 0 && r < plan.n_rows && pg[i] == 0 && sidx == r % nseg_grid) {
+      // padding (or invalid) row: defined outputs for this kv head's 4 q heads
+      if (bad) record_error(p.err, PA_ERR_DEVICE_INDEX);
+      uint4* o = reinterpret_cast<uint4*>(p.out + ((size_t)r * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim);
+      for (int j = 0; j < kGroup * kHeadDim * 2 / 16; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (p.lse)
+        for (int g = 0; g < kGroup; ++g) p.lse[(size_t)r * p.num_q_heads + kvh * kGroup + g] = -INFINITY;
+    }
+  }
+  // exclusive scan of the row costs (thread-local, then across the block)
+  int incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.scan[warp] = incl;
+  __syncthreads();
+  int total = 0, woff = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int v = sm.scan[w];
+    woff += (w < warp) ? v : 0;
+    total += v;
+  }
+  int A = woff + incl - tsum;  // cost position of this thread's first row
+  const int n_eff = max(1, min(nseg_grid, (total + kStepMinSegCost - 1) / kStepMinSegCost));
+  const int C = max(1, (total + n_eff - 1) / n_eff);
+  const int S = sidx * C, E = min(S + C, total);
+  // this segment's part of each row: (first page p0, pages nn), packed with
+  // an item count for the second scan: (pages << 16) | 1
+  int p0v[kRows], nnv[kRows], Av[kRows];
+  int t2 = 0;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int u0 = A + kStepItemCost, u1 = u0 + pg[i];
+    const bool in = pg[i] > 0 && u1 > S && u0 < E;
+    p0v[i] = in ? max(0, S - u0) : 0;
+    nnv[i] = in ? min(u1, E) - u0 - p0v[i] : 0;
+    Av[i] = A;
+    t2 += in ? ((nnv[i] << 16) | 1) : 0;
+    A += pg[i] > 0 ? pg[i] + kStepItemCost : 0;
+  }
+  __syncthreads();  // sm.scan is reused
+  int incl2 = t2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl2, o);
+    if (lane >= o) incl2 += y;
+  }
+  if (lane == 31) sm.scan[warp] = incl2;
+  __syncthreads();
+  int tot2 = 0, woff2 = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int v = sm.scan[w];
+    woff2 += (w < warp) ? v : 0;
+    tot2 += v;
+  }
+  int e2 = woff2 + incl2 - t2;
+  const int n_all = tot2 & 0xffff;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    if (nnv[i] > 0) {
+      const int idx = (e2 & 0xffff) - win0;
+      if (idx >= 0 && idx < kDecodeMaxItemsPerCta) {
+        const int r = tid * kRows + i;
+        Item& it = sm.items[idx];
+        it.q_start = e2 >> 16;
+        it.n = nnv[i];
+        it.p0 = p0v[i];
+        it.r = r;
+        it.L = len[i];
+        it.tok = r;
+        it.A = Av[i];
+        const size_t qoff = ((size_t)r * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
+        bulk_prefetch_l2(p.q + qoff, kGroup * kHeadDim * 2);
+        if (p0v[i] + nnv[i] == pg[i]) {  // this CTA appends the row's new token
+          const size_t noff = ((size_t)r * Hkv + kvh) * kHeadDim;
+          bulk_prefetch_l2(p.k_new + noff, kHeadDim * 2);
+          bulk_prefetch_l2(p.v_new + noff, kHeadDim * 2);
+        }
+      }
+      e2 += (nnv[i] << 16) | 1;
+    }
+  }
+  if (tid == 0) {
+    sm.n_items = max(0, min(n_all - win0, kDecodeMaxItemsPerCta));
+    sm.n_items_all = n_all;
+    sm.seg_cost = C;
+    sm.seg_pages = tot2 >> 16;
+    if (tot2 >> 16 > kDecodeMaxPagesPerCta) {  // bounded by the host's grid choice
+      record_error(p.err, PA_ERR_DEVICE_INDEX);
+      sm.n_items = 0;
+    }
+  }
+  __syncthreads();
+}
+
+template <bool kQ8, bool kStep>
 __global__ void __launch_bounds__(kThreads, 3)
-    decode_kernel(const DecodeParams p, const __grid_constant__ DecodePlan plan) {
+    decode_kernel(const DecodeParams p, const __grid_constant__ typename PlanOf<kStep>::type plan) {
+  static_assert(!(kQ8 && kStep), "the decode step serves bf16 pages");
+  // the fixed cost of a row in the stream's units (the host plan cuts in
+  // pages, with no fixed cost)
+  constexpr int kAlpha = kStep ? kStepItemCost : 0;
   constexpr int kSlab = kQ8 ? kQ8SlabBytes : kSlabBytes;
   using Smem = DecodeSmem<kSlab>;
   // No early launch of the next kernel: this grid is one wave sized to fill
@@ -264,101 +408,86 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.num_kv_heads;
   const int kvh = b % Hkv, sidx = b / Hkv;
-  const int S0 = sidx * plan.seg;
-  const int npg = min(plan.total, S0 + plan.seg) - S0;
-  if (npg <= 0) return;
-  const int n_items_all = plan.n_rows;
-
-  // ---- item table of this segment (warp 0), 32 items per round
-  if (warp == 0) {
-    int base_q = 0, n_it = 0;
-    for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
-      const int item = plan.first_row[sidx] + k0 + lane;
-      const bool exists = item < n_items_all;
-      int r = 0, L = 0, size = 0, tok = 0;
-      const int p0 = (k0 + lane == 0) ? plan.first_page[sidx] : 0;
-      if (exists) {
-        // the plan's copies of seq_lens[r] and qo_indptr[r] (no device read)
-        r = plan.rows[item];
-        L = plan.seq[item];
-        tok = plan.tok[item];
-        size = max((L + kPage - 1) / kPage - p.page_offset - p0, 0);
+  int npg;  // pages of this CTA's segment
+  if constexpr (kStep) {
+    if (tid == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&sm.full[s], 1);
+        sm.readers[s] = 0;
+        sm.stage_page[s] = -1;
       }
-      int incl = size;
+      sm.abort_flag = 0;
+      fence_mbar_init();
+    }
+    step_window(p, plan, sm, kvh, sidx, (int)gridDim.x / Hkv, 0);
+    npg = sm.seg_pages;
+  } else {
+    const int S0 = sidx * plan.seg;
+    npg = min(plan.total, S0 + plan.seg) - S0;
+    if (npg <= 0) return;
+    if (tid == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&sm.full[s], 1);
+        sm.readers[s] = 0;
+        sm.stage_page[s] = -1;
+      }
+      sm.abort_flag = 0;
+      fence_mbar_init();
+    }
+    const int n_items_all = plan.n_rows;
+
+    // ---- item table of this segment (warp 0), 32 items per round
+    if (warp == 0) {
+      int base_q = 0, n_it = 0;
+      for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
+        const int item = plan.first_row[sidx] + k0 + lane;
+        const bool exists = item < n_items_all;
+        int r = 0, L = 0, size = 0, tok = 0;
+        const int p0 = (k0 + lane == 0) ? plan.first_page[sidx] : 0;
+        if (exists) {
+          // the plan's copies of seq_lens[r] and qo_indptr[r] (no device read)
+          r = plan.rows[item];
+          L = plan.seq[item];
+          tok = plan.tok[item];
+          size = max((L + kPage - 1) / kPage - p.page_offset - p0, 0);
+        }
+        int incl = size;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int start = base_q + incl - size;
+        const bool in_seg = size > 0 && start < npg;
+        if (in_seg && k0 + lane < kDecodeMaxItemsPerCta) {
+          Item& it = sm.items[k0 + lane];
+          it.q_start = start;
+          it.n = min(size, npg - start);
+          it.p0 = p0;
+          it.r = r;
+          it.L = L;
+          it.tok = tok;
+          it.A = S0 + start - p0;  // stream position of the row's page 0
+          // the item's q (4 heads x 256 B) into L2 now; it is read at the item's start
+          bulk_prefetch_l2(p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim,
+                           kGroup * kHeadDim * 2);
+        }
+        // the table is the leading run of covered items (a gap can only come
+        // from metadata that differ from the plan)
+        const unsigned covered = __ballot_sync(0xffffffffu, in_seg);
+        const int prefix = (~covered == 0u) ? 32 : (__ffs((int)~covered) - 1);
+        n_it = k0 + prefix;
+        base_q += __shfl_sync(0xffffffffu, incl, 31);
+        if (prefix < 32 || base_q >= npg) break;
       }
-      const int start = base_q + incl - size;
-      const bool in_seg = size > 0 && start < npg;
-      if (in_seg && k0 + lane < kDecodeMaxItemsPerCta) {
-        Item& it = sm.items[k0 + lane];
-        it.q_start = start;
-        it.n = min(size, npg - start);
-        it.p0 = p0;
-        it.r = r;
-        it.L = L;
-        it.tok = tok;
-        // the item's q (4 heads x 256 B) into L2 now; it is read at the item's start
-        bulk_prefetch_l2(p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim,
-                         kGroup * kHeadDim * 2);
+      if (lane == 0) {
+        if (base_q < npg) record_error(p.err, PA_ERR_DEVICE_INDEX);  // metadata differ from the plan
+        sm.n_items = min(n_it, kDecodeMaxItemsPerCta);
       }
-      // the table is the leading run of covered items (a gap can only come
-      // from metadata that differ from the plan)
-      const unsigned covered = __ballot_sync(0xffffffffu, in_seg);
-      const int prefix = (~covered == 0u) ? 32 : (__ffs((int)~covered) - 1);
-      n_it = k0 + prefix;
-      base_q += __shfl_sync(0xffffffffu, incl, 31);
-      if (prefix < 32 || base_q >= npg) break;
     }
-    if (lane == 0) {
-      if (base_q < npg) record_error(p.err, PA_ERR_DEVICE_INDEX);  // metadata differ from the plan
-      sm.n_items = min(n_it, kDecodeMaxItemsPerCta);
-    }
+    __syncthreads();
   }
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      sm.readers[s] = 0;
-      sm.stage_page[s] = -1;
-    }
-    sm.abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const int n_items = sm.n_items;
-  if (n_items == 0) return;  // nothing covered (recorded above); no copy was issued
-
-  // ---- block ids of the segment's pages; an id outside the pool (or a page
-  // past the table) is recorded and masked, and fetched from block 0
-  int ok = 1;
-  for (int q = tid; q < npg; q += kThreads) {
-    int lo = 0, hi = n_items - 1;
-    while (lo < hi) {  // last item with q_start <= q
-      const int mid = (lo + hi + 1) >> 1;
-      if (sm.items[mid].q_start <= q) lo = mid; else hi = mid - 1;
-    }
-    int32_t blk = -1;
-    const Item& it = sm.items[lo];
-    const int page = p.page_offset + it.p0 + (q - it.q_start);
-    if (q < it.q_start + it.n && page < p.max_blocks_per_req)
-      blk = p.block_tables[(size_t)it.r * p.max_blocks_per_req + page];
-    if (blk < 0 || blk >= p.num_blocks) {
-      record_error(p.err, PA_ERR_DEVICE_INDEX);
-      blk = -1;
-      ok = 0;
-    }
-    sm.ids[q] = blk;
-  }
-  if (tid == 0) {
-    // pages the items cover: exactly these are issued, and every one of
-    // them is consumed, so no copy is in flight when the CTA exits
-    sm.n_cov = sm.items[n_items - 1].q_start + sm.items[n_items - 1].n;
-  }
-  const bool ids_ok = __syncthreads_and(ok) != 0;
-  const int n_cov = sm.n_cov;
-
+  int n_cov = 0;
   const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_cache);
   const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v_cache);
   // segment page i -> stage i % kStages (K and V slabs of kv head kvh)
@@ -370,10 +499,6 @@ __global__ void __launch_bounds__(kThreads, 3)
     bulk_g2s(sm.v[s], vbase + off, kSlab, &sm.full[s]);
     sm.stage_page[s] = i;  // one issuer per stage at a time
   };
-  if (tid == 0) {
-    const int n0 = min(n_cov, kStages);
-    for (int i = 0; i < n0; ++i) issue(i);
-  }
   // a warp is done with page i: the last of the 4 warps refills its stage
   // with page i + kStages
   auto release = [&](int i) {
@@ -393,8 +518,56 @@ __global__ void __launch_bounds__(kThreads, 3)
   // iteration and head hd = 2 bit2(c) + bit1(c).
   const int slot_base = lane & ~7;
   bool aborted = false;
-  int qg = 0;  // segment page counter at the current item's start
+  int qg = 0;    // segment page counter at the current item's start
+  int win0 = 0;  // the window's first item within the segment
 
+  // Windows of up to kDecodeMaxItemsPerCta items: one for the host plan;
+  // the self-planned step walks a segment with more items in several.  The
+  // host path keeps the shape of the single-window loop (its register
+  // allocation, and so its speed, is sensitive to the code around the page
+  // loop).
+  for (;;) {
+  const int n_items = sm.n_items;
+  if (n_items == 0) break;  // nothing covered (recorded above); no copy was issued
+
+  // ---- block ids of the window's pages; an id outside the pool (or a page
+  // past the table) is recorded and masked, and fetched from block 0
+  const int q_lo = kStep ? sm.items[0].q_start : 0;
+  const int q_hi = kStep ? sm.items[n_items - 1].q_start + sm.items[n_items - 1].n : npg;
+  int ok = 1;
+  for (int q = q_lo + tid; q < q_hi; q += kThreads) {
+    int lo = 0, hi = n_items - 1;
+    while (lo < hi) {  // last item with q_start <= q
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.items[mid].q_start <= q) lo = mid; else hi = mid - 1;
+    }
+    int32_t blk = -1;
+    const Item& it = sm.items[lo];
+    const int page = p.page_offset + it.p0 + (q - it.q_start);
+    if (q < it.q_start + it.n && page < p.max_blocks_per_req)
+      blk = p.block_tables[(size_t)it.r * p.max_blocks_per_req + page];
+    if (blk < 0 || blk >= p.num_blocks) {
+      record_error(p.err, PA_ERR_DEVICE_INDEX);
+      blk = -1;
+      ok = 0;
+    }
+    sm.ids[q] = blk;
+  }
+  if (tid == 0) {
+    // pages the items cover: exactly these are issued, and every one of
+    // them is consumed, so no copy is in flight when the window ends
+    sm.n_cov = sm.items[n_items - 1].q_start + sm.items[n_items - 1].n;
+  }
+  const bool ids_ok = __syncthreads_and(ok) != 0;
+  n_cov = sm.n_cov;
+
+
+  if (tid == 0) {
+    // a later window refills stages the warps have read (generic proxy)
+    if (kStep && q_lo > 0) fence_proxy_async_smem();
+    const int n0 = min(n_cov, q_lo + kStages);
+    for (int i = q_lo; i < n0; ++i) issue(i);
+  }
   for (int k = 0; k < n_items && !aborted; ++k) {
     const Item& it = sm.items[k];
     const int tok = it.tok;
@@ -405,6 +578,38 @@ __global__ void __launch_bounds__(kThreads, 3)
     // segment page at which this token slot is past the row's end (the
     // row's last page, when this slot is beyond its tokens), else none
     const int q_inv = (ts < tail_tokens) ? -1 : qg + (pages_r - 1 - it.p0);
+    // decode step: the CTA holding the row's last page appends the new token
+    // (position L - 1) to its slot and reads it from shared memory at that
+    // page instead of the stage (the stage's copy may predate the store).
+    // The 8 threads of its token slot each move and later read only their
+    // own 32 bytes of the K and V rows.
+    int q_new = -1;
+    if constexpr (kStep) {
+      if (it.p0 + it.n == pages_r && ts == tail_tokens - 1) {
+        q_new = qg + it.n - 1;
+        const size_t noff = ((size_t)it.r * Hkv + kvh) * kHeadDim;
+        const uint4* kn = reinterpret_cast<const uint4*>(p.k_new + noff);
+        const uint4* vn = reinterpret_cast<const uint4*>(p.v_new + noff);
+        const uint4 k0 = kn[c], k1 = kn[8 + c], v0 = vn[c], v1 = vn[8 + c];
+        uint4* ks = reinterpret_cast<uint4*>(sm.knew);
+        uint4* vs = reinterpret_cast<uint4*>(sm.vnew);
+        ks[c] = k0;
+        ks[8 + c] = k1;
+        vs[c] = v0;
+        vs[8 + c] = v1;
+        const int blk = sm.ids[q_new];
+        if (blk >= 0) {
+          const size_t dst = (((size_t)blk * Hkv + kvh) * kPage + (tail_tokens - 1)) * kHeadDim;
+          uint4* kd = reinterpret_cast<uint4*>(p.k_store + dst);
+          uint4* vd = reinterpret_cast<uint4*>(p.v_store + dst);
+          kd[c] = k0;
+          kd[8 + c] = k1;
+          vd[c] = v0;
+          vd[8 + c] = v1;
+        }
+      }
+    }
+
 
     // q of the 4 heads of this group, scaled into the log2 domain, as head
     // pairs (h0, h1), (h2, h3) per dim of this thread
@@ -465,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         qk16_q8(qp, *reinterpret_cast<const uint2*>(kr1 + 8 * c), *reinterpret_cast<const uint2*>(kr1 + 64 + 8 * c),
                 kdA1, kdB1, sB01, sB23);
       } else {
-        const uint8_t* kr0 = sm.k[sa] + ts * (kHeadDim * 2);
-        const uint8_t* kr1 = sm.k[sb] + ts * (kHeadDim * 2);
+        const uint8_t* kr0 = (kStep && qa == q_new) ? sm.knew : sm.k[sa] + ts * (kHeadDim * 2);
+        const uint8_t* kr1 = (kStep && qb == q_new) ? sm.knew : sm.k[sb] + ts * (kHeadDim * 2);
         const uint4 ka0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
         const uint4 kb0 = *reinterpret_cast<const uint4*>(kr0 + 128 + 16 * c);
         const uint4 ka1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
@@ -525,12 +730,12 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
       } else {
         if (valid0) {
-          const uint8_t* vr = sm.v[sa] + ts * (kHeadDim * 2);
+          const uint8_t* vr = (kStep && qa == q_new) ? sm.vnew : sm.v[sa] + ts * (kHeadDim * 2);
           pv16(acc, pA, *reinterpret_cast<const uint4*>(vr + 16 * c),
                *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
         }
         if (valid1) {
-          const uint8_t* vr = sm.v[sb] + ts * (kHeadDim * 2);
+          const uint8_t* vr = (kStep && qb == q_new) ? sm.vnew : sm.v[sb] + ts * (kHeadDim * 2);
           pv16(acc, pB, *reinterpret_cast<const uint4*>(vr + 16 * c),
                *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
         }
@@ -651,9 +856,14 @@ __global__ void __launch_bounds__(kThreads, 3)
       continue;
     }
     // the item is cut by segment boundaries: publish this CTA's partial
-    const int A = S0 + it.q_start - it.p0;  // stream position of the row's page 0
-    const int b0 = A / plan.seg, b1 = (A + pages_r - 1) / plan.seg;  // segments holding the row
-    const int jslot = (k == 0) ? 0 : 1;
+    const int A = it.A;
+    // segments holding the row's pages: the row starts at stream position A,
+    // its pages at A + kAlpha.  Its piece in segment b0 is that CTA's last
+    // item (slot 1) when the segment starts before the row, else its first
+    int seg_len;
+    if constexpr (kStep) seg_len = sm.seg_cost; else seg_len = plan.seg;
+    const int b0 = (A + kAlpha) / seg_len, b1 = (A + kAlpha + pages_r - 1) / seg_len;
+    const int jslot = ((kStep ? win0 : 0) + k == 0) ? 0 : 1;
     const size_t slot = ((size_t)b * 2 + jslot) * kGroup + g;
     *reinterpret_cast<float4*>(p.piece_o + slot * kHeadDim + d0) = o;
     if (lane == 0) p.piece_lse[slot] = lse2;
@@ -672,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int c0 = 0; c0 < n_pc; c0 += 32) {
         const int bb = b0 + c0 + lane;
         if (c0 + lane < n_pc) {
-          const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+          const int jj = (bb == b0 && b0 * seg_len < A) ? 1 : 0;
           Mx = fmaxf(Mx, __ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g));
         }
       }
@@ -686,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 3)
           float w = 0.f;
           if (lane < nc) {
             const int bb = b0 + c0 + lane;
-            const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+            const int jj = (bb == b0 && b0 * seg_len < A) ? 1 : 0;
             w = fast_exp2(__ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g) - Mx);
           }
           float ws = w;
@@ -696,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll 4
           for (int i = 0; i < nc; ++i) {
             const int bb = b0 + c0 + i;
-            const int jj = (bb == b0 && A != b0 * plan.seg) ? 1 : 0;
+            const int jj = (bb == b0 && b0 * seg_len < A) ? 1 : 0;
             const size_t sl = ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
             const float wi = __shfl_sync(0xffffffffu, w, i);
             const float4 x = __ldcg(reinterpret_cast<const float4*>(p.piece_o + sl * kHeadDim + d0));
@@ -722,6 +932,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     bar_all();  // the merge scratch and is_last are free again
   }
+  if (aborted || !kStep) break;
+  // next window: every item of this one is done (the barrier at its end)
+  // and its pages are consumed, so the ring is empty
+  win0 += n_items;
+  if (win0 >= sm.n_items_all) break;
+  if constexpr (kStep) step_window(p, plan, sm, kvh, sidx, (int)gridDim.x / Hkv, win0);
+  }
 
   __syncthreads();  // every thread has left the item loop
   if (*reinterpret_cast<volatile int*>(&sm.abort_flag) && tid == 0) {
@@ -734,26 +951,32 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-bool g_decode_attr_set[2][64] = {};
+bool g_decode_attr_set[3][64] = {};
 
-template <bool kQ8>
-cudaError_t launch_decode_as(const DecodeParams& p, const DecodePlan& plan, int grid, cudaStream_t stream) {
+template <bool kQ8, bool kStep>
+cudaError_t launch_decode_as(const DecodeParams& p, const typename PlanOf<kStep>::type& plan, int grid,
+                             cudaStream_t stream) {
   constexpr size_t kSmem = sizeof(DecodeSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
+  constexpr int kVariant = kStep ? 2 : (kQ8 ? 1 : 0);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !g_decode_attr_set[kQ8][dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  if (dev < 64 && !g_decode_attr_set[kVariant][dev]) {
+    e = cudaFuncSetAttribute(decode_kernel<kQ8, kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
-    g_decode_attr_set[kQ8][dev] = true;
+    g_decode_attr_set[kVariant][dev] = true;
   }
-  return launch_pdl(decode_kernel<kQ8>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
+  return launch_pdl(decode_kernel<kQ8, kStep>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, cudaStream_t stream) {
-  return q8 ? launch_decode_as<true>(p, plan, grid, stream) : launch_decode_as<false>(p, plan, grid, stream);
+  return q8 ? launch_decode_as<true, false>(p, plan, grid, stream) : launch_decode_as<false, false>(p, plan, grid, stream);
+}
+
+cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream) {
+  return launch_decode_as<false, true>(p, plan, grid, stream);
 }
 
 }  // namespace pa

@@ -51,6 +51,27 @@ struct DecodePlan {
   int32_t first_page[kPlanMaxCtas];   // that page's index within its row
 };
 
+// Decode step (self-planned launch): the kernel parameters carry only the
+// padded batch size and the longest valid seq_len; each CTA plans its own
+// segment from the device seq_lens, so one captured launch serves any
+// lengths within these bounds.  A row costs its pages plus kStepItemCost
+// stream units (the item-end merge work, in pages of streaming), and the
+// stream is cut into segments of at least kStepMinSegCost units.
+struct StepPlan {
+  int32_t n_rows;       // rows of the padded batch (<= kPlanMaxRows)
+  int32_t max_seq_len;  // rows with a longer seq_len are errors
+};
+constexpr int kStepItemCost = 8;
+constexpr int kStepMinSegCost = 8;
+template <bool kStep>
+struct PlanOf {
+  using type = DecodePlan;
+};
+template <>
+struct PlanOf<true> {
+  using type = StepPlan;
+};
+
 struct DecodeParams {
   const uint16_t* q;
   const uint16_t* k_cache;
@@ -75,6 +96,12 @@ struct DecodeParams {
   int* counters;         // [num_reqs, Hkv] CTAs finished per item; zero between calls
   float* scratch;        // [grid, kScratchFloats]: per-CTA merge scratch
   int* err;
+  // decode step only: the new token of every row ([rows, Hkv, D] bf16) and
+  // the pools it is appended to (the same memory as k_cache / v_cache)
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_store;
+  uint16_t* v_store;
 };
 // per-CTA merge scratch: 4 warps x 4 heads x D sums, then 4 x 4 max and sum
 constexpr int kScratchFloats = 4 * 4 * 128 + 2 * 4 * 4;
@@ -163,6 +190,7 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_kv_append_q8(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, cudaStream_t stream);
+cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
                            cudaStream_t stream);
 cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream);

@@ -125,16 +125,37 @@ struct WorkspaceLayout {
   size_t counters, piece_o, piece_lse, scratch, total;
 };
 
-WorkspaceLayout layout(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim, int32_t max_seq_len) {
+WorkspaceLayout layout_for_grid(int32_t num_reqs, int32_t hkv, int32_t head_dim, int grid) {
   WorkspaceLayout w;
-  const int32_t hkv = std::max(std::max(num_q_heads, 0) / PA_GQA_GROUP, 1);
-  const size_t slots = (size_t)2 * grid_cap(num_reqs, hkv, max_seq_len) * PA_GQA_GROUP;
+  const size_t slots = (size_t)2 * grid * PA_GQA_GROUP;
   w.counters = PA_ERROR_WORD_BYTES;
   w.piece_o = w.counters + align256((size_t)std::max(num_reqs, 0) * (size_t)hkv * 4);
   w.piece_lse = w.piece_o + align256(slots * (size_t)std::max(head_dim, 0) * 4);
   w.scratch = w.piece_lse + align256(slots * 4);
-  w.total = w.scratch + align256((size_t)grid_cap(num_reqs, hkv, max_seq_len) * pa::kScratchFloats * 4);
+  w.total = w.scratch + align256((size_t)grid * pa::kScratchFloats * 4);
   return w;
+}
+
+WorkspaceLayout layout(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim, int32_t max_seq_len) {
+  const int32_t hkv = std::max(std::max(num_q_heads, 0) / PA_GQA_GROUP, 1);
+  return layout_for_grid(num_reqs, hkv, head_dim, grid_cap(num_reqs, hkv, max_seq_len));
+}
+
+// Decode step: the launch shape, a function of the call's scalars only (so a
+// captured launch is valid for every batch within them).  Segments per kv
+// head: enough for one wave of resident CTAs when the largest stream allows
+// it, and always enough that a segment of the largest stream holds at most
+// kDecodeMaxPagesPerCta units.  -1 when that needs more than kPlanMaxCtas.
+int step_grid(int32_t num_reqs, int32_t hkv, int32_t max_seq_len) {
+  const int64_t cost = (int64_t)std::max(num_reqs, 0) * (pages_of(max_seq_len) + pa::kStepItemCost);
+  const int64_t wave = std::max<int64_t>(1, (int64_t)sm_count() * kDecodeCtasPerSm / std::max(hkv, 1));
+  int64_t nseg = std::min<int64_t>(wave, (cost + pa::kStepMinSegCost - 1) / pa::kStepMinSegCost);
+  const int forced = g_forced_ctas.load();  // pa_set_decode_ctas
+  if (forced > 0) nseg = (forced + std::max(hkv, 1) - 1) / std::max(hkv, 1);
+  nseg = std::max<int64_t>(nseg, (cost + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta);
+  nseg = std::max<int64_t>(nseg, 1);
+  if (nseg * hkv > pa::kPlanMaxCtas) return -1;
+  return (int)(nseg * hkv);
 }
 
 // Shared-prefix pass: the chunk count for a call and the workspace region
@@ -473,7 +494,7 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
   }
 
   if (!decode_rows.empty()) {
-    pa::DecodeParams dp;
+    pa::DecodeParams dp{};
     dp.q = static_cast<const uint16_t*>(q);
     dp.k_cache = static_cast<const uint16_t*>(k_cache);
     dp.v_cache = static_cast<const uint16_t*>(v_cache);
@@ -646,6 +667,85 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
   return attention(q, k_cache, v_cache, num_blocks, block_tables, max_blocks_per_req, seq_lens, qo_indptr,
                    seq_lens_host, qo_indptr_host, num_reqs, total_q, num_q_heads, num_kv_heads, head_dim, block_size,
                    0, sm_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+size_t pa_decode_step_workspace_size(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim,
+                                     int32_t max_seq_len) {
+  if (num_reqs < 0 || num_reqs > pa::kPlanMaxRows || num_q_heads < PA_GQA_GROUP || head_dim < 0 || max_seq_len < 1 ||
+      max_seq_len > PA_MAX_SEQ_LEN)
+    return 0;
+  const int32_t hkv = num_q_heads / PA_GQA_GROUP;
+  const int grid = step_grid(num_reqs, hkv, max_seq_len);
+  if (grid < 0) return 0;
+  return layout_for_grid(num_reqs, hkv, head_dim, grid).total;
+}
+
+int32_t pa_decode_step_bucket(int32_t num_reqs) {
+  if (num_reqs < 0 || num_reqs > pa::kPlanMaxRows) return -1;
+  int32_t b = 1;
+  while (b < num_reqs) b <<= 1;
+  return b;
+}
+
+pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_req,
+                         const int32_t* seq_lens, int32_t num_reqs, int32_t max_seq_len, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size, float sm_scale, void* out,
+                         float* lse, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  pa_status s = check_shape(num_q_heads, num_kv_heads, head_dim, block_size);
+  if (s != PA_OK) return s;
+  if (num_reqs < 0 || num_reqs > pa::kPlanMaxRows)
+    return fail(PA_ERR_UNSUPPORTED, "num_reqs %d outside [0, %d]", num_reqs, pa::kPlanMaxRows);
+  if (max_seq_len < 1 || max_seq_len > PA_MAX_SEQ_LEN)
+    return fail(PA_ERR_INVALID_ARG, "max_seq_len %d outside [1, %d]", max_seq_len, PA_MAX_SEQ_LEN);
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be positive");
+  if (max_blocks_per_req < 1) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_req must be positive");
+  if (!(fabsf(sm_scale) < INFINITY)) return fail(PA_ERR_INVALID_ARG, "sm_scale must be finite");
+  if (!workspace || !k_cache || !v_cache ||
+      (num_reqs > 0 && (!q || !k_new || !v_new || !block_tables || !seq_lens || !out)))
+    return fail(PA_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(out, 16) || !aligned(workspace, 256) || !aligned(lse, 4) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+    return fail(PA_ERR_INVALID_ARG, "q, k_new, v_new, caches and out must be 16-byte aligned, workspace 256-byte aligned");
+  const int grid = step_grid(num_reqs, num_kv_heads, max_seq_len);
+  if (grid < 0)
+    return fail(PA_ERR_UNSUPPORTED, "%d rows of up to %d tokens need more than %d CTAs", num_reqs, max_seq_len,
+                pa::kPlanMaxCtas);
+  const WorkspaceLayout wl = layout_for_grid(num_reqs, num_kv_heads, head_dim, grid);
+  if (workspace_bytes < wl.total)
+    return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, wl.total);
+  if (num_reqs == 0) return ok();
+
+  char* ws = static_cast<char*>(workspace);
+  pa::DecodeParams dp{};
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.k_cache = static_cast<const uint16_t*>(k_cache);
+  dp.v_cache = static_cast<const uint16_t*>(v_cache);
+  dp.num_blocks = num_blocks;
+  dp.block_tables = block_tables;
+  dp.max_blocks_per_req = max_blocks_per_req;
+  dp.seq_lens = seq_lens;
+  dp.num_q_heads = num_q_heads;
+  dp.num_kv_heads = num_kv_heads;
+  dp.scale_log2 = sm_scale * pa::kLog2e;
+  dp.out = static_cast<uint16_t*>(out);
+  dp.lse = lse;
+  dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
+  dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
+  dp.counters = reinterpret_cast<int*>(ws + wl.counters);
+  dp.scratch = reinterpret_cast<float*>(ws + wl.scratch);
+  dp.err = reinterpret_cast<int*>(ws);
+  dp.k_new = static_cast<const uint16_t*>(k_new);
+  dp.v_new = static_cast<const uint16_t*>(v_new);
+  dp.k_store = static_cast<uint16_t*>(k_cache);
+  dp.v_store = static_cast<uint16_t*>(v_cache);
+  pa::StepPlan plan;
+  plan.n_rows = num_reqs;
+  plan.max_seq_len = max_seq_len;
+  s = run_launch(PA_KERNEL_DECODE_STEP, "decode_step", stream,
+                 [&] { return pa::launch_decode_step(dp, plan, grid, stream); });
+  return s == PA_OK ? ok() : s;
 }
 
 size_t pa_shared_prefix_workspace_size(int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t head_dim,

@@ -285,8 +285,13 @@ def step_bytes(b: Batch, prefix_pages: int = 0, kv: str = "bf16") -> dict:
         pre_tab += 4 * (-(-L // P) - prefix_pages)
         pre_flops += (c * h + c * (c + 1) // 2) * Hq * D * 4
     prefill_kernel = pre_kv + pre_q + pre_tab
+    # the decode step's one kernel (pa_decode_step): the decode kernel's
+    # bytes plus the append of every row's new token (read as bf16, written
+    # into its page) and the seq_lens it plans from
+    step_kernel = decode_kernel + n_dec * (new_tok + per_tok) + 4 * len(seq)
     return dict(unique=unique_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
                 logical=logical_kv + qo_bytes + table_bytes + meta_bytes + append_bytes,
                 unique_kv=unique_kv, logical_kv=logical_kv, decode_kernel=decode_kernel,
                 prefix_kernel=prefix_kernel, prefill_kernel=prefill_kernel, prefill_flops=pre_flops,
+                step_kernel=step_kernel,
                 query_tokens=int(total_q))

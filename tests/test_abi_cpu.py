@@ -176,3 +176,55 @@ def test_q8_validation():
     assert lib.pa_attention_varlen_q8(FAKE, FAKE, FAKE, 64, FAKE, 40, FAKE, FAKE, slh, qih, 2, 5, 32, 8, 128, 16,
                                       0.088, FAKE, None, FAKE, 1 << 30, None) == b.PA_ERR_UNSUPPORTED
     assert "q8_0" in lib.pa_last_error_message().decode()
+
+
+def test_decode_step_sizes_and_buckets():
+    assert [b.pa_decode_step_bucket(n) for n in (0, 1, 2, 3, 5, 64, 65, 1024)] == [1, 1, 2, 4, 8, 64, 128, 1024]
+    assert b.pa_decode_step_bucket(1025) == -1 and b.pa_decode_step_bucket(-1) == -1
+    small = b.pa_decode_step_workspace_size(8, 32, 128, 4096)
+    assert small > b.PA_ERROR_WORD_BYTES and small % 256 == 0
+    # the size depends only on the scalars; more rows or longer rows never shrink it
+    assert b.pa_decode_step_workspace_size(8, 32, 128, 4096) == small
+    assert b.pa_decode_step_workspace_size(64, 32, 128, 4096) >= small
+    assert b.pa_decode_step_workspace_size(8, 32, 128, 1 << 16) >= small
+    for bad in [(1025, 32, 128, 4096), (8, 32, 128, 0), (8, 32, 128, (1 << 20) + 1), (-1, 32, 128, 16),
+                (8, 2, 128, 16), (1024, 32, 128, 1 << 20)]:
+        assert b.pa_decode_step_workspace_size(*bad) == 0, bad
+
+
+def _step(**kw):
+    a = dict(q=FAKE, kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, nb=64, bt=FAKE, mb=40, sl=FAKE, R=4, maxlen=600, Hq=32,
+             Hkv=8, D=128, P=16, scale=0.088, out=FAKE, lse=None, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.pa_decode_step(a["q"], a["kn"], a["vn"], a["k"], a["v"], a["nb"], a["bt"], a["mb"], a["sl"], a["R"],
+                              a["maxlen"], a["Hq"], a["Hkv"], a["D"], a["P"], a["scale"], a["out"], a["lse"], a["ws"],
+                              a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), b.PA_ERR_INVALID_ARG),
+    (dict(kn=None), b.PA_ERR_INVALID_ARG),
+    (dict(sl=None), b.PA_ERR_INVALID_ARG),
+    (dict(ws=None), b.PA_ERR_INVALID_ARG),
+    (dict(vn=ctypes.c_void_p((1 << 20) + 8)), b.PA_ERR_INVALID_ARG),
+    (dict(maxlen=0), b.PA_ERR_INVALID_ARG),
+    (dict(maxlen=(1 << 20) + 1), b.PA_ERR_INVALID_ARG),
+    (dict(nb=0), b.PA_ERR_INVALID_ARG),
+    (dict(mb=0), b.PA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), b.PA_ERR_INVALID_ARG),
+    (dict(R=1025), b.PA_ERR_UNSUPPORTED),
+    (dict(Hkv=4), b.PA_ERR_UNSUPPORTED),
+    (dict(D=64), b.PA_ERR_UNSUPPORTED),
+    (dict(wsb=1024), b.PA_ERR_WORKSPACE_TOO_SMALL),
+    (dict(R=1024, maxlen=1 << 20), b.PA_ERR_UNSUPPORTED),
+])
+def test_decode_step_validation(kw, status):
+    n0 = lib.pa_launch_count()
+    assert _step(**kw) == status, lib.pa_last_error_message().decode()
+    assert lib.pa_launch_count() == n0
+
+
+def test_decode_step_empty_batch_launches_nothing():
+    n0 = lib.pa_launch_count()
+    assert _step(R=0, q=None, kn=None, vn=None, bt=None, sl=None, out=None) == b.PA_OK
+    assert lib.pa_launch_count() == n0
