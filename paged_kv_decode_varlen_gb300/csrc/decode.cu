@@ -86,15 +86,11 @@ struct __align__(128) DecodeSmem {
   int n_items_all;           // items of the segment
   int seg_cost;              // segment length in stream units (self-planned)
   int scan[kThreads / 32];   // per-warp totals of the planning scans
-  alignas(16) uint8_t knew[kHeadDim * 2];  // decode step: the appended token's K row (16-byte accesses)
-  alignas(16) uint8_t vnew[kHeadDim * 2];  // and V row
   int stage_page[kStages];   // last page issued into each stage (-1: none)
   int abort_flag;
   int is_last;
 };
 
-static_assert(offsetof(DecodeSmem<kSlabBytes>, knew) % 16 == 0 && offsetof(DecodeSmem<kSlabBytes>, vnew) % 16 == 0,
-              "the appended rows are read and written with 16-byte accesses");
 static_assert(offsetof(DecodeSmem<kSlabBytes>, k) % 128 == 0 && offsetof(DecodeSmem<kSlabBytes>, v) % 128 == 0 &&
                   offsetof(DecodeSmem<kQ8SlabBytes>, v) % 16 == 0,
               "bulk copies land on 16-byte boundaries");
@@ -558,6 +554,26 @@ __global__ void __launch_bounds__(kThreads, 3)
     // them is consumed, so no copy is in flight when the window ends
     sm.n_cov = sm.items[n_items - 1].q_start + sm.items[n_items - 1].n;
   }
+  if constexpr (kStep) {
+    // decode step: the CTA that streams a row's last page appends the row's
+    // new token (position L - 1) for its kv head before any copy of the
+    // window is issued; the proxy fence and the barrier below order the
+    // stores before the bulk copies that read the page.  32 threads move one
+    // row's 256 bytes of K and of V.
+    for (int w = tid; w < n_items * 32; w += kThreads) {
+      const Item& it = sm.items[w >> 5];
+      if (it.p0 + it.n != (it.L + kPage - 1) / kPage) continue;  // not the row's last page
+      const int pos = it.L - 1;
+      const int blk = p.block_tables[(size_t)it.r * p.max_blocks_per_req + pos / kPage];
+      if (blk < 0 || blk >= p.num_blocks) continue;  // recorded by the id check above
+      const int j = w & 31;
+      const size_t src = ((size_t)it.r * Hkv + kvh) * kHeadDim;
+      const size_t dst = (((size_t)blk * Hkv + kvh) * kPage + pos % kPage) * kHeadDim;
+      const uint4 x = reinterpret_cast<const uint4*>((j < 16 ? p.k_new : p.v_new) + src)[j & 15];
+      reinterpret_cast<uint4*>((j < 16 ? p.k_store : p.v_store) + dst)[j & 15] = x;
+    }
+    fence_proxy_async_global();
+  }
   const bool ids_ok = __syncthreads_and(ok) != 0;
   n_cov = sm.n_cov;
 
@@ -578,39 +594,6 @@ __global__ void __launch_bounds__(kThreads, 3)
     // segment page at which this token slot is past the row's end (the
     // row's last page, when this slot is beyond its tokens), else none
     const int q_inv = (ts < tail_tokens) ? -1 : qg + (pages_r - 1 - it.p0);
-    // decode step: the CTA holding the row's last page appends the new token
-    // (position L - 1) to its slot and reads it from shared memory at that
-    // page instead of the stage (the stage's copy may predate the store).
-    // The 8 threads of its token slot each move and later read only their
-    // own 32 bytes of the K and V rows.
-    int q_new = -1;
-    if constexpr (kStep) {
-      if (it.p0 + it.n == pages_r && ts == tail_tokens - 1) {
-        q_new = qg + it.n - 1;
-        const size_t noff = ((size_t)it.r * Hkv + kvh) * kHeadDim;
-        const uint4* kn = reinterpret_cast<const uint4*>(p.k_new + noff);
-        const uint4* vn = reinterpret_cast<const uint4*>(p.v_new + noff);
-        const uint4 k0 = kn[c], k1 = kn[8 + c], v0 = vn[c], v1 = vn[8 + c];
-        uint4* ks = reinterpret_cast<uint4*>(sm.knew);
-        uint4* vs = reinterpret_cast<uint4*>(sm.vnew);
-        ks[c] = k0;
-        ks[8 + c] = k1;
-        vs[c] = v0;
-        vs[8 + c] = v1;
-        const int blk = sm.ids[q_new];
-        if (blk >= 0) {
-          const size_t dst = (((size_t)blk * Hkv + kvh) * kPage + (tail_tokens - 1)) * kHeadDim;
-          uint4* kd = reinterpret_cast<uint4*>(p.k_store + dst);
-          uint4* vd = reinterpret_cast<uint4*>(p.v_store + dst);
-          kd[c] = k0;
-          kd[8 + c] = k1;
-          vd[c] = v0;
-          vd[8 + c] = v1;
-        }
-      }
-    }
-
-
     // q of the 4 heads of this group, scaled into the log2 domain, as head
     // pairs (h0, h1), (h2, h3) per dim of this thread
     float2 qp[2][16];
@@ -651,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       bool valid1 = has1 && (qb != q_inv);
       if (!ids_ok) {
         valid0 = valid0 && sm.ids[qa] >= 0;
-        valid1 = valid1 && sm.ids[min(qb, npg - 1)] >= 0;
+        valid1 = valid1 && sm.ids[min(qb, (kStep ? kDecodeMaxPagesPerCta : npg) - 1)] >= 0;
       }
       // a missing second page reads whatever stage sb holds; its scores are
       // masked below and its V is not read
@@ -670,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         qk16_q8(qp, *reinterpret_cast<const uint2*>(kr1 + 8 * c), *reinterpret_cast<const uint2*>(kr1 + 64 + 8 * c),
                 kdA1, kdB1, sB01, sB23);
       } else {
-        const uint8_t* kr0 = (kStep && qa == q_new) ? sm.knew : sm.k[sa] + ts * (kHeadDim * 2);
-        const uint8_t* kr1 = (kStep && qb == q_new) ? sm.knew : sm.k[sb] + ts * (kHeadDim * 2);
+        const uint8_t* kr0 = sm.k[sa] + ts * (kHeadDim * 2);
+        const uint8_t* kr1 = sm.k[sb] + ts * (kHeadDim * 2);
         const uint4 ka0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
         const uint4 kb0 = *reinterpret_cast<const uint4*>(kr0 + 128 + 16 * c);
         const uint4 ka1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
@@ -730,12 +713,12 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
       } else {
         if (valid0) {
-          const uint8_t* vr = (kStep && qa == q_new) ? sm.vnew : sm.v[sa] + ts * (kHeadDim * 2);
+          const uint8_t* vr = sm.v[sa] + ts * (kHeadDim * 2);
           pv16(acc, pA, *reinterpret_cast<const uint4*>(vr + 16 * c),
                *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
         }
         if (valid1) {
-          const uint8_t* vr = (kStep && qb == q_new) ? sm.vnew : sm.v[sb] + ts * (kHeadDim * 2);
+          const uint8_t* vr = sm.v[sb] + ts * (kHeadDim * 2);
           pv16(acc, pB, *reinterpret_cast<const uint4*>(vr + 16 * c),
                *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
         }
