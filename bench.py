@@ -76,10 +76,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
+def profiled_traffic(workload, kernel="decode"):
+    """DRAM bytes per launch of the decode kernel (kernel = "decode") or of
+    the decode step ("decode_step") from the committed ncu summary, if it was
     taken on the current decode kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.json")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
@@ -601,7 +602,8 @@ def main():
         "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2) if achieved else None,
                      "peak": r_peak, "peak_source": r_source, "unit": r_unit,
                      "frac": round(achieved / r_peak, 4) if achieved else None,
-                     "traffic": profiled_traffic(args.workload) if dom == "decode" and not q8 else None,
+                     "traffic": (profiled_traffic(args.workload, dom)
+                                 if dom in ("decode", "decode_step") and not q8 else None),
                      "algorithmic_bytes_per_launch": dom_bytes,
                      **({"algorithmic_flops_per_launch": dom_flops} if dom_flops else {}),
                      "avg_launch_ms": round(dom_ms, 5) if dom_ms else None,
