@@ -111,39 +111,60 @@ __device__ __forceinline__ void unpack16s(const uint4& a, const uint4& b, float*
   }
 }
 
-// Partial scores of one token over this thread's 16 dims as head pairs
-// (h0, h1) and (h2, h3): qp[h][i] = (q[2h][dim i], q[2h+1][dim i]).
+// Partial scores of one token over this thread's 16 dims (bf16 pages), with
+// the dims paired: qp[hp][8 e + j] = (q[2 hp + e][dim 2j], q[2 hp + e][dim
+// 2j + 1]).  A K word holds two consecutive dims, so it unpacks straight into
+// the operand pair of a packed fp32x2 FMA; each head's two lanes are added
+// at the end.  Returns the (h0, h1) and (h2, h3) score pairs.
 __device__ __forceinline__ void qk16(const float2 (&qp)[2][16], const uint4& ka, const uint4& kb, float2& s01,
                                      float2& s23) {
-  float kf[16];
-  unpack16s(ka, kb, kf);
-  float2 a0 = __fmul2_rn(qp[0][0], make_float2(kf[0], kf[0]));
-  float2 a1 = __fmul2_rn(qp[0][1], make_float2(kf[1], kf[1]));
-  float2 c0 = __fmul2_rn(qp[1][0], make_float2(kf[0], kf[0]));
-  float2 c1 = __fmul2_rn(qp[1][1], make_float2(kf[1], kf[1]));
+  float2 k2[8];
+  unpack16(ka, kb, k2);
+  float2 a0 = __fmul2_rn(qp[0][0], k2[0]);
+  float2 a1 = __fmul2_rn(qp[0][8], k2[0]);
+  float2 a2 = __fmul2_rn(qp[1][0], k2[0]);
+  float2 a3 = __fmul2_rn(qp[1][8], k2[0]);
 #pragma unroll
-  for (int i = 2; i < 16; i += 2) {
-    a0 = __ffma2_rn(qp[0][i], make_float2(kf[i], kf[i]), a0);
-    a1 = __ffma2_rn(qp[0][i + 1], make_float2(kf[i + 1], kf[i + 1]), a1);
-    c0 = __ffma2_rn(qp[1][i], make_float2(kf[i], kf[i]), c0);
-    c1 = __ffma2_rn(qp[1][i + 1], make_float2(kf[i + 1], kf[i + 1]), c1);
+  for (int j = 1; j < 8; ++j) {
+    a0 = __ffma2_rn(qp[0][j], k2[j], a0);
+    a1 = __ffma2_rn(qp[0][8 + j], k2[j], a1);
+    a2 = __ffma2_rn(qp[1][j], k2[j], a2);
+    a3 = __ffma2_rn(qp[1][8 + j], k2[j], a3);
   }
-  s01 = __fadd2_rn(a0, a1);
-  s23 = __fadd2_rn(c0, c1);
+  s01 = make_float2(a0.x + a0.y, a1.x + a1.y);
+  s23 = make_float2(a2.x + a2.y, a3.x + a3.y);
 }
 
-// q8_0 pages: 8 int8 codes (dims 8c..8c+7 or 64+8c..) -> 8 floats.
+// q8_0 pages: 8 int8 codes (dims 8c..8c+7 or 64+8c..) -> 8 floats, without
+// integer-to-float conversion instructions (exponent-bias construction): a
+// code c biased to c + 128 (flipping each byte's top bit) becomes the low
+// mantissa byte of a binary32 with exponent 2^23 (a byte permute), whose value
+// is 2^23 + c + 128 exactly; subtracting 2^23 + 128 gives c exactly.  Two
+// codes share one packed subtraction.
 __device__ __forceinline__ void codes8(const uint2& w, float* f) {
+  const uint32_t x = w.x ^ 0x80808080u, y = w.y ^ 0x80808080u;
+  const float2 bias = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[i] = (float)(int8_t)((w.x >> (8 * i)) & 0xffu);
-    f[4 + i] = (float)(int8_t)((w.y >> (8 * i)) & 0xffu);
+  for (int i = 0; i < 4; i += 2) {
+    // byte 0 from the word (selector nibble i), bytes 1-2 zero, byte 3 = 0x4B
+    const float2 a = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u + i)),
+                                            __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7441u + i))),
+                                bias);
+    const float2 b = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(y, 0x4B000000u, 0x7440u + i)),
+                                            __uint_as_float(__byte_perm(y, 0x4B000000u, 0x7441u + i))),
+                                bias);
+    f[i] = a.x;
+    f[i + 1] = a.y;
+    f[4 + i] = b.x;
+    f[5 + i] = b.y;
   }
 }
 
-// qk16 over q8_0 codes: the dims of ka lie in one 32-value group (scale
-// dA), those of kb in another (dB); each group's partial dot product is
-// scaled once.
+// qk16 over q8_0 codes, with q as head pairs per dim: qp[hp][i] =
+// (q[2 hp][dim i], q[2 hp + 1][dim i]).  The dims of ka lie in one 32-value
+// group (scale dA), those of kb in another (dB); each group's partial dot
+// product is scaled once.  (The dim-pair layout of qk16 measured ~1% slower
+// here: the int8 conversions, not the operand pairing, dominate.)
 __device__ __forceinline__ void qk16_q8(const float2 (&qp)[2][16], const uint2& ka, const uint2& kb, float dA,
                                         float dB, float2& s01, float2& s23) {
   float kf[16];
@@ -594,8 +615,9 @@ __global__ void __launch_bounds__(kThreads, 3)
     // segment page at which this token slot is past the row's end (the
     // row's last page, when this slot is beyond its tokens), else none
     const int q_inv = (ts < tail_tokens) ? -1 : qg + (pages_r - 1 - it.p0);
-    // q of the 4 heads of this group, scaled into the log2 domain, as head
-    // pairs (h0, h1), (h2, h3) per dim of this thread
+    // q of the 4 heads of this group, scaled into the log2 domain: for bf16
+    // pages as dim pairs per head (see qk16), for q8_0 pages as head pairs
+    // per dim (see qk16_q8)
     float2 qp[2][16];
     {
       const uint16_t* qrow = p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
@@ -607,7 +629,15 @@ __global__ void __launch_bounds__(kThreads, 3)
         unpack16s(*reinterpret_cast<const uint4*>(qrow + (2 * hp + 1) * kHeadDim + 8 * c),
                   *reinterpret_cast<const uint4*>(qrow + (2 * hp + 1) * kHeadDim + 64 + 8 * c), f1);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) qp[hp][i] = make_float2(f0[i] * p.scale_log2, f1[i] * p.scale_log2);
+        for (int i = 0; i < 16; ++i) {
+          if constexpr (kQ8) {
+            qp[hp][i] = make_float2(f0[i] * p.scale_log2, f1[i] * p.scale_log2);
+          } else {
+            const float* f = (i < 8) ? f0 : f1;
+            const int j = i & 7;
+            qp[hp][i] = make_float2(f[2 * j] * p.scale_log2, f[2 * j + 1] * p.scale_log2);
+          }
+        }
       }
     }
     float2 acc[kGroup][8];
