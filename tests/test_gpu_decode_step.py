@@ -232,3 +232,59 @@ def test_step_errors_recorded_without_fault():
     torch.cuda.synchronize()
     assert B.pa_get_device_error(ws) == B.PA_ERR_DEVICE_INDEX
     torch.zeros(1, device="cuda").sum().item()  # the context still works
+
+
+def test_step_sweep_point_b128_2048():
+    """The largest 2048-token sweep point (128 rows) through pa_decode_step,
+    against the oracle on every output."""
+    lens = [2048] * 128
+    h = step_inputs(lens, num_blocks=128 * 128 + 50, seed=371)
+    d = DevStep(h)
+    out, lse = run_step(d, h, 2048)
+    check(d, out, lse, h, 2048, "b128 x 2048")
+
+
+def test_step_graph_of_layers():
+    """A CUDA graph of 4 layers (one pa_decode_step each, own pools, one
+    shared workspace), as the 36-layer sweep captures it; every layer's
+    output and pools match the oracle after a replay with new lengths."""
+    R, maxlen, nb, layers = 8, 1024, 600, 4
+    lens0 = [1024, 700, 33, 1, 512, 0, 64, 999]
+    lens1 = [17, 1000, 256, 0, 0, 640, 1, 1024]
+    hs = [step_inputs(lens0, num_blocks=nb, seed=380 + l, max_blocks=64) for l in range(layers)]
+    ds = [DevStep(h) for h in hs]
+    ws = B.new_workspace(B.pa_decode_step_workspace_size(R, 32, 128, maxlen), "cuda")
+    outs = [torch.empty_like(d.q) for d in ds]
+    lses = [torch.empty((R, 32), dtype=torch.float32, device="cuda") for _ in ds]
+
+    def step():
+        for d, o, l_ in zip(ds, outs, lses):
+            B.pa_decode_step(d.q, d.k_new, d.v_new, d.k_cache, d.v_cache, d.block_tables, d.seq_lens,
+                             hs[0]["sm_scale"], maxlen, out=o, lse=l_, workspace=ws)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for lens, seed in ((lens0, 390), (lens1, 395)):
+        hs = [step_inputs(lens, num_blocks=nb, seed=seed + l, max_blocks=64) for l in range(layers)]
+        for d, h in zip(ds, hs):
+            d.load(h)
+        g.replay()
+        for l, (d, h) in enumerate(zip(ds, hs)):
+            check(d, outs[l], lses[l], h, maxlen, f"layer {l} lens {lens[:3]}", ws)
+
+
+def test_step_long_row_over_many_segments():
+    """One 150,000-token row among short ones: its pages span dozens of CTAs
+    (each segment at most 1,024 pages), its pieces are merged by the last."""
+    lens = [150_000, 40, 2, 5000]
+    h = step_inputs(lens, num_blocks=sum(-(-L // 16) for L in lens) + 10, seed=401)
+    d = DevStep(h)
+    ws = B.new_workspace(B.pa_decode_step_workspace_size(len(lens), 32, 128, 150_000), "cuda")
+    out, lse = run_step(d, h, 150_000, ws)
+    check(d, out, lse, h, 150_000, "long row", ws)
