@@ -27,7 +27,9 @@
 //     (128 columns).  S of tile j + 1 is queued before PV of tile j, so it
 //     runs while the softmax of tile j does; PV of tile j follows the
 //     softmax that wrote its P (bf16, to a double-buffered shared tile in the
-//     layout the MMA reads).
+//     layout the MMA reads).  The softmax of tile j waits only for PV of
+//     tile j - 2 (the last reader of its P buffer) unless it must rescale O,
+//     so its exponentials overlap PV of tile j - 1.
 //   * Online softmax in the log2 domain; the running max is re-based (and O
 //     in tensor memory rescaled) only when it grows by more than 2^8, so P
 //     stays below 256 and the rescale is rare.
@@ -312,15 +314,12 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
         l_run *= corr;
         m_run = mt;
       }
-      if (j > 0) {
-        // PV of tile j - 1 done (and with it every earlier PV: they form one
-        // chain on O): O is stable and the P tile of tile j - 2 is free.  S
-        // products go to other accumulators and may finish before it.
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O is rescaled: PV of tile j - 1 must be done (and with it every
+        // earlier PV: they form one chain on O), so O is stable
         ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err));
         if (!ok) break;
         fence_after_sync();
-      }
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // rescale the rows of O whose running max grew
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -330,6 +329,14 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
           for (int i = 0; i < 32; ++i) o[i] *= corr;
           tmem_st32(lane_base + kColO + 32 * c, o);
         }
+      } else if (j >= 2) {
+        // P tile j & 1 was last read by PV of tile j - 2, which must be done
+        // before it is rewritten (an S product goes to another accumulator
+        // and may finish before it).  PV of tile j - 1 may still run: the
+        // exponentials below overlap it.
+        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[j & 1], ((j - 2) >> 1) & 1, err));
+        if (!ok) break;
+        fence_after_sync();
       }
       const float nm = (m_run == -INFINITY) ? 0.f : -m_run;
       const float2 nm2 = make_float2(nm, nm);
