@@ -19,15 +19,16 @@
 //     heads.  Keys go in tiles of 128 (8 pages).
 //   * Warp roles: warps 4 and 6 issue tiled TMA copies (Q once; per key tile
 //     the two 64-dim halves of each page's K slab, resp. V slab, 128-byte
-//     swizzled, into 2-stage K and V rings: a K stage is refilled as soon as
-//     its S product is done); warp 5 owns the tensor memory and one of its
+//     swizzled, into a 4-stage K ring and a 2-stage V ring: a K stage is
+//     refilled as soon as its S product is done); warp 5 owns the tensor memory and one of its
 //     threads issues the MMAs; warps 0-3 run the softmax, one thread per row
 //     (tensor-memory lane = row).
-//   * Tensor memory: two S buffers of 128 fp32 columns and the O accumulator
-//     (128 columns).  S of tile j + 1 is queued before PV of tile j, so it
-//     runs while the softmax of tile j does; PV of tile j follows the
-//     softmax that wrote its P (bf16, to a double-buffered shared tile in the
-//     layout the MMA reads).  The softmax of tile j waits only for PV of
+//   * Tensor memory: two S buffers of 128 fp32 columns, the O accumulator
+//     (128 columns) and two P buffers of 64 columns (bf16 key pairs: P is the
+//     A operand of the PV product, read from tensor memory, which leaves the
+//     shared memory to the K ring).  S of tile j + 1 is queued before PV of
+//     tile j, so it runs while the softmax of tile j does; PV of tile j
+//     follows the softmax that wrote its P.  The softmax of tile j waits only for PV of
 //     tile j - 2 (the last reader of its P buffer) unless it must rescale O,
 //     so its exponentials overlap PV of tile j - 1.
 //   * Online softmax in the log2 domain; the running max is re-based (and O
@@ -55,13 +56,15 @@ constexpr int kPagesPerTile = kKeys / kPage;     // 8
 constexpr int kHalf = 128 * 128;                 // 128 rows x 64 bf16 (one 64-column half): 16 KiB
 constexpr int kTileBytes = 2 * kHalf;            // 32 KiB
 constexpr int kPageHalfBytes = kPage * 128;      // one page's rows of one half: 2 KiB
-constexpr int kStages = 2;
+constexpr int kKStages = 4;  // K ring: S of a tile waits for its K, so it runs deep
+constexpr int kVStages = 2;  // V ring: PV of a tile comes a softmax later
 constexpr int kSoftmaxWarps = 4;
 constexpr int kKWarp = 4, kMmaWarp = 5, kVWarp = 6;  // Q/K copies, MMA issue, V copies
 constexpr int kThreads = 7 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S buffers at columns 0 and 128
 constexpr uint32_t kColO = 256;  // O accumulator
+constexpr uint32_t kColP = 384;  // two P buffers of 64 columns (128 bf16 keys per lane, in pairs)
 constexpr float kRescaleSlack = 8.f;
 constexpr uint32_t kIdescS = idesc_bf16_f32(kRows, kKeys, false);     // Q (K-major) x K^T (K-major)
 constexpr uint32_t kIdescO = idesc_bf16_f32(kRows, kHeadDim, true);   // P (K-major) x V (MN-major)
@@ -69,12 +72,12 @@ static_assert(kRows == 128 && kKeys == 128, "tile shape");
 
 struct __align__(1024) TcSmem {
   uint8_t q[kTileBytes];
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
-  uint8_t p[2][kTileBytes];
+  uint8_t k[kKStages][kTileBytes];
+  uint8_t v[kVStages][kTileBytes];
   uint64_t bar_q;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];  // S of the stage's tile done: the stage may be refilled
+  uint64_t v_full[kVStages];
   uint64_t pv_done[2];  // PV of tile j done: phase j / 2 of pv_done[j % 2]
   uint64_t s_full[2];
   uint64_t p_full[2];
@@ -83,7 +86,7 @@ struct __align__(1024) TcSmem {
 };
 constexpr size_t kSmemBytes = sizeof(TcSmem) + 1024;  // + slack to align the base to 1024 B
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(offsetof(TcSmem, p) + 2 * kTileBytes <= sizeof(TcSmem), "staging area = both P tiles (64 KiB)");
+static_assert(kKStages >= 2, "staging area = the first two K stages (64 KiB)");
 
 __device__ __forceinline__ TcSmem& tc_smem() {
   extern __shared__ uint8_t tc_smem_raw[];
@@ -159,11 +162,11 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
 
   if (is_k && lane == 0) {
     mbar_init(&sm.bar_q, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.v_full[s], 1);
-
+      mbar_init(&sm.k_empty[s], 1);
     }
+    for (int s = 0; s < kVStages; ++s) mbar_init(&sm.v_full[s], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_full[b], kSoftmaxWarps * 32);
@@ -186,17 +189,20 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
   if (is_producer) {
     // ----------------------------------------------------------- producers
     // warp kKWarp: Q (above), then the K ring; warp kVWarp: the V ring.  A K
-    // stage is free once its S product is done (s_full), a V stage once its
-    // PV product is (pv_done); stage s serves tiles s, s + 2, ..., and so do
-    // both barrier pairs, so tile j waits for phase (j - 2) / 2.
+    // stage is free once its S product is done (k_empty), a V stage once its
+    // PV product is (pv_done); stage s serves tiles s, s + n, ... (n stages),
+    // so tile j waits for phase j / n - 1 of the stage's barrier.
     const CUtensorMap* map = is_k ? &maps.k : &maps.v;
     uint64_t* full = is_k ? sm.k_full : sm.v_full;
-    uint64_t* empty = is_k ? sm.s_full : sm.pv_done;
-    int last_issued[kStages] = {-1, -1};
+    uint64_t* empty = is_k ? sm.k_empty : sm.pv_done;
+    const int n_st = is_k ? kKStages : kVStages;
+    int last_issued[kKStages];
+#pragma unroll
+    for (int s = 0; s < kKStages; ++s) last_issued[s] = -1;
     if (lane == 0) prefetch_tensormap(map);
     for (int j = 0; j < n_tiles; ++j) {
-      const int s = j & (kStages - 1);
-      if (j >= kStages && !__all_sync(0xffffffffu, tc_wait(sm, &empty[s], ((j / kStages) - 1) & 1, err))) break;
+      const int s = j % n_st;
+      if (j >= n_st && !__all_sync(0xffffffffu, tc_wait(sm, &empty[s], ((j / n_st) - 1) & 1, err))) break;
       if (j > 0 && (j & 3) == 0) {
         grp_cur = grp_next;
         grp_next = load_group((j >> 2) + 1);
@@ -215,8 +221,8 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
     if (*reinterpret_cast<volatile int*>(&sm.abort) && lane == 0) {
       // let the copies in flight land before the CTA leaves (bounded)
       if (is_k) mbar_wait_bounded(&sm.bar_q, 0);
-      for (int s = 0; s < kStages; ++s)
-        if (last_issued[s] >= 0) mbar_wait_bounded(&full[s], (last_issued[s] / kStages) & 1);
+      for (int s = 0; s < n_st; ++s)
+        if (last_issued[s] >= 0) mbar_wait_bounded(&full[s], (last_issued[s] / n_st) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
@@ -224,8 +230,8 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       const uint32_t qb = smem_addr(sm.q);
       int last_s = -1, last_pv = -1;  // last S / PV issued
       auto issue_s = [&](int j) -> bool {
-        const int s = j & (kStages - 1);
-        if (!tc_wait(sm, &sm.k_full[s], (j / kStages) & 1, err)) return false;
+        const int s = j % kKStages;
+        if (!tc_wait(sm, &sm.k_full[s], (j / kKStages) & 1, err)) return false;
         fence_after_sync();
         last_s = j;
         const uint32_t kb = smem_addr(sm.k[s]);
@@ -235,7 +241,8 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
           const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;  // 64-dim half, 16-dim step in it
           mma_bf16(d, desc_sw128(qb + off, 16, 1024), desc_sw128(kb + off, 16, 1024), kIdescS, ks > 0);
         }
-        commit(&sm.s_full[j & 1]);  // one commit per MMA group
+        commit(&sm.s_full[j & 1]);  // one commit per MMA group and barrier
+        commit(&sm.k_empty[s]);
         return true;
       };
       // S runs one tile ahead: S(j + 1) is queued before PV(j), which waits
@@ -243,17 +250,16 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       bool ok = tc_wait(sm, &sm.bar_q, 0, err) && issue_s(0);
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-        const int s = j & (kStages - 1);
-        ok = tc_wait(sm, &sm.p_full[j & 1], (j >> 1) & 1, err) && tc_wait(sm, &sm.v_full[s], (j / kStages) & 1, err);
+        const int s = j % kVStages;
+        ok = tc_wait(sm, &sm.p_full[j & 1], (j >> 1) & 1, err) && tc_wait(sm, &sm.v_full[s], (j / kVStages) & 1, err);
         if (!ok) break;
         fence_after_sync();
-        const uint32_t pb = smem_addr(sm.p[j & 1]), vb = smem_addr(sm.v[s]);
+        const uint32_t pt = tmem + kColP + (uint32_t)(j & 1) * (kKeys / 2), vb = smem_addr(sm.v[s]);
 #pragma unroll
         for (int ks = 0; ks < kKeys / 16; ++ks) {
-          const uint32_t pa = pb + (ks >> 2) * kHalf + (ks & 3) * 32;  // 64-key half, 16-key step
-          const uint32_t va = vb + ks * 2 * 1024;                      // 16 keys = two 8-row groups
-          mma_bf16(tmem + kColO, desc_sw128(pa, 16, 1024), desc_sw128(va, kHalf, 1024), kIdescO,
-                   (j > 0 || ks > 0) ? 1u : 0u);
+          const uint32_t va = vb + ks * 2 * 1024;  // 16 keys = two 8-row groups
+          // A = P in tensor memory: 16 keys = 8 columns of bf16 pairs
+          mma_bf16_ts(tmem + kColO, pt + 8 * ks, desc_sw128(va, kHalf, 1024), kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
         }
         commit(&sm.pv_done[j & 1]);
         last_pv = j;
@@ -330,7 +336,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
           tmem_st32(lane_base + kColO + 32 * c, o);
         }
       } else if (j >= 2) {
-        // P tile j & 1 was last read by PV of tile j - 2, which must be done
+        // P buffer j & 1 was last read by PV of tile j - 2, which must be done
         // before it is rewritten (an S product goes to another accumulator
         // and may finish before it).  PV of tile j - 1 may still run: the
         // exponentials below overlap it.
@@ -343,25 +349,23 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       float2 ls4[4];  // 4 independent pair-sum chains
 #pragma unroll
       for (int i = 0; i < 4; ++i) ls4[i] = make_float2(0.f, 0.f);
-      uint8_t* prow = sm.p[j & 1] + r * 128;
+      // P of this row: 128 bf16 keys as 64 pairs, into this lane's P columns
+      const uint32_t prow = lane_base + kColP + (uint32_t)(j & 1) * (kKeys / 2);
 #pragma unroll
-      for (int c = 0; c < kKeys / 8; ++c) {  // 8 keys = one 16-byte chunk
-        uint32_t w[4];
+      for (int hf = 0; hf < 2; ++hf) {  // keys 64 hf .. + 63 = P columns 32 hf .. + 31
+        uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 d = __fadd2_rn(x[4 * c + i], nm2);
+        for (int i = 0; i < 32; ++i) {
+          const float2 d = __fadd2_rn(x[32 * hf + i], nm2);
           const float2 e = make_float2(fast_exp2(d.x), fast_exp2(d.y));
-          ls4[i] = __fadd2_rn(ls4[i], e);
+          ls4[i & 3] = __fadd2_rn(ls4[i & 3], e);
           w[i] = pack_bf16x2(e.x, e.y);
         }
-        // 64-key half c / 8, chunk c % 8 of the row, 128-byte swizzle
-        *reinterpret_cast<uint4*>(prow + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        tmem_st32u(prow + 32 * hf, w);
       }
       const float2 l2 = __fadd2_rn(__fadd2_rn(ls4[0], ls4[1]), __fadd2_rn(ls4[2], ls4[3]));
       l_run += l2.x + l2.y;
-      fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
-      fence_before_sync();       // tensor-memory reads / writes above precede the arrive
+      fence_before_sync();  // the tensor-memory reads / writes above precede the arrive
       mbar_arrive(&sm.p_full[j & 1]);
     }
     if (ok) ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, err));
@@ -370,11 +374,12 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       float o[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kColO + 32 * c, o[c]);
-      // the P tiles are free (every PV is done): they are the staging area
-      stage(r, o, m_run, l_run, sm.p[0]);
+      // the K stages are free (every S and PV is done, no copy is in
+      // flight): the first two are the staging area
+      stage(r, o, m_run, l_run, sm.k[0]);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
-    if (!*reinterpret_cast<volatile int*>(&sm.abort)) store(r, sm.p[0]);
+    if (!*reinterpret_cast<volatile int*>(&sm.abort)) store(r, sm.k[0]);
   }
 
   fence_before_sync();
