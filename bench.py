@@ -321,6 +321,7 @@ def run_sweep(args):
     from paged_kv_decode_varlen_gb300 import build as pa_build
     pa_build.build()
     from paged_kv_decode_varlen_gb300 import binding as B
+    B.pa_set_decode_ctas(args.decode_ctas)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     layers = args.layers
@@ -393,7 +394,7 @@ def run_sweep(args):
                     "l2": "not flushed (36 layers x distinct pools stream %.1f GB per step)" %
                           (sb["unique"] * layers / 1e9),
                     "graph": ("36 x pa_decode_step" if use_step else "36 x (kv_append + attention)")
-                    + " in one CUDA graph"}
+                    + " in one CUDA graph", "decode_ctas": args.decode_ctas or "automatic"}
             print(json.dumps(line), flush=True)
             del pools, graph
             torch.cuda.empty_cache()

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -199,18 +200,24 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
                 int page_offset, int num_kv_heads, int gcap, pa::DecodePlan& plan) {
   std::vector<int32_t> pages(n);
   int64_t total = 0;  // pages of one kv head's stream
+  int32_t longest = 0;
   for (int d = 0; d < n; ++d) {
     pages[d] = pages_of(seq_lens_host[rows[d]]) - page_offset;
     total += pages[d];
+    longest = std::max(longest, pages[d]);
   }
   if (total == 0) return 0;
+  // A row cut into m pieces costs its last CTA a merge of m partials, so
+  // when few rows leave CTAs to spare, segments get longer than
+  // kMinSegPages: a row of R pages costs about seg + c R / seg, least at
+  // seg ~ sqrt(R / 2) pages (measured: 8 for 128-page rows, 16 for 512).
+  const int64_t min_seg = std::max<int64_t>(kMinSegPages, std::llround(std::sqrt(longest / 2.0)));
   const int seg_cap = std::min(gcap / num_kv_heads, pa::kPlanMaxCtas);  // segments per stream
   if (seg_cap < 1) return -1;
   const int forced = g_forced_ctas.load();
   int64_t nseg = forced > 0 ? (forced + num_kv_heads - 1) / num_kv_heads
                             : std::min<int64_t>((int64_t)sm_count() * kDecodeCtasPerSm / num_kv_heads,
-                                                (total * num_kv_heads + kMinSegPages - 1) / kMinSegPages /
-                                                    num_kv_heads);
+                                                (total + min_seg - 1) / min_seg);
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, seg_cap));
   // a segment holds at most kDecodeMaxPagesPerCta pages; when that forces more
   // segments than one wave has slots, use whole waves so no wave runs part-empty
