@@ -192,7 +192,9 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t nu
  *   bf16 data; out is rounded to bf16.  The launch plan is made on the host
  *   from seq_lens_host / qo_indptr_host and travels in the kernel
  *   parameters, so a CUDA graph captured around this call replays the plan
- *   of the lengths it was captured with.
+ *   of the lengths it was captured with (for graphs replayed with new
+ *   lengths, decode-only batches use pa_decode_step, which plans on the
+ *   device).
  * q              [total_q, num_q_heads, head_dim] bf16, 16-byte aligned.
  * block_tables   [num_reqs, max_blocks_per_req] int32, device.  Entries past
  *                ceil(seq_len / 16) are never read.
