@@ -233,8 +233,8 @@ pa_status pa_attention_varlen(const void* q, const void* k_cache, const void* v_
  *
  * pa_decode_step -- the KV append and the attention of a decode-only batch
  * in one kernel launch whose launch shape depends only on the scalars
- * (num_reqs, num_kv_heads, max_seq_len), and which reads no array on the
- * host.  A launch captured in a CUDA graph is therefore valid for every
+ * (num_reqs, num_kv_heads, max_seq_len) and the device's SM count, and which
+ * reads no array on the host.  A launch captured in a CUDA graph is therefore valid for every
  * batch within those scalars: between replays the caller rewrites q, k_new,
  * v_new, block_tables and seq_lens in place.
  *   Row r (0 <= r < num_reqs) is one decode request with L = seq_lens[r]
@@ -281,7 +281,7 @@ pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, vo
 
 /*
  * pa_decode_step_workspace_size -- bytes of workspace pa_decode_step needs
- * for these scalars; 0 when no launch exists for them (num_reqs outside
+ * for these scalars on the current device; 0 when no launch exists for them (num_reqs outside
  * 0 .. 1024, max_seq_len outside 1 .. PA_MAX_SEQ_LEN, num_q_heads < 4, or
  * num_reqs x max_seq_len too large).
  */
