@@ -152,10 +152,11 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Launch `kernel` on `stream` with programmatic stream serialization.
+// Launch `kernel` on `stream`, with programmatic stream serialization when
+// `overlap` is set (else in plain stream order).
 template <class... Exp, class... Act>
-cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Act&&... args) {
+cudaError_t launch_maybe_pdl(bool overlap, void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Act&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -163,10 +164,17 @@ cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t sme
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
+// Launch `kernel` on `stream` with programmatic stream serialization.
+template <class... Exp, class... Act>
+cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Act&&... args) {
+  return launch_maybe_pdl(true, kernel, grid, block, smem, stream, static_cast<Act&&>(args)...);
 }
 
 // bf16 pair -> float2 (element 0 in .x)

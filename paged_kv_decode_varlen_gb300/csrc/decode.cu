@@ -968,7 +968,7 @@ bool g_decode_attr_set[3][64] = {};
 
 template <bool kQ8, bool kStep>
 cudaError_t launch_decode_as(const DecodeParams& p, const typename PlanOf<kStep>::type& plan, int grid,
-                             cudaStream_t stream) {
+                             bool overlap, cudaStream_t stream) {
   constexpr size_t kSmem = sizeof(DecodeSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
   constexpr int kVariant = kStep ? 2 : (kQ8 ? 1 : 0);
   int dev = 0;
@@ -979,17 +979,19 @@ cudaError_t launch_decode_as(const DecodeParams& p, const typename PlanOf<kStep>
     if (e != cudaSuccess) return e;
     g_decode_attr_set[kVariant][dev] = true;
   }
-  return launch_pdl(decode_kernel<kQ8, kStep>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
+  return launch_maybe_pdl(overlap, decode_kernel<kQ8, kStep>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, cudaStream_t stream) {
-  return q8 ? launch_decode_as<true, false>(p, plan, grid, stream) : launch_decode_as<false, false>(p, plan, grid, stream);
+cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
+                          cudaStream_t stream) {
+  return q8 ? launch_decode_as<true, false>(p, plan, grid, overlap, stream)
+            : launch_decode_as<false, false>(p, plan, grid, overlap, stream);
 }
 
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream) {
-  return launch_decode_as<false, true>(p, plan, grid, stream);
+  return launch_decode_as<false, true>(p, plan, grid, true, stream);
 }
 
 }  // namespace pa

@@ -189,7 +189,9 @@ pa_status set_error(pa_status s, const char* fmt, ...);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_kv_append_q8(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, cudaStream_t stream);
+// overlap: programmatic launch after the stream's previous kernel
+cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
+                          cudaStream_t stream);
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
                            cudaStream_t stream);

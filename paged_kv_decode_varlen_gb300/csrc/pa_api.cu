@@ -531,11 +531,15 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     // parameters); launches on one stream run in order and reuse the slots
     for (size_t d0 = 0; d0 < decode_rows.size(); d0 += pa::kPlanMaxRows) {
       const int n = (int)std::min(decode_rows.size() - d0, (size_t)pa::kPlanMaxRows);
+      // after the prefix pass or the prefill tiles, the decode CTAs go in
+      // plain stream order: resident early, waiting on the tile kernel's
+      // tail, they made the step 1-2 us longer, not shorter
+      const bool overlap = d0 > 0 || (P == 0 && tiles.empty());
       const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
                                    plan);
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
-      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, q8, stream); });
+      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, q8, overlap, stream); });
       if (s != PA_OK) return s;
     }
   }
