@@ -35,9 +35,12 @@
 //     last of the 4 warps issues that stage's next page at once, so the
 //     ring stays 8 pages deep and the TMA issue work is spread over warps.
 //   * Item end: the 16 token slots are merged (a transposed shuffle
-//     reduction inside each warp, then across the 4 warps through an 8 KiB
-//     per-CTA scratch in the workspace, which stays in L2; shared memory is
-//     all ring).  An item that lies inside one segment is written out at once;
+//     reduction inside each warp, then across the 4 warps through 4 KiB of
+//     shared memory, two heads per round: three CTAs per SM leave no room
+//     for all four at once).  With bf16 pages and the host plan the next
+//     item's q is bulk-copied into shared memory at the item end, so the
+//     next item starts without a global-memory round trip.  An item that
+//     lies inside one segment is written out at once;
 //     an item cut by segment boundaries leaves one partial per CTA in the
 //     workspace, and the last of those CTAs to finish (a counter it resets)
 //     merges them into out / lse.
@@ -76,7 +79,12 @@ template <int kSlab>
 struct __align__(128) DecodeSmem {
   uint8_t k[kStages][kSlab];
   uint8_t v[kStages][kSlab];
+  uint16_t qs[kGroup * kHeadDim];        // the current item's q (bulk copy)
+  float mrg_o[kWarps][2][kHeadDim];      // cross-warp merge: two heads per round
+  float mrg_m[kWarps][2], mrg_l[kWarps][2];
   uint64_t full[kStages];   // TMA landed
+  uint64_t q_full;          // q landed
+  int q_issued;             // q copies issued
   int readers[kStages];     // warps done reading the stage's current page
   int32_t ids[kDecodeMaxPagesPerCta];
   Item items[kDecodeMaxItemsPerCta];
@@ -92,8 +100,11 @@ struct __align__(128) DecodeSmem {
 };
 
 static_assert(offsetof(DecodeSmem<kSlabBytes>, k) % 128 == 0 && offsetof(DecodeSmem<kSlabBytes>, v) % 128 == 0 &&
-                  offsetof(DecodeSmem<kQ8SlabBytes>, v) % 16 == 0,
+                  offsetof(DecodeSmem<kQ8SlabBytes>, v) % 16 == 0 && offsetof(DecodeSmem<kSlabBytes>, qs) % 16 == 0 &&
+                  offsetof(DecodeSmem<kQ8SlabBytes>, qs) % 16 == 0,
               "bulk copies land on 16-byte boundaries");
+// three CTAs per SM: 228 KiB of shared memory per SM, 1 KiB of it reserved per CTA
+static_assert(3 * (sizeof(DecodeSmem<kSlabBytes>) + 1024) <= 228 * 1024, "three decode CTAs per SM");
 
 // 8 packed bf16 pairs (two 16-byte loads) -> 8 float2
 __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float2* f) {
@@ -415,10 +426,16 @@ __global__ void __launch_bounds__(kThreads, 3)
   constexpr int kAlpha = kStep ? kStepItemCost : 0;
   constexpr int kSlab = kQ8 ? kQ8SlabBytes : kSlabBytes;
   using Smem = DecodeSmem<kSlab>;
+  // q of each item by a bulk copy into shared memory, issued an item ahead
+  // (bf16 pages, host plan), else read from global memory at the item's
+  // start: measured, the copy shortens the first and lengthens the others
+  constexpr bool kQSmem = !kQ8 && !kStep;
   // No early launch of the next kernel: this grid is one wave sized to fill
   // every SM, and CTAs of a dependent kernel arriving early would take slots
-  // its own CTAs need.  The next kernel is released as the CTAs exit.
-  pdl_wait();
+  // its own CTAs need.  The next kernel is released as the CTAs exit.  The
+  // host plan's item table comes from the kernel parameters alone, so it is
+  // built before the wait for the previous kernel (which may still run).
+  if constexpr (kStep) pdl_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int b = blockIdx.x;
@@ -433,6 +450,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         sm.readers[s] = 0;
         sm.stage_page[s] = -1;
       }
+      mbar_init(&sm.q_full, 1);
+      sm.q_issued = 0;
       sm.abort_flag = 0;
       fence_mbar_init();
     }
@@ -448,6 +467,8 @@ __global__ void __launch_bounds__(kThreads, 3)
         sm.readers[s] = 0;
         sm.stage_page[s] = -1;
       }
+      mbar_init(&sm.q_full, 1);
+      sm.q_issued = 0;
       sm.abort_flag = 0;
       fence_mbar_init();
     }
@@ -503,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     }
     __syncthreads();
+    pdl_wait();
   }
   int n_cov = 0;
   const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_cache);
@@ -515,6 +537,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     bulk_g2s(sm.k[s], kbase + off, kSlab, &sm.full[s]);
     bulk_g2s(sm.v[s], vbase + off, kSlab, &sm.full[s]);
     sm.stage_page[s] = i;  // one issuer per stage at a time
+  };
+  // q of item k of the window (4 heads x 256 B) -> sm.qs
+  auto issue_q = [&](int k) {
+    const size_t qoff = ((size_t)sm.items[k].tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
+    mbar_arrive_expect_tx(&sm.q_full, kGroup * kHeadDim * 2);
+    bulk_g2s(sm.qs, p.q + qoff, kGroup * kHeadDim * 2, &sm.q_full);
+    sm.q_issued += 1;
   };
   // a warp is done with page i: the last of the 4 warps refills its stage
   // with page i + kStages
@@ -602,6 +631,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (tid == 0) {
     // a later window refills stages the warps have read (generic proxy)
     if (kStep && q_lo > 0) fence_proxy_async_smem();
+    if constexpr (kQSmem) issue_q(0);
     const int n0 = min(n_cov, q_lo + kStages);
     for (int i = q_lo; i < n0; ++i) issue(i);
   }
@@ -619,8 +649,14 @@ __global__ void __launch_bounds__(kThreads, 3)
     // pages as dim pairs per head (see qk16), for q8_0 pages as head pairs
     // per dim (see qk16_q8)
     float2 qp[2][16];
+    if (kQSmem && !mbar_wait_bounded(&sm.q_full, (uint32_t)k & 1u)) {
+      // the page loop's first abort check ends the item
+      record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+      *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+    }
     {
-      const uint16_t* qrow = p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
+      const uint16_t* qrow =
+          kQSmem ? sm.qs : p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
 #pragma unroll
       for (int hp = 0; hp < 2; ++hp) {
         float f0[16], f1[16];
@@ -771,28 +807,36 @@ __global__ void __launch_bounds__(kThreads, 3)
       aborted = true;
       break;
     }
-    float* scr = p.scratch + (size_t)b * kScratchFloats;  // this CTA's merge scratch (L2)
-    float* scr_m = scr + kWarps * kGroup * kHeadDim;
-    float* scr_l = scr_m + kWarps * kGroup;
+    // every warp has read the item's q: the next item's q can land
+    if (kQSmem && tid == 0 && k + 1 < n_items) {
+      fence_proxy_async_smem();
+      issue_q(k + 1);
+    }
+    // merge across the 4 warps in two rounds of two heads (shared memory);
+    // warp g ends with head g
+    const int g = warp;
+    const int d0 = lane * 4;
+    float M = -INFINITY, Ls = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     {
       const float l_pair = l_own + __shfl_xor_sync(0xffffffffu, l_own, 1);
       float mh[kGroup], lh[kGroup], Mw[kGroup], Lw[kGroup];
 #pragma unroll
-      for (int g = 0; g < kGroup; ++g) {
-        const int src = slot_base + (g >> 1) * 4 + (g & 1) * 2;
-        mh[g] = __shfl_sync(0xffffffffu, m_own, src);
-        lh[g] = __shfl_sync(0xffffffffu, l_pair, src);
-        float M = fmaxf(mh[g], __shfl_xor_sync(0xffffffffu, mh[g], 8));
-        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
-        Mw[g] = M;
-        const float f = (mh[g] == -INFINITY) ? 0.f : fast_exp2(mh[g] - M);
+      for (int gg = 0; gg < kGroup; ++gg) {
+        const int src = slot_base + (gg >> 1) * 4 + (gg & 1) * 2;
+        mh[gg] = __shfl_sync(0xffffffffu, m_own, src);
+        lh[gg] = __shfl_sync(0xffffffffu, l_pair, src);
+        float Mg = fmaxf(mh[gg], __shfl_xor_sync(0xffffffffu, mh[gg], 8));
+        Mg = fmaxf(Mg, __shfl_xor_sync(0xffffffffu, Mg, 16));
+        Mw[gg] = Mg;
+        const float f = (mh[gg] == -INFINITY) ? 0.f : fast_exp2(mh[gg] - Mg);
         const float2 f2 = make_float2(f, f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[g][j] = __fmul2_rn(acc[g][j], f2);
-        float lsum = lh[g] * f;
+        for (int j = 0; j < 8; ++j) acc[gg][j] = __fmul2_rn(acc[gg][j], f2);
+        float lsum = lh[gg] * f;
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-        Lw[g] = lsum;
+        Lw[gg] = lsum;
       }
       // sum over the warp's 4 token slots, transposed: the slot with bits
       // (s1, s0) ends with head 2 s1 + s0
@@ -805,48 +849,49 @@ __global__ void __launch_bounds__(kThreads, 3)
         h0[j] = __fadd2_rn(keep0, shfl_xor2(send0, 16));
         h1[j] = __fadd2_rn(keep1, shfl_xor2(send1, 16));
       }
-      const int h = (s1 ? 2 : 0) + (s0 ? 1 : 0);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {  // xor 8: keep head 2 s1 + s0
         const float2 keep = s0 ? h1[j] : h0[j], send = s0 ? h0[j] : h1[j];
         h0[j] = __fadd2_rn(keep, shfl_xor2(send, 8));
       }
-      float* dst = scr + (warp * kGroup + h) * kHeadDim;
-      *reinterpret_cast<float4*>(dst + 8 * c) = make_float4(h0[0].x, h0[0].y, h0[1].x, h0[1].y);
-      *reinterpret_cast<float4*>(dst + 8 * c + 4) = make_float4(h0[2].x, h0[2].y, h0[3].x, h0[3].y);
-      *reinterpret_cast<float4*>(dst + 64 + 8 * c) = make_float4(h0[4].x, h0[4].y, h0[5].x, h0[5].y);
-      *reinterpret_cast<float4*>(dst + 64 + 8 * c + 4) = make_float4(h0[6].x, h0[6].y, h0[7].x, h0[7].y);
-      if (lane == 0) {
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-          scr_m[warp * kGroup + g] = Mw[g];
-          scr_l[warp * kGroup + g] = Lw[g];
+      for (int rnd = 0; rnd < 2; ++rnd) {  // heads 2 rnd and 2 rnd + 1
+        if (rnd) bar_all();                // round 0's reads are done
+        if ((int)s1 == rnd) {
+          float* dst = sm.mrg_o[warp][s0 ? 1 : 0];
+          *reinterpret_cast<float4*>(dst + 8 * c) = make_float4(h0[0].x, h0[0].y, h0[1].x, h0[1].y);
+          *reinterpret_cast<float4*>(dst + 8 * c + 4) = make_float4(h0[2].x, h0[2].y, h0[3].x, h0[3].y);
+          *reinterpret_cast<float4*>(dst + 64 + 8 * c) = make_float4(h0[4].x, h0[4].y, h0[5].x, h0[5].y);
+          *reinterpret_cast<float4*>(dst + 64 + 8 * c + 4) = make_float4(h0[6].x, h0[6].y, h0[7].x, h0[7].y);
         }
-      }
-    }
-    bar_all();  // makes the scratch writes of all warps visible to the block (plain loads below)
-    // warp g merges head g across the 4 warps; lane owns dims [4 lane, +4)
-    const int g = warp;
-    const int d0 = lane * 4;
-    float mwv[kWarps];
-    float M = -INFINITY;
+        if (lane == 0) {
+          sm.mrg_m[warp][0] = Mw[2 * rnd];
+          sm.mrg_m[warp][1] = Mw[2 * rnd + 1];
+          sm.mrg_l[warp][0] = Lw[2 * rnd];
+          sm.mrg_l[warp][1] = Lw[2 * rnd + 1];
+        }
+        bar_all();
+        if ((g >> 1) == rnd) {  // head g: lane owns dims [4 lane, +4)
+          const int j = g & 1;
+          float mwv[kWarps];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      mwv[w] = scr_m[w * kGroup + g];
-      M = fmaxf(M, mwv[w]);
-    }
-    float Ls = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
+          for (int w = 0; w < kWarps; ++w) {
+            mwv[w] = sm.mrg_m[w][j];
+            M = fmaxf(M, mwv[w]);
+          }
+          if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = (mwv[w] == -INFINITY) ? 0.f : fast_exp2(mwv[w] - M);
-        const float4 x = *reinterpret_cast<const float4*>(scr + (w * kGroup + g) * kHeadDim + d0);
-        Ls += scr_l[w * kGroup + g] * f;
-        o.x = fmaf(f, x.x, o.x);
-        o.y = fmaf(f, x.y, o.y);
-        o.z = fmaf(f, x.z, o.z);
-        o.w = fmaf(f, x.w, o.w);
+            for (int w = 0; w < kWarps; ++w) {
+              const float f = (mwv[w] == -INFINITY) ? 0.f : fast_exp2(mwv[w] - M);
+              const float4 x = *reinterpret_cast<const float4*>(&sm.mrg_o[w][j][d0]);
+              Ls += sm.mrg_l[w][j] * f;
+              o.x = fmaf(f, x.x, o.x);
+              o.y = fmaf(f, x.y, o.y);
+              o.z = fmaf(f, x.z, o.z);
+              o.w = fmaf(f, x.w, o.w);
+            }
+          }
+        }
       }
     }
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
@@ -865,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       packed.y = pack_bf16x2(o.z, o.w);
       *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + d0) = packed;
       if (p.lse && lane == 0) p.lse[orow] = lse2 * kLn2;
-      bar_all();  // the merge scratch is free again
+      bar_all();  // warps leave the item together (measured faster than without)
       continue;
     }
     // the item is cut by segment boundaries: publish this CTA's partial
@@ -943,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + d0) = packed;
       if (p.lse && lane == 0) p.lse[orow] = l2 * kLn2;
     }
-    bar_all();  // the merge scratch and is_last are free again
+    bar_all();  // is_last is free again
   }
   if (aborted || !kStep) break;
   // next window: every item of this one is done (the barrier at its end)
@@ -961,6 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       const int j = *reinterpret_cast<volatile int*>(&sm.stage_page[s]);
       if (j >= 0 && !mbar_wait_bounded(&sm.full[s], (uint32_t)(j / kStages) & 1u)) break;
     }
+    if (sm.q_issued > 0) mbar_wait_bounded(&sm.q_full, (uint32_t)(sm.q_issued - 1) & 1u);
   }
 }
 

@@ -94,7 +94,6 @@ struct DecodeParams {
   float* piece_o;        // fp32 [2 * grid, 4, D]: a CTA's partial of its first / last item
   float* piece_lse;      // fp32 [2 * grid, 4], log2 domain
   int* counters;         // [num_reqs, Hkv] CTAs finished per item; zero between calls
-  float* scratch;        // [grid, kScratchFloats]: per-CTA merge scratch
   int* err;
   // decode step only: the new token of every row ([rows, Hkv, D] bf16) and
   // the pools it is appended to (the same memory as k_cache / v_cache)
@@ -103,8 +102,6 @@ struct DecodeParams {
   uint16_t* k_store;
   uint16_t* v_store;
 };
-// per-CTA merge scratch: 4 warps x 4 heads x D sums, then 4 x 4 max and sum
-constexpr int kScratchFloats = 4 * 4 * 128 + 2 * 4 * 4;
 
 // Tiled TMA maps of the tensor-core tile kernels (host-encoded, passed by
 // value): q as [total_q][Hq][D] with 64 x 4 x 32 boxes, the K and V pools as

@@ -120,10 +120,9 @@ int grid_cap(int32_t num_reqs, int32_t num_kv_heads, int32_t max_seq_len) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: [error word | item counters (num_reqs x Hkv int32) |
-// partial o (2 x grid_cap x 4 heads x D fp32) | partial lse (fp32) |
-// per-CTA merge scratch (grid_cap x kScratchFloats fp32)].
+// partial o (2 x grid_cap x 4 heads x D fp32) | partial lse (fp32)].
 struct WorkspaceLayout {
-  size_t counters, piece_o, piece_lse, scratch, total;
+  size_t counters, piece_o, piece_lse, total;
 };
 
 WorkspaceLayout layout_for_grid(int32_t num_reqs, int32_t hkv, int32_t head_dim, int grid) {
@@ -132,8 +131,7 @@ WorkspaceLayout layout_for_grid(int32_t num_reqs, int32_t hkv, int32_t head_dim,
   w.counters = PA_ERROR_WORD_BYTES;
   w.piece_o = w.counters + align256((size_t)std::max(num_reqs, 0) * (size_t)hkv * 4);
   w.piece_lse = w.piece_o + align256(slots * (size_t)std::max(head_dim, 0) * 4);
-  w.scratch = w.piece_lse + align256(slots * 4);
-  w.total = w.scratch + align256((size_t)grid * pa::kScratchFloats * 4);
+  w.total = w.piece_lse + align256(slots * 4);
   return w;
 }
 
@@ -523,7 +521,6 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
     dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
     dp.counters = reinterpret_cast<int*>(ws + wl.counters);
-    dp.scratch = reinterpret_cast<float*>(ws + wl.scratch);
     dp.err = err;
     static thread_local pa::DecodePlan plan;
     const int gcap = grid_cap(num_reqs, num_kv_heads, max_len);
@@ -745,7 +742,6 @@ pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, vo
   dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
   dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
   dp.counters = reinterpret_cast<int*>(ws + wl.counters);
-  dp.scratch = reinterpret_cast<float*>(ws + wl.scratch);
   dp.err = reinterpret_cast<int*>(ws);
   dp.k_new = static_cast<const uint16_t*>(k_new);
   dp.v_new = static_cast<const uint16_t*>(v_new);

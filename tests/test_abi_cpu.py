@@ -36,11 +36,9 @@ def test_workspace_size_query():
     assert small >= b.PA_ERROR_WORD_BYTES and big >= small and big % 256 == 0 and small % 256 == 0
     # error word + counters (num_reqs x 8 int32) + two partial slots of 4 heads x 129 fp32 per CTA
     # for a 480-CTA bound
-    # plus an 8320-byte merge scratch per CTA, for a 480-CTA bound
     slots = 2 * 480 * 4
-    scratch = 480 * 8320
-    assert b.pa_attention_workspace_size(1, 1, 32, 128, 16) == 256 + 256 + slots * 512 + 15360 + scratch
-    assert b.pa_attention_workspace_size(100, 100, 32, 128, 16) == 256 + 3328 + slots * 512 + 15360 + scratch
+    assert b.pa_attention_workspace_size(1, 1, 32, 128, 16) == 256 + 256 + slots * 512 + 15360
+    assert b.pa_attention_workspace_size(100, 100, 32, 128, 16) == 256 + 3328 + slots * 512 + 15360
     # very long rows raise the grid bound (1024 pages per CTA at most)
     assert b.pa_attention_workspace_size(1024, 1024, 32, 128, 1 << 20) > big
 

@@ -45,10 +45,12 @@ def test_noalloc_matches_workspace_call_twice_in_a_row():
 
 
 def test_noalloc_rejects_a_batch_beyond_its_scratch():
-    # host metadata describing rows far longer than the fixed scratch can plan
-    # for; the call is refused on the host before anything is launched
-    n = 1024
-    seq = torch.full((n,), 1 << 20, dtype=torch.int32)
+    # more rows than the fixed scratch has room for (229,376 rows x 8 kv
+    # heads x 4-byte counters is 7 MiB, plus the split partials); the call
+    # is refused on the host before anything is launched
+    n = 229376
+    assert B.pa_attention_workspace_size(n, n, 32, 128, 16) > (8 << 20)
+    seq = torch.full((n,), 16, dtype=torch.int32)
     ind = torch.arange(n + 1, dtype=torch.int32)
     q = torch.zeros((n, 32, 128), dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros((4, 8, 16, 128), dtype=torch.bfloat16, device="cuda")
