@@ -107,6 +107,22 @@ def test_forced_decode_grid(ctas):
     compare(out, ref, lse, ref_lse, what=f"ctas={ctas}")
 
 
+@pytest.mark.parametrize("ctas", [8, 16])
+def test_many_rows_per_cta(ctas):
+    """64 short rows on one or two segments per kv head: a CTA walks up to
+    64 rows, each with its q staged in shared memory while the previous row
+    ends (the longest chain of the per-row q copies), next to rows cut
+    between the two segments."""
+    seq = [int(x) for x in np.random.default_rng(41).integers(1, 200, 64)]
+    need = sum(-(-L // 16) for L in seq)
+    b = W.make_batch(seq, [1] * 64, num_blocks=need + 5, seed=40 + ctas)
+    d = DevBatch(b)
+    B.pa_set_decode_ctas(ctas)
+    out, lse = run_step(d)
+    ref, ref_lse, _, _ = oracle_step(b)
+    compare(out, ref, lse, ref_lse, what=f"64 rows on ctas={ctas}")
+
+
 def test_workspace_reused_across_grid_sizes():
     """The item counters in the workspace return to zero after every call,
     so one workspace serves consecutive calls with different grid sizes."""
