@@ -123,6 +123,20 @@ def test_many_rows_per_cta(ctas):
     compare(out, ref, lse, ref_lse, what=f"64 rows on ctas={ctas}")
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.0883883])
+def test_nonpositive_sm_scale(scale):
+    """sm_scale may be any finite value: zero weighs every key alike and a
+    negative scale turns the softmax around.  Decode rows (cut between CTAs)
+    and chunked-prefill rows (tensor-core tiles) both follow the oracle."""
+    seq, qo = [1500, 300, 2000, 77], [1, 40, 1, 9]
+    need = sum(-(-L // 16) for L in seq)
+    b = W.make_batch(seq, qo, num_blocks=need + 5, seed=51, sm_scale=scale)
+    d = DevBatch(b)
+    out, lse = run_step(d)
+    ref, ref_lse, _, _ = oracle_step(b)
+    compare(out, ref, lse, ref_lse, what=f"sm_scale={scale}")
+
+
 def test_workspace_reused_across_grid_sizes():
     """The item counters in the workspace return to zero after every call,
     so one workspace serves consecutive calls with different grid sizes."""
