@@ -2,16 +2,14 @@
 // allocate device memory.
 //
 // pa_attention_varlen needs a caller-provided workspace (the error word, the
-// per-(request, kv head) counters of the persistent decode kernel, the
-// partial results of key ranges cut between CTAs and the per-CTA merge
-// scratch).  Some callers cannot obtain one: code that runs where
-// cudaMalloc is forbidden or unsafe (inside a stream being captured into a
-// graph, in a real-time loop that must not touch the allocator, in a host
-// framework whose device memory is fully handed out to its own pool), or a
-// plugin that is only given input and output pointers.  This entry point
-// serves them with a fixed scratch array that lives in the library's own
-// device memory for as long as the library is loaded, on every GPU that
-// loads it; it allocates nothing per call.
+// per-(request, kv head) counters of the persistent decode kernel and the
+// partial results of key ranges cut between CTAs).  Some callers cannot
+// obtain one: a real-time serving loop that must not touch the allocator
+// between steps, a host framework whose device memory is all handed out to
+// its own pool, or a plugin that is given only its input and output
+// pointers.  This entry point serves them with a fixed scratch array that
+// lives in the library's own device memory for as long as the library is
+// loaded, on every GPU that loads it; it allocates nothing per call.
 //
 // The array is shared by every call on a device: calls on that device must
 // not overlap on the GPU (they would race on the counters and partials);
@@ -57,8 +55,9 @@ extern "C" pa_status pa_attention_varlen_noalloc(
     const int32_t* qo_indptr_host, int32_t num_reqs, int32_t total_q, int32_t num_q_heads, int32_t num_kv_heads,
     int32_t head_dim, int32_t block_size, float sm_scale, void* out, float* lse, int32_t* device_error,
     pa_stream_t stream) {
-  if (!seq_lens_host || !qo_indptr_host || num_reqs < 0)
-    return pa::set_error(PA_ERR_INVALID_ARG, "noalloc: host metadata pointers and num_reqs >= 0 are required");
+  // the same bound as pa_attention_varlen, checked before seq_lens_host is read
+  if (!seq_lens_host || !qo_indptr_host || num_reqs < 0 || num_reqs > 65535)
+    return pa::set_error(PA_ERR_INVALID_ARG, "noalloc: host metadata pointers and num_reqs in [0, 65535] are required");
   int32_t max_len = 1;
   for (int r = 0; r < num_reqs; ++r) max_len = seq_lens_host[r] > max_len ? seq_lens_host[r] : max_len;
   const size_t need = pa_attention_workspace_size(num_reqs, total_q, num_q_heads, head_dim, max_len);
