@@ -23,8 +23,10 @@
  *     inside a page, so one head's page is contiguous).
  *
  * Conventions shared by every call:
- *   - All tensors are device memory owned by the caller.  The library never
- *     allocates device memory; scratch space is the caller's `workspace`.
+ *   - All tensors are device memory owned by the caller.  No call allocates
+ *     device memory: scratch space is the caller's `workspace`, except for
+ *     pa_attention_varlen_noalloc, whose scratch is one fixed array that the
+ *     library holds in each device's memory while it is loaded.
  *   - All launches are asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  A call that returns PA_OK has only enqueued
  *     work.
@@ -81,7 +83,12 @@ const char* pa_status_string(int32_t status);
 const char* pa_last_error_message(void);
 
 /*
- * pa_kv_append -- write this step's new keys and values into their slots.
+ * pa_kv_append -- write this step's new keys and values into their slots
+ * ("Inference optimisation", AI-infra book ch. 8, §8.1.1: the keys and values
+ * of every layer are kept for later tokens; §8.3.1 and Fig. 8-10: a token's
+ * slot is a (physical block, offset) pair, and a sequence that grows takes a
+ * new block from the free pool; "vLLM, SGLang and continuous batching",
+ * section "PagedAttention": 16-token blocks).
  *   For new token i with slot = slot_mapping[i] >= 0, block = slot / 16 and
  *   offset = slot % 16, and every kv head h:
  *     k_cache[block, h, offset, :] = k_new[i, h, :]   (v likewise)
@@ -174,7 +181,13 @@ size_t pa_attention_workspace_size(int32_t num_reqs, int32_t total_q, int32_t nu
 
 /*
  * pa_attention_varlen -- causal GQA softmax attention over a paged KV cache
- * for a varlen batch.
+ * for a varlen batch ("Inference optimisation", AI-infra book ch. 8: §8.1.1,
+ * decode attends each new token to the whole cached context; §8.2.3, the
+ * N_pair equation and Fig. 8-8/8-9, a chunk of c tokens after h cached ones,
+ * token j seeing h + j + 1 keys; §8.3.1 and Fig. 8-10, keys found through the
+ * block table; "Continuous batching architecture", iteration-level batches
+ * mixing decode rows and prefill chunks; "Disaggregated prefill and decode",
+ * per-request qo_len / kv_len).
  *   Request r has qo_len = qo_indptr[r+1] - qo_indptr[r] query tokens, rows
  *   qo_indptr[r] .. qo_indptr[r+1]-1 of q, and seq_len = seq_lens[r] keys
  *   (the KV length after this step's append, so 0 <= qo_len <= seq_len).
@@ -346,10 +359,10 @@ pa_status pa_attention_varlen_shared_prefix(
 /*
  * pa_attention_varlen_noalloc -- pa_attention_varlen for callers that cannot
  * allocate device memory.  The pages describe no counterpart of this call;
- * it exists for callers that cannot obtain a workspace: code running where
- * cudaMalloc is not allowed or not wanted (inside stream capture, in a
- * real-time loop, under a host framework that owns all device memory), or a
- * plugin that is handed only its input and output pointers.
+ * it exists for callers that cannot obtain a workspace: a real-time serving
+ * loop that must not enter the allocator between steps, a host framework
+ * whose device memory is all handed out to its own pool, or a plugin that is
+ * handed only its input and output pointers.
  *   Same computation, arguments and results as pa_attention_varlen, except
  *   that there is no workspace argument: the scratch is a fixed array of
  *   PA_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, present on every
@@ -358,10 +371,14 @@ pa_status pa_attention_varlen_shared_prefix(
  *   PA_ERR_UNSUPPORTED (and a message in pa_last_error_message()).
  *   No device memory is allocated or freed by this call.
  * device_error   nullable device int32; if given, receives the call's device
- *                error word (PA_OK or PA_ERR_DEVICE_*) on `stream`.
+ *                error word (PA_OK or PA_ERR_DEVICE_*) on `stream`.  With
+ *                NULL the device error word of the call is not reported
+ *                anywhere (the next call clears it).
+ * num_reqs       0 .. 65535 as for pa_attention_varlen (PA_ERR_INVALID_ARG
+ *                outside, checked before seq_lens_host is read).
  * Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before capturing `stream` into a graph.
+ *   first call before any stream capture.
  * Sharing: every call on a device uses the same array and leaves its contents
  *   there; each call clears its error word and counters on `stream` first.
  *   Calls that overlap on the GPU race on the array, so issue them in order
@@ -378,7 +395,10 @@ pa_status pa_attention_varlen_noalloc(const void* q, const void* k_cache, const 
 
 /*
  * pa_merge_lse -- combine two partial attentions of the same queries over
- * disjoint key sets A and B (log-sum-exp identity):
+ * disjoint key sets A and B.  The pages do not define this operation; it is
+ * part of this library's interface so that a caller can split one request's
+ * keys (across calls or devices) and combine the results.  It is the
+ * log-sum-exp identity of softmax over a union of key sets:
  *   M = max(lse_a, lse_b), w_a = exp(lse_a - M), w_b = exp(lse_b - M)
  *   o = (w_a o_a + w_b o_b) / (w_a + w_b),  lse = M + ln(w_a + w_b)
  *   A part with lse = -inf has weight 0 (its o is ignored); if both are
@@ -430,6 +450,22 @@ typedef enum {
 } pa_kernel_kind;
 
 pa_status pa_set_decode_ctas(int32_t n);
+/*
+ * pa_set_decode_fault_injection(on) -- a test of the bounded-wait path, off
+ * (0) by default, process-wide.  With on = 1, decode launches of
+ * pa_attention_varlen and pa_attention_varlen_shared_prefix over bf16 pages
+ * use a diagnostic build of the decode kernel in which CTA 0 arms the
+ * barrier of its second page without issuing that page's copies, and every
+ * wait gives up after 1 ms instead of 2 s.  Nothing faults or hangs: the
+ * waiting warps give up, record PA_ERR_DEVICE_TIMEOUT in the error word, let
+ * the copies they did issue land and return; the other CTAs finish
+ * normally.  What such a call leaves: the error word set; the outputs of
+ * the rows whose keys CTA 0 holds undefined; for rows cut between CTAs, their
+ * counters in the workspace non-zero -- zero the workspace before its next
+ * use, as after any PA_ERR_DEVICE_* error.  on outside {0, 1} gives
+ * PA_ERR_INVALID_ARG.
+ */
+pa_status pa_set_decode_fault_injection(int32_t on);
 int64_t pa_launch_count(void);
 pa_status pa_trace_enable(int32_t on);
 pa_status pa_trace_read(int32_t* kinds, float* ms, int32_t capacity, int32_t* count);

@@ -69,6 +69,7 @@ _SIGS = {
     "pa_get_device_error": (_i32, [_P, ctypes.POINTER(_i32)]),
     "pa_clear_device_error": (_i32, [_P, _P]),
     "pa_set_decode_ctas": (_i32, [_i32]),
+    "pa_set_decode_fault_injection": (_i32, [_i32]),
     "pa_launch_count": (_i64, []),
     "pa_trace_enable": (_i32, [_i32]),
     "pa_trace_read": (_i32, [ctypes.POINTER(_i32), ctypes.POINTER(_f32), _i32, ctypes.POINTER(_i32)]),
@@ -438,6 +439,13 @@ def pa_clear_device_error(workspace, stream=None):
 
 def pa_set_decode_ctas(n: int):
     _check(_lib.pa_set_decode_ctas(int(n)))
+
+
+def pa_set_decode_fault_injection(on: bool):
+    """Test switch of the bounded-wait path (see include/pa.h): with on, the
+    decode kernel's CTA 0 lets one wait run out (1 ms) and the call records
+    PA_ERR_DEVICE_TIMEOUT."""
+    _check(_lib.pa_set_decode_fault_injection(1 if on else 0))
 
 
 def pa_launch_count() -> int:

@@ -69,14 +69,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after
-// kWaitLimitNs.  Returns false on timeout (the caller records it).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete, giving up after limit_ns
+// (kWaitLimitNs unless a diagnostic kernel shortens it).  Returns false on
+// timeout (the caller records it).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((it & 63u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
 }
 

@@ -417,10 +417,17 @@ __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& s
   __syncthreads();
 }
 
-template <bool kQ8, bool kStep>
+// kDiag: the diagnostic instantiation that tests the timeout path (bf16
+// pages, host plan).  CTA 0 arms the barrier of its segment's second page
+// without issuing that page's copies, so the wait on it runs out; every wait
+// of this instantiation gives up after 1 ms instead of kWaitLimitNs.  No
+// copy is dropped anywhere else, and nothing is read out of bounds.
+template <bool kQ8, bool kStep, bool kDiag = false>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_kernel(const DecodeParams p, const __grid_constant__ typename PlanOf<kStep>::type plan) {
   static_assert(!(kQ8 && kStep), "the decode step serves bf16 pages");
+  static_assert(!(kDiag && (kQ8 || kStep)), "the diagnostic instantiation is the bf16 host-plan kernel");
+  constexpr unsigned long long kLimit = kDiag ? 1000000ull : kWaitLimitNs;
   // the fixed cost of a row in the stream's units (the host plan cuts in
   // pages, with no fixed cost)
   constexpr int kAlpha = kStep ? kStepItemCost : 0;
@@ -534,8 +541,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int s = i & (kStages - 1);
     const size_t off = ((size_t)max(sm.ids[i], 0) * Hkv + kvh) * kSlab;
     mbar_arrive_expect_tx(&sm.full[s], 2 * kSlab);
-    bulk_g2s(sm.k[s], kbase + off, kSlab, &sm.full[s]);
-    bulk_g2s(sm.v[s], vbase + off, kSlab, &sm.full[s]);
+    if (!(kDiag && b == 0 && i == 1)) {  // (diagnostic: CTA 0's page 1 is armed, never copied)
+      bulk_g2s(sm.k[s], kbase + off, kSlab, &sm.full[s]);
+      bulk_g2s(sm.v[s], vbase + off, kSlab, &sm.full[s]);
+    }
     sm.stage_page[s] = i;  // one issuer per stage at a time
   };
   // q of item k of the window (4 heads x 256 B) -> sm.qs
@@ -649,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     // pages as dim pairs per head (see qk16), for q8_0 pages as head pairs
     // per dim (see qk16_q8)
     float2 qp[2][16];
-    if (kQSmem && !mbar_wait_bounded(&sm.q_full, (uint32_t)k & 1u)) {
+    if (kQSmem && !mbar_wait_bounded(&sm.q_full, (uint32_t)k & 1u, kLimit)) {
       // the page loop's first abort check ends the item
       record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
       *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
@@ -690,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       const bool has1 = qb < qend;
       const int sa = qa & (kStages - 1), sb = qb & (kStages - 1);
       const uint32_t pa = (uint32_t)(qa / kStages) & 1u, pb = (uint32_t)(qb / kStages) & 1u;
-      if (!mbar_wait_bounded(&sm.full[sa], pa) || (has1 && !mbar_wait_bounded(&sm.full[sb], pb))) {
+      if (!mbar_wait_bounded(&sm.full[sa], pa, kLimit) || (has1 && !mbar_wait_bounded(&sm.full[sb], pb, kLimit))) {
         record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
         *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
         aborted = true;
@@ -1001,39 +1010,38 @@ __global__ void __launch_bounds__(kThreads, 3)
   __syncthreads();  // every thread has left the item loop
   if (*reinterpret_cast<volatile int*>(&sm.abort_flag) && tid == 0) {
     // A wait gave up: let the last copy issued into each stage land
-    // (bounded), then leave.
+    // (bounded), then leave.  A stage whose copies never land is passed
+    // over after the bound, and the others are still waited for, so no
+    // copy that can land is still in flight when the CTA leaves.
     for (int s = 0; s < kStages; ++s) {
       const int j = *reinterpret_cast<volatile int*>(&sm.stage_page[s]);
-      if (j >= 0 && !mbar_wait_bounded(&sm.full[s], (uint32_t)(j / kStages) & 1u)) break;
+      if (j >= 0) mbar_wait_bounded(&sm.full[s], (uint32_t)(j / kStages) & 1u, kLimit);
     }
-    if (sm.q_issued > 0) mbar_wait_bounded(&sm.q_full, (uint32_t)(sm.q_issued - 1) & 1u);
+    if (sm.q_issued > 0) mbar_wait_bounded(&sm.q_full, (uint32_t)(sm.q_issued - 1) & 1u, kLimit);
   }
 }
 
-bool g_decode_attr_set[3][64] = {};
+std::atomic<bool> g_decode_attr_set[4][kMaxDevices];
 
-template <bool kQ8, bool kStep>
+template <bool kQ8, bool kStep, bool kDiag = false>
 cudaError_t launch_decode_as(const DecodeParams& p, const typename PlanOf<kStep>::type& plan, int grid,
                              bool overlap, cudaStream_t stream) {
   constexpr size_t kSmem = sizeof(DecodeSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
-  constexpr int kVariant = kStep ? 2 : (kQ8 ? 1 : 0);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  constexpr int kVariant = kDiag ? 3 : kStep ? 2 : (kQ8 ? 1 : 0);
+  const cudaError_t e = set_smem_limit_once((const void*)decode_kernel<kQ8, kStep, kDiag>, (int)kSmem,
+                                            g_decode_attr_set[kVariant]);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !g_decode_attr_set[kVariant][dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<kQ8, kStep>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-    if (e != cudaSuccess) return e;
-    g_decode_attr_set[kVariant][dev] = true;
-  }
-  return launch_maybe_pdl(overlap, decode_kernel<kQ8, kStep>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
+  return launch_maybe_pdl(overlap, decode_kernel<kQ8, kStep, kDiag>, dim3(grid), dim3(kThreads), kSmem, stream, p,
+                          plan);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
-                          cudaStream_t stream) {
-  return q8 ? launch_decode_as<true, false>(p, plan, grid, overlap, stream)
-            : launch_decode_as<false, false>(p, plan, grid, overlap, stream);
+                          bool diag, cudaStream_t stream) {
+  if (q8) return launch_decode_as<true, false>(p, plan, grid, overlap, stream);
+  return diag ? launch_decode_as<false, false, true>(p, plan, grid, overlap, stream)
+              : launch_decode_as<false, false>(p, plan, grid, overlap, stream);
 }
 
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream) {

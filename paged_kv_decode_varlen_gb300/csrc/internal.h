@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pa.h"
 
 namespace pa {
@@ -179,6 +181,21 @@ struct MergeParams {
   int32_t head_dim;
 };
 
+// Raises the dynamic shared-memory limit of kernel `fn` to `bytes` once per
+// device: done[dev] records that it was set.  Host threads may race on the
+// first call of a device; each then sets the same value, which is harmless,
+// and the flag is an atomic.
+constexpr int kMaxDevices = 64;
+inline cudaError_t set_smem_limit_once(const void* fn, int bytes, std::atomic<bool>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 // Sets the calling thread's pa_last_error_message() text and returns s.
 pa_status set_error(pa_status s, const char* fmt, ...);
 
@@ -186,9 +203,10 @@ pa_status set_error(pa_status s, const char* fmt, ...);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_kv_append_q8(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
-// overlap: programmatic launch after the stream's previous kernel
+// overlap: programmatic launch after the stream's previous kernel; diag:
+// the timeout-path diagnostic instantiation (bf16 pages only)
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
-                          cudaStream_t stream);
+                          bool diag, cudaStream_t stream);
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
                            cudaStream_t stream);

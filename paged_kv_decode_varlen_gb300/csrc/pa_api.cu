@@ -24,6 +24,7 @@ namespace {
 thread_local char g_msg[512] = "";
 std::atomic<int64_t> g_launches{0};
 std::atomic<int32_t> g_forced_ctas{0};
+std::atomic<int32_t> g_decode_fault{0};  // pa_set_decode_fault_injection
 
 pa_status fail(pa_status s, const char* fmt, ...) {
   va_list ap;
@@ -93,14 +94,20 @@ constexpr int kMinSegPages = 8;      // fewest pages per CTA worth a CTA
 
 int pages_of(int64_t len) { return (int)((len + pa::kPage - 1) / pa::kPage); }
 
+// SM count of the current device, cached per device (atomics: host threads
+// may race on a device's first call and store the same value).
 int sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[pa::kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (dev < 64 && cached[dev]) return cached[dev];
+  const bool slot = dev >= 0 && dev < pa::kMaxDevices;
+  if (slot) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  if (dev < 64) cached[dev] = n;
+  if (slot) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -536,7 +543,9 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
                                    plan);
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
-      s = run_launch(PA_KERNEL_DECODE, "decode", stream, [&] { return pa::launch_decode(dp, plan, grid, q8, overlap, stream); });
+      const bool diag = !q8 && g_decode_fault.load() != 0;
+      s = run_launch(PA_KERNEL_DECODE, "decode", stream,
+                     [&] { return pa::launch_decode(dp, plan, grid, q8, overlap, diag, stream); });
       if (s != PA_OK) return s;
     }
   }
@@ -826,6 +835,12 @@ pa_status pa_set_decode_ctas(int32_t n) {
   if (n < 0 || n > pa::kPlanMaxCtas)
     return fail(PA_ERR_INVALID_ARG, "decode grid %d outside [0, %d]", n, pa::kPlanMaxCtas);
   g_forced_ctas.store(n);
+  return ok();
+}
+
+pa_status pa_set_decode_fault_injection(int32_t on) {
+  if (on != 0 && on != 1) return fail(PA_ERR_INVALID_ARG, "fault injection switch %d (0 or 1)", on);
+  g_decode_fault.store(on);
   return ok();
 }
 

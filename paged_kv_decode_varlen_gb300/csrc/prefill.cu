@@ -566,17 +566,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefix_merge_kernel(const Pr
   if (lane == 0) p.prefix_lse[row] = wsum > 0.f ? M + log2f(wsum) : -INFINITY;
 }
 
-bool g_prefill_attr_set[64] = {};
-bool g_prefix_attr_set[64] = {};
+std::atomic<bool> g_prefill_attr_set[kMaxDevices];
+std::atomic<bool> g_prefix_attr_set[kMaxDevices];
 
-cudaError_t set_smem_attr(const void* fn, bool* done) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e == cudaSuccess && dev < 64) done[dev] = true;
-  return e;
+cudaError_t set_smem_attr(const void* fn, std::atomic<bool>* done) {
+  return set_smem_limit_once(fn, (int)kSmemBytes, done);
 }
 
 }  // namespace

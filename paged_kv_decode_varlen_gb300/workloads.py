@@ -270,7 +270,10 @@ def step_bytes(b: Batch, prefix_pages: int = 0, kv: str = "bf16") -> dict:
             dec_seen[blk] = max(dec_seen.get(blk, 0), min(P, L - i * P))
     decode_kv_unique = sum(dec_seen.values()) * per_tok
     n_dec = int(decode.sum())
-    decode_kernel = decode_kv_unique + n_dec * Hq * D * 2 + int(
+    # per decode row: its K/V pages, q read and out written (Hq x D bf16
+    # each), one 4-byte block-table entry per page; split partials are
+    # implementation overhead and not counted
+    decode_kernel = decode_kv_unique + 2 * n_dec * Hq * D * 2 + int(
         sum(4 * (-(-int(L) // P) - prefix_pages) for L in seq[decode]))
     prefix_kernel = prefix_pages * P * per_tok + total_q * Hq * D * 2 + 4 * prefix_pages if prefix_pages else 0
     # tensor-core tile kernel (rows with qo_len > 1): the keys each row reads
@@ -281,7 +284,7 @@ def step_bytes(b: Batch, prefix_pages: int = 0, kv: str = "bf16") -> dict:
         L, c = int(seq[r]), int(qo[r])
         h = L - c
         pre_kv += (L - prefix_pages * P) * per_tok
-        pre_q += c * Hq * D * 2
+        pre_q += 2 * c * Hq * D * 2          # q read, out written
         pre_tab += 4 * (-(-L // P) - prefix_pages)
         pre_flops += (c * h + c * (c + 1) // 2) * Hq * D * 4
     prefill_kernel = pre_kv + pre_q + pre_tab

@@ -109,6 +109,12 @@ def test_grid_override_bounds():
     assert lib.pa_set_decode_ctas(0) == b.PA_OK
 
 
+def test_fault_injection_switch_bounds():
+    assert lib.pa_set_decode_fault_injection(2) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_decode_fault_injection(-1) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_decode_fault_injection(0) == b.PA_OK
+
+
 def test_shared_prefix_workspace_size():
     base = b.pa_attention_workspace_size(16, 16, 32, 128, 8447)
     assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 0) == base

@@ -337,3 +337,32 @@ def test_launch_count_and_trace():
     names = [k for k, _ in rec]
     assert names[0] == "kv_append" and "decode" in names
     assert all(ms > 0 for _, ms in rec)
+
+
+# ------------------------------------------------ bounded waits (timeout path)
+def test_decode_wait_timeout_is_recorded_and_the_context_stays_usable():
+    # Rows long enough that every CTA's segment holds several pages; the
+    # diagnostic decode kernel arms CTA 0's second page without copying it,
+    # so that wait runs out after 1 ms: no fault, no hang.
+    b = W.make_batch([700, 900, 1200, 1500], [1, 1, 1, 1], num_blocks=300, seed=W.SEED0 + 72)
+    d = DevBatch(b)
+    B.pa_kv_append(d.k_new, d.v_new, d.slot_mapping, d.k_cache, d.v_cache)
+    ws = B.new_workspace(B.pa_attention_workspace_size(4, 4, 32, 128, 1500), "cuda")
+    B.pa_set_decode_fault_injection(True)
+    try:
+        B.pa_attention_varlen(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.qo_indptr, b.sm_scale,
+                              seq_lens_host=d.seq_lens_host, qo_indptr_host=d.qo_indptr_host, workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        B.pa_set_decode_fault_injection(False)
+    assert B.pa_get_device_error(ws) == B.PA_ERR_DEVICE_TIMEOUT
+    # a timed-out call leaves counters of the rows it cut; after zeroing the
+    # workspace the next call is exact again
+    ws.zero_()
+    out, lse = B.pa_attention_varlen(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.qo_indptr,
+                                     b.sm_scale, seq_lens_host=d.seq_lens_host, qo_indptr_host=d.qo_indptr_host,
+                                     workspace=ws, return_lse=True)
+    torch.cuda.synchronize()
+    assert B.pa_get_device_error(ws) == 0
+    ref_out, ref_lse, _, _ = oracle_step(b)
+    compare(out, ref_out, lse, ref_lse, what="after a timed-out call")
