@@ -365,7 +365,7 @@ pa_status pa_attention_varlen_shared_prefix(
  * handed only its input and output pointers.
  *   Same computation, arguments and results as pa_attention_varlen, except
  *   that there is no workspace argument: the scratch is a fixed array of
- *   PA_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, present on every
+ *   PA_NOALLOC_SCRATCH_BYTES (24 MiB) inside the library, present on every
  *   GPU that loads the library until the process exits.  A batch whose
  *   pa_attention_workspace_size() exceeds it is rejected with
  *   PA_ERR_UNSUPPORTED (and a message in pa_last_error_message()).
@@ -384,7 +384,7 @@ pa_status pa_attention_varlen_shared_prefix(
  *   Calls that overlap on the GPU race on the array, so issue them in order
  *   (e.g. on one stream).
  */
-#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define PA_NOALLOC_SCRATCH_BYTES (24u << 20)
 pa_status pa_attention_varlen_noalloc(const void* q, const void* k_cache, const void* v_cache, int64_t num_blocks,
                                       const int32_t* block_tables, int32_t max_blocks_per_req,
                                       const int32_t* seq_lens, const int32_t* qo_indptr,

@@ -1021,27 +1021,612 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
+
+// ------------------------------------------------- warp-granular host plan
+// Host-planned launches (pa_attention_varlen and its q8_0 / shared-prefix
+// forms) cut every CTA segment into kWarps equal warp segments: warp w of
+// CTA b streams pages [w sw, (w + 1) sw) of the CTA's segment (sw = seg /
+// kWarps) through its own kWgStages-deep ring and finishes its items on its
+// own.  A warp's item end (the merge of its 4 token slots, the partial of a
+// cut row, the count of finished pieces, the merge of all pieces by the
+// last one) then stalls only that warp: the other warps of the SM keep
+// streaming, and no CTA-wide barrier follows the prologue.  The page loop is
+// the same arithmetic as above; a warp takes the 16 tokens of a page as two
+// pairs per lane (tokens ts + 8 h and ts + 4 + 8 h, h = 0, 1).
+constexpr int kWgStages = 2;  // pages in flight per warp
+
+template <int kSlab>
+struct __align__(128) WgSmem {
+  uint8_t k[kWarps][kWgStages][kSlab];
+  uint8_t v[kWarps][kWgStages][kSlab];
+  uint16_t qs[kWarps][kGroup * kHeadDim];  // each warp's current item's q (bulk copy)
+  uint64_t full[kWarps][kWgStages];        // TMA landed
+  uint64_t q_full[kWarps];                 // q landed
+  int32_t ids[kDecodeMaxPagesPerCta];
+  Item items[kDecodeMaxItemsPerCta];
+  int stage_page[kWarps][kWgStages];  // last warp page issued into each stage (-1: none)
+  int q_issued[kWarps];
+  int n_items;
+  int abort_flag;
+};
+
+static_assert(offsetof(WgSmem<kSlabBytes>, v) % 128 == 0 && offsetof(WgSmem<kQ8SlabBytes>, v) % 16 == 0 &&
+                  offsetof(WgSmem<kSlabBytes>, qs) % 16 == 0 && offsetof(WgSmem<kQ8SlabBytes>, qs) % 16 == 0 &&
+                  (kWgStages * kSlabBytes) % 16 == 0 && (kWgStages * kQ8SlabBytes) % 16 == 0,
+              "bulk copies land on 16-byte boundaries");
+static_assert(3 * (sizeof(WgSmem<kSlabBytes>) + 1024) <= 228 * 1024, "three decode CTAs per SM");
+
+// One head per 8-lane group (head g = lane >> 3), 16 dims per lane (dims
+// 8c .. 8c + 7 and 64 + 8c .. 64 + 8c + 7): folds the shared-prefix
+// partials of output row orow into the normalised partial o with log2 lse
+// lse2 by log-sum-exp; returns the merged lse.  The 8 lanes of a group read
+// the partials' lse in parallel, then every partial load is in flight at once.
+__device__ __forceinline__ float fold_prefix_wg(const DecodeParams& p, float (&o)[16], float lse2, size_t orow,
+                                                int c, int lane) {
+  const int n = p.prefix_n;
+  const int gbase = lane & ~7;
+  float M = lse2;
+  for (int c0 = 0; c0 < n; c0 += 8)
+    if (c0 + c < n) M = fmaxf(M, p.prefix_lse[(size_t)(c0 + c) * p.prefix_rows + orow]);
+#pragma unroll
+  for (int s = 4; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+  if (M == -INFINITY) return -INFINITY;
+  const float wo = exp2f(lse2 - M);  // own part (-inf -> 0)
+  float wsum = wo;
+  float a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = o[i] * wo;
+  for (int c0 = 0; c0 < n; c0 += 8) {
+    const int nc = min(8, n - c0);
+    const float w = c < nc ? exp2f(p.prefix_lse[(size_t)(c0 + c) * p.prefix_rows + orow] - M) : 0.f;
+    float ws = w;
+#pragma unroll
+    for (int s = 4; s > 0; s >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s);
+    wsum += ws;
+    for (int i = 0; i < nc; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, w, gbase + i);
+      const float* y = p.prefix_o + ((size_t)(c0 + i) * p.prefix_rows + orow) * kHeadDim;
+      const float4 y0 = *reinterpret_cast<const float4*>(y + 8 * c);
+      const float4 y1 = *reinterpret_cast<const float4*>(y + 8 * c + 4);
+      const float4 y2 = *reinterpret_cast<const float4*>(y + 64 + 8 * c);
+      const float4 y3 = *reinterpret_cast<const float4*>(y + 64 + 8 * c + 4);
+      const float yy[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
+                            y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a[j] = fmaf(wi, yy[j], a[j]);
+    }
+  }
+  const float inv = 1.f / wsum;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = a[i] * inv;
+  return M + log2f(wsum);
+}
+
+// bf16 store of a lane's 16 dims (dims 8c .. 8c + 7 and 64 + 8c .. 64 + 8c + 7)
+__device__ __forceinline__ void store_row16(uint16_t* row, const float (&o)[16], int c) {
+  uint4 lo, hi;
+  lo.x = pack_bf16x2(o[0], o[1]);
+  lo.y = pack_bf16x2(o[2], o[3]);
+  lo.z = pack_bf16x2(o[4], o[5]);
+  lo.w = pack_bf16x2(o[6], o[7]);
+  hi.x = pack_bf16x2(o[8], o[9]);
+  hi.y = pack_bf16x2(o[10], o[11]);
+  hi.z = pack_bf16x2(o[12], o[13]);
+  hi.w = pack_bf16x2(o[14], o[15]);
+  *reinterpret_cast<uint4*>(row + 8 * c) = lo;
+  *reinterpret_cast<uint4*>(row + 64 + 8 * c) = hi;
+}
+
+// kDiag: the diagnostic instantiation that tests the timeout path (bf16
+// pages).  Warp 0 of CTA 0 arms the barrier of its second page without
+// issuing that page's copies, so the wait on it runs out; every wait of this
+// instantiation gives up after 1 ms instead of kWaitLimitNs.  No copy is
+// dropped anywhere else, and nothing is read out of bounds.
+template <bool kQ8, bool kDiag>
+__global__ void __launch_bounds__(kThreads, 3)
+    decode_wg_kernel(const DecodeParams p, const __grid_constant__ DecodePlan plan) {
+  static_assert(!(kDiag && kQ8), "the diagnostic instantiation reads bf16 pages");
+  constexpr unsigned long long kLimit = kDiag ? 1000000ull : kWaitLimitNs;
+  constexpr int kSlab = kQ8 ? kQ8SlabBytes : kSlabBytes;
+  using Smem = WgSmem<kSlab>;
+  // q of each item by a bulk copy into the warp's shared-memory slot, issued
+  // an item ahead (bf16 pages); q8_0 pages read q from global memory
+  constexpr bool kQSmem = !kQ8;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hkv = p.num_kv_heads;
+  const int kvh = b % Hkv, sidx = b / Hkv;
+  const int S0 = sidx * plan.seg;
+  const int npg = min(plan.total, S0 + plan.seg) - S0;  // pages of this CTA's segment
+  if (npg <= 0) return;
+  if (tid == 0) {
+    for (int w = 0; w < kWarps; ++w) {
+      for (int s = 0; s < kWgStages; ++s) {
+        mbar_init(&sm.full[w][s], 1);
+        sm.stage_page[w][s] = -1;
+      }
+      mbar_init(&sm.q_full[w], 1);
+      sm.q_issued[w] = 0;
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+  }
+  const int n_items_all = plan.n_rows;
+  // ---- item table of the CTA's segment (warp 0), 32 items per round; it
+  // comes from the kernel parameters alone, so it is built before the wait
+  // for the previous kernel
+  if (warp == 0) {
+    int base_q = 0, n_it = 0;
+    for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
+      const int item = plan.first_row[sidx] + k0 + lane;
+      const bool exists = item < n_items_all;
+      int r = 0, L = 0, size = 0, tok = 0;
+      const int p0 = (k0 + lane == 0) ? plan.first_page[sidx] : 0;
+      if (exists) {
+        r = plan.rows[item];
+        L = plan.seq[item];
+        tok = plan.tok[item];
+        size = max((L + kPage - 1) / kPage - p.page_offset - p0, 0);
+      }
+      int incl = size;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int start = base_q + incl - size;
+      const bool in_seg = size > 0 && start < npg;
+      if (in_seg && k0 + lane < kDecodeMaxItemsPerCta) {
+        Item& it = sm.items[k0 + lane];
+        it.q_start = start;
+        it.n = min(size, npg - start);
+        it.p0 = p0;
+        it.r = r;
+        it.L = L;
+        it.tok = tok;
+        it.A = S0 + start - p0;  // stream position of the row's page 0
+        bulk_prefetch_l2(p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim,
+                         kGroup * kHeadDim * 2);
+      }
+      const unsigned covered = __ballot_sync(0xffffffffu, in_seg);
+      const int prefix = (~covered == 0u) ? 32 : (__ffs((int)~covered) - 1);
+      n_it = k0 + prefix;
+      base_q += __shfl_sync(0xffffffffu, incl, 31);
+      if (prefix < 32 || base_q >= npg) break;
+    }
+    if (lane == 0) {
+      if (base_q < npg) record_error(p.err, PA_ERR_DEVICE_INDEX);  // metadata differ from the plan
+      sm.n_items = min(n_it, kDecodeMaxItemsPerCta);
+    }
+  }
+  __syncthreads();
+  pdl_wait();
+  const int n_items = sm.n_items;
+  if (n_items == 0) return;  // nothing covered (recorded above); no copy was issued
+  // ---- block ids of the segment's pages; an id outside the pool (or a page
+  // past the table) is recorded and masked, and fetched from block 0
+  const int n_cov = sm.items[n_items - 1].q_start + sm.items[n_items - 1].n;
+  int ok = 1;
+  for (int q = tid; q < n_cov; q += kThreads) {
+    int lo = 0, hi = n_items - 1;
+    while (lo < hi) {  // last item with q_start <= q
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.items[mid].q_start <= q) lo = mid; else hi = mid - 1;
+    }
+    int32_t blk = -1;
+    const Item& it = sm.items[lo];
+    const int page = p.page_offset + it.p0 + (q - it.q_start);
+    if (page < p.max_blocks_per_req) blk = p.block_tables[(size_t)it.r * p.max_blocks_per_req + page];
+    if (blk < 0 || blk >= p.num_blocks) {
+      record_error(p.err, PA_ERR_DEVICE_INDEX);
+      blk = -1;
+      ok = 0;
+    }
+    sm.ids[q] = blk;
+  }
+  const bool ids_ok = __syncthreads_and(ok) != 0;
+
+  // ---- this warp's part of the segment: pages [a, e)
+  const int sw = plan.seg / kWarps;
+  const int a = warp * sw;
+  const int e = min(a + sw, n_cov);
+  if (a >= e) return;
+  int k = 0;  // first item holding page a
+  {
+    int lo = 0, hi = n_items - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sm.items[mid].q_start <= a) lo = mid; else hi = mid - 1;
+    }
+    k = lo;
+  }
+  const int k_first = k;
+  const int gw = sidx * kWarps + warp;  // warp segment of the stream
+  const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_cache);
+  const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v_cache);
+  // segment page q in [a, e) -> warp page j = q - a -> stage j % kWgStages
+  auto issue = [&](int q) {
+    const int j = q - a;
+    const int s = j & (kWgStages - 1);
+    const size_t off = ((size_t)max(sm.ids[q], 0) * Hkv + kvh) * kSlab;
+    mbar_arrive_expect_tx(&sm.full[warp][s], 2 * kSlab);
+    if (!(kDiag && b == 0 && warp == 0 && j == 1)) {  // (diagnostic: armed, never copied)
+      bulk_g2s(sm.k[warp][s], kbase + off, kSlab, &sm.full[warp][s]);
+      bulk_g2s(sm.v[warp][s], vbase + off, kSlab, &sm.full[warp][s]);
+    }
+    sm.stage_page[warp][s] = j;  // only lane 0 of this warp writes it
+  };
+  auto issue_q = [&](int kk) {
+    const size_t qoff = ((size_t)sm.items[kk].tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
+    mbar_arrive_expect_tx(&sm.q_full[warp], kGroup * kHeadDim * 2);
+    bulk_g2s(sm.qs[warp], p.q + qoff, kGroup * kHeadDim * 2, &sm.q_full[warp]);
+    sm.q_issued[warp] += 1;
+  };
+  if (lane == 0) {
+    if constexpr (kQSmem) issue_q(k);
+    for (int q = a; q < min(e, a + kWgStages); ++q) issue(q);
+  }
+
+  const int ts = lane >> 3;  // token slot: tokens ts + 4 u of every page
+  const int c = lane & 7;    // dim chunk: dims [8c, 8c+8) and [64+8c, 64+8c+8)
+  // After the transposed reduction lane c holds token u = bit0(c) of the
+  // pair and head hd = 2 bit2(c) + bit1(c).
+  const int slot_base = lane & ~7;
+  bool aborted = false;
+  int nq = 0;  // q copies this warp has consumed
+
+  for (; k < n_items && !aborted; ++k) {
+    const Item& it = sm.items[k];
+    const int i0 = max(it.q_start, a);
+    const int i1 = min(it.q_start + it.n, e);
+    if (i0 >= i1) break;  // past this warp's pages
+    const int tok = it.tok;
+    const int p0w = it.p0 + (i0 - it.q_start);  // row page of the warp's first page of the item
+    const int pages_abs = (it.L + kPage - 1) / kPage;
+    const int pages_r = pages_abs - p.page_offset;  // pages of the row in the stream
+    const int tail_tokens = it.L - (pages_abs - 1) * kPage;
+    const int q_last = i0 + (pages_r - 1 - p0w);  // segment page holding the row's last token
+    // q of the 4 heads of this group, scaled into the log2 domain (see qk16 /
+    // qk16_q8 for the two layouts)
+    float2 qp[2][16];
+    if (kQSmem && !mbar_wait_bounded(&sm.q_full[warp], (uint32_t)nq & 1u, kLimit)) {
+      record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+      *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+      aborted = true;
+      break;
+    }
+    ++nq;
+    {
+      const uint16_t* qrow =
+          kQSmem ? sm.qs[warp] : p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim;
+#pragma unroll
+      for (int hp = 0; hp < 2; ++hp) {
+        float f0[16], f1[16];
+        unpack16s(*reinterpret_cast<const uint4*>(qrow + (2 * hp) * kHeadDim + 8 * c),
+                  *reinterpret_cast<const uint4*>(qrow + (2 * hp) * kHeadDim + 64 + 8 * c), f0);
+        unpack16s(*reinterpret_cast<const uint4*>(qrow + (2 * hp + 1) * kHeadDim + 8 * c),
+                  *reinterpret_cast<const uint4*>(qrow + (2 * hp + 1) * kHeadDim + 64 + 8 * c), f1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if constexpr (kQ8) {
+            qp[hp][i] = make_float2(f0[i] * p.scale_log2, f1[i] * p.scale_log2);
+          } else {
+            const float* f = (i < 8) ? f0 : f1;
+            const int j = i & 7;
+            qp[hp][i] = make_float2(f[2 * j] * p.scale_log2, f[2 * j + 1] * p.scale_log2);
+          }
+        }
+      }
+    }
+    if constexpr (kQSmem) {
+      // every lane holds its q: the warp's next item's q can land
+      __syncwarp();
+      if (lane == 0 && k + 1 < n_items && sm.items[k + 1].q_start < e) {
+        fence_proxy_async_smem();
+        issue_q(k + 1);
+      }
+    }
+    float2 acc[kGroup][8];
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[g][j] = make_float2(0.f, 0.f);
+    // running max of head hd (the same in lanes c and c ^ 1) and the sum of
+    // this lane's own weights
+    float m_own = -INFINITY, l_own = 0.f;
+
+    for (int q = i0; q < i1; ++q) {
+      const int j = q - a;
+      const int s = j & (kWgStages - 1);
+      if (!mbar_wait_bounded(&sm.full[warp][s], (uint32_t)(j / kWgStages) & 1u, kLimit)) {
+        record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
+        aborted = true;
+        break;
+      }
+      const bool last_pg = q == q_last;
+      const bool pg_ok = ids_ok || sm.ids[q] >= 0;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int t0 = ts + 8 * h, t1 = t0 + 4;  // the pair's two tokens of the page
+        const bool valid0 = pg_ok && (!last_pg || t0 < tail_tokens);
+        const bool valid1 = pg_ok && (!last_pg || t1 < tail_tokens);
+        float2 sA01, sA23, sB01, sB23;
+        float vdA0 = 0.f, vdB0 = 0.f, vdA1 = 0.f, vdB1 = 0.f;  // q8_0: V group scales of the two tokens
+        if constexpr (kQ8) {
+          const uint8_t* kr0 = sm.k[warp][s] + t0 * kHeadDim;
+          const uint8_t* kr1 = sm.k[warp][s] + t1 * kHeadDim;
+          float kdA0, kdB0, kdA1, kdB1;
+          q8_scales(sm.k[warp][s], t0, c, kdA0, kdB0);
+          q8_scales(sm.k[warp][s], t1, c, kdA1, kdB1);
+          q8_scales(sm.v[warp][s], t0, c, vdA0, vdB0);
+          q8_scales(sm.v[warp][s], t1, c, vdA1, vdB1);
+          qk16_q8(qp, *reinterpret_cast<const uint2*>(kr0 + 8 * c),
+                  *reinterpret_cast<const uint2*>(kr0 + 64 + 8 * c), kdA0, kdB0, sA01, sA23);
+          qk16_q8(qp, *reinterpret_cast<const uint2*>(kr1 + 8 * c),
+                  *reinterpret_cast<const uint2*>(kr1 + 64 + 8 * c), kdA1, kdB1, sB01, sB23);
+        } else {
+          const uint8_t* kr0 = sm.k[warp][s] + t0 * (kHeadDim * 2);
+          const uint8_t* kr1 = sm.k[warp][s] + t1 * (kHeadDim * 2);
+          const uint4 ka0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
+          const uint4 kb0 = *reinterpret_cast<const uint4*>(kr0 + 128 + 16 * c);
+          const uint4 ka1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
+          const uint4 kb1 = *reinterpret_cast<const uint4*>(kr1 + 128 + 16 * c);
+          qk16(qp, ka0, kb0, sA01, sA23);
+          qk16(qp, ka1, kb1, sB01, sB23);
+        }
+        // transposed reduction: 8 values per lane -> 1 complete (token, head)
+        float sc;
+        {
+          const bool b2 = (c >> 2) & 1, b1 = (c >> 1) & 1, b0 = c & 1;
+          float2 kA = b2 ? sA23 : sA01, kB = b2 ? sB23 : sB01;
+          const float2 oA = shfl_xor2(b2 ? sA01 : sA23, 4), oB = shfl_xor2(b2 ? sB01 : sB23, 4);
+          kA = __fadd2_rn(kA, oA);
+          kB = __fadd2_rn(kB, oB);
+          float2 kk = b1 ? make_float2(kA.y, kB.y) : make_float2(kA.x, kB.x);
+          const float2 send = b1 ? make_float2(kA.x, kB.x) : make_float2(kA.y, kB.y);
+          kk = __fadd2_rn(kk, shfl_xor2(send, 2));
+          sc = (b0 ? kk.y : kk.x) + __shfl_xor_sync(0xffffffffu, b0 ? kk.x : kk.y, 1);
+        }
+        const bool my_valid = (c & 1) ? valid1 : valid0;
+        const float sv = my_valid ? sc : -INFINITY;
+        const float mx = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, 1));  // both tokens of head hd
+        const bool grow = mx > m_own + kRescaleSlack;
+        if (__any_sync(0xffffffffu, grow)) {  // running max grew a lot: rescale (rare)
+          const float corr = grow ? fast_exp2(m_own - mx) : 1.f;  // m_own = -inf -> 0
+          if (grow) m_own = mx;
+          l_own *= corr;
+#pragma unroll
+          for (int g = 0; g < kGroup; ++g) {
+            const float cg = __shfl_sync(0xffffffffu, corr, slot_base + (g >> 1) * 4 + (g & 1) * 2);
+            const float2 c2 = make_float2(cg, cg);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) acc[g][jj] = __fmul2_rn(acc[g][jj], c2);
+          }
+        }
+        const float pown = my_valid ? fast_exp2(sv - m_own) : 0.f;
+        l_own += pown;
+        float pA[kGroup], pB[kGroup];
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+          const int src = slot_base + (g >> 1) * 4 + (g & 1) * 2;
+          pA[g] = __shfl_sync(0xffffffffu, pown, src);
+          pB[g] = __shfl_sync(0xffffffffu, pown, src + 1);
+        }
+        if constexpr (kQ8) {
+          if (valid0) {
+            const uint8_t* vr = sm.v[warp][s] + t0 * kHeadDim;
+            pv16_q8(acc, pA, *reinterpret_cast<const uint2*>(vr + 8 * c),
+                    *reinterpret_cast<const uint2*>(vr + 64 + 8 * c), vdA0, vdB0);
+          }
+          if (valid1) {
+            const uint8_t* vr = sm.v[warp][s] + t1 * kHeadDim;
+            pv16_q8(acc, pB, *reinterpret_cast<const uint2*>(vr + 8 * c),
+                    *reinterpret_cast<const uint2*>(vr + 64 + 8 * c), vdA1, vdB1);
+          }
+        } else {
+          if (valid0) {
+            const uint8_t* vr = sm.v[warp][s] + t0 * (kHeadDim * 2);
+            pv16(acc, pA, *reinterpret_cast<const uint4*>(vr + 16 * c),
+                 *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
+          }
+          if (valid1) {
+            const uint8_t* vr = sm.v[warp][s] + t1 * (kHeadDim * 2);
+            pv16(acc, pB, *reinterpret_cast<const uint4*>(vr + 16 * c),
+                 *reinterpret_cast<const uint4*>(vr + 128 + 16 * c));
+          }
+        }
+      }
+      // the warp is done with page q: refill its stage with page q + kWgStages
+      __syncwarp();
+      if (lane == 0 && q + kWgStages < e) {
+        fence_proxy_async_smem();
+        issue(q + kWgStages);
+      }
+      if (((q - i0) & 15) == 15 && *reinterpret_cast<volatile int*>(&sm.abort_flag)) {
+        aborted = true;
+        break;
+      }
+    }
+    if (aborted) break;
+
+    // ---- item end: merge the warp's 4 token slots (shuffles only); lane
+    // (ts, c) ends with head g = ts, dims of chunk c
+    const int g = ts;
+    float o[16];
+    float lse2;
+    {
+      const float l_pair = l_own + __shfl_xor_sync(0xffffffffu, l_own, 1);
+      float Mw[kGroup], Lw[kGroup];
+#pragma unroll
+      for (int gg = 0; gg < kGroup; ++gg) {
+        const int src = slot_base + (gg >> 1) * 4 + (gg & 1) * 2;
+        const float mh = __shfl_sync(0xffffffffu, m_own, src);
+        const float lh = __shfl_sync(0xffffffffu, l_pair, src);
+        float Mg = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 8));
+        Mg = fmaxf(Mg, __shfl_xor_sync(0xffffffffu, Mg, 16));
+        Mw[gg] = Mg;
+        const float f = (mh == -INFINITY) ? 0.f : fast_exp2(mh - Mg);
+        const float2 f2 = make_float2(f, f);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) acc[gg][jj] = __fmul2_rn(acc[gg][jj], f2);
+        float lsum = lh * f;
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
+        Lw[gg] = lsum;
+      }
+      // sum over the 4 token slots, transposed: slot (s1, s0) ends with head 2 s1 + s0
+      const bool s1 = (lane >> 4) & 1, s0 = (lane >> 3) & 1;
+      float2 h0[8], h1[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {  // xor 16: keep heads {2 s1, 2 s1 + 1}
+        const float2 keep0 = s1 ? acc[2][jj] : acc[0][jj], send0 = s1 ? acc[0][jj] : acc[2][jj];
+        const float2 keep1 = s1 ? acc[3][jj] : acc[1][jj], send1 = s1 ? acc[1][jj] : acc[3][jj];
+        h0[jj] = __fadd2_rn(keep0, shfl_xor2(send0, 16));
+        h1[jj] = __fadd2_rn(keep1, shfl_xor2(send1, 16));
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {  // xor 8: keep head 2 s1 + s0
+        const float2 keep = s0 ? h1[jj] : h0[jj], send = s0 ? h0[jj] : h1[jj];
+        h0[jj] = __fadd2_rn(keep, shfl_xor2(send, 8));
+      }
+      const float M = g == 0 ? Mw[0] : g == 1 ? Mw[1] : g == 2 ? Mw[2] : Mw[3];
+      const float Ls = g == 0 ? Lw[0] : g == 1 ? Lw[1] : g == 2 ? Lw[2] : Lw[3];
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        o[2 * jj] = h0[jj].x * inv;
+        o[2 * jj + 1] = h0[jj].y * inv;
+      }
+      lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
+    }
+    const int head = kvh * kGroup + g;
+    const size_t orow = (size_t)tok * p.num_q_heads + head;
+    if (p0w == 0 && i1 - i0 == pages_r) {  // the whole row in this warp
+      if (p.prefix_o) lse2 = fold_prefix_wg(p, o, lse2, orow, c, lane);
+      store_row16(p.out + orow * kHeadDim, o, c);
+      if (p.lse && c == 0) p.lse[orow] = lse2 * kLn2;
+      continue;
+    }
+    // the item is cut by warp-segment boundaries: publish this warp's partial
+    const int A = it.A;
+    const int b0 = A / sw, b1 = (A + pages_r - 1) / sw;  // warp segments holding the row's pages
+    const int jslot = (k == k_first) ? 0 : 1;
+    {
+      const size_t slot = ((size_t)(gw * Hkv + kvh) * 2 + jslot) * kGroup + g;
+      float* dst = p.piece_o + slot * kHeadDim;
+      *reinterpret_cast<float4*>(dst + 8 * c) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(dst + 8 * c + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      *reinterpret_cast<float4*>(dst + 64 + 8 * c) = make_float4(o[8], o[9], o[10], o[11]);
+      *reinterpret_cast<float4*>(dst + 64 + 8 * c + 4) = make_float4(o[12], o[13], o[14], o[15]);
+      if (c == 0) p.piece_lse[slot] = lse2;
+    }
+    __syncwarp();  // every lane's piece write precedes lane 0's release below
+    int last = 0;
+    if (lane == 0) {
+      int* cnt = p.counters + (size_t)it.r * Hkv + kvh;
+      const int done = atom_add_acq_rel_gpu(cnt, 1);
+      last = done == b1 - b0;
+      if (last) *cnt = 0;  // every piece has arrived: ready for the next call
+    }
+    __syncwarp();  // lane 0's acquire orders the piece reads below
+    if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+    // the last piece to finish: merge all pieces of the row (8 lanes of a
+    // head read 8 pieces' lse in parallel, then every piece load is in flight)
+    {
+      const int n_pc = b1 - b0 + 1;
+      const int gbase = lane & ~7;
+      auto piece_slot = [&](int bb) {
+        const int jj = (bb == b0 && b0 * sw < A) ? 1 : 0;
+        return ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
+      };
+      float Mx = -INFINITY;
+      for (int c0 = 0; c0 < n_pc; c0 += 8)
+        if (c0 + c < n_pc) Mx = fmaxf(Mx, __ldcg(p.piece_lse + piece_slot(b0 + c0 + c)));
+#pragma unroll
+      for (int s2 = 4; s2 > 0; s2 >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, s2));
+      float wsum = 0.f;
+      float a4[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) a4[i] = 0.f;
+      if (Mx != -INFINITY) {
+        for (int c0 = 0; c0 < n_pc; c0 += 8) {
+          const int nc = min(8, n_pc - c0);
+          const float w = c < nc ? fast_exp2(__ldcg(p.piece_lse + piece_slot(b0 + c0 + c)) - Mx) : 0.f;
+          float ws = w;
+#pragma unroll
+          for (int s2 = 4; s2 > 0; s2 >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s2);
+          wsum += ws;
+          for (int i = 0; i < nc; ++i) {
+            const float wi = __shfl_sync(0xffffffffu, w, gbase + i);
+            const float* y = p.piece_o + piece_slot(b0 + c0 + i) * kHeadDim;
+            const float4 y0 = __ldcg(reinterpret_cast<const float4*>(y + 8 * c));
+            const float4 y1 = __ldcg(reinterpret_cast<const float4*>(y + 8 * c + 4));
+            const float4 y2 = __ldcg(reinterpret_cast<const float4*>(y + 64 + 8 * c));
+            const float4 y3 = __ldcg(reinterpret_cast<const float4*>(y + 64 + 8 * c + 4));
+            const float yy[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
+                                  y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) a4[jj] = fmaf(wi, yy[jj], a4[jj]);
+          }
+        }
+      }
+      const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) a4[i] *= winv;
+      float l2 = wsum > 0.f ? Mx + log2f(wsum) : -INFINITY;
+      if (p.prefix_o) l2 = fold_prefix_wg(p, a4, l2, orow, c, lane);
+      store_row16(p.out + orow * kHeadDim, a4, c);
+      if (p.lse && c == 0) p.lse[orow] = l2 * kLn2;
+    }
+  }
+
+  if (aborted && lane == 0) {
+    // A wait gave up: let the last copy issued into each of this warp's
+    // stages land (bounded), then leave.  A stage whose copies never land is
+    // passed over after the bound; the others are still waited for, so no
+    // copy that can land is in flight when the warp leaves.
+    for (int s = 0; s < kWgStages; ++s) {
+      const int j = sm.stage_page[warp][s];
+      if (j >= 0) mbar_wait_bounded(&sm.full[warp][s], (uint32_t)(j / kWgStages) & 1u, kLimit);
+    }
+    if (sm.q_issued[warp] > 0) mbar_wait_bounded(&sm.q_full[warp], (uint32_t)(sm.q_issued[warp] - 1) & 1u, kLimit);
+  }
+}
+
 std::atomic<bool> g_decode_attr_set[4][kMaxDevices];
 
 template <bool kQ8, bool kStep, bool kDiag = false>
 cudaError_t launch_decode_as(const DecodeParams& p, const typename PlanOf<kStep>::type& plan, int grid,
                              bool overlap, cudaStream_t stream) {
   constexpr size_t kSmem = sizeof(DecodeSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
-  constexpr int kVariant = kDiag ? 3 : kStep ? 2 : (kQ8 ? 1 : 0);
   const cudaError_t e = set_smem_limit_once((const void*)decode_kernel<kQ8, kStep, kDiag>, (int)kSmem,
-                                            g_decode_attr_set[kVariant]);
+                                            g_decode_attr_set[2]);
   if (e != cudaSuccess) return e;
   return launch_maybe_pdl(overlap, decode_kernel<kQ8, kStep, kDiag>, dim3(grid), dim3(kThreads), kSmem, stream, p,
                           plan);
+}
+
+template <bool kQ8, bool kDiag>
+cudaError_t launch_decode_wg(const DecodeParams& p, const DecodePlan& plan, int grid, bool overlap,
+                             cudaStream_t stream) {
+  constexpr size_t kSmem = sizeof(WgSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
+  constexpr int kVariant = kDiag ? 3 : (kQ8 ? 1 : 0);
+  const cudaError_t e =
+      set_smem_limit_once((const void*)decode_wg_kernel<kQ8, kDiag>, (int)kSmem, g_decode_attr_set[kVariant]);
+  if (e != cudaSuccess) return e;
+  return launch_maybe_pdl(overlap, decode_wg_kernel<kQ8, kDiag>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
                           bool diag, cudaStream_t stream) {
-  if (q8) return launch_decode_as<true, false>(p, plan, grid, overlap, stream);
-  return diag ? launch_decode_as<false, false, true>(p, plan, grid, overlap, stream)
-              : launch_decode_as<false, false>(p, plan, grid, overlap, stream);
+  if (q8) return launch_decode_wg<true, false>(p, plan, grid, overlap, stream);
+  return diag ? launch_decode_wg<false, true>(p, plan, grid, overlap, stream)
+              : launch_decode_wg<false, false>(p, plan, grid, overlap, stream);
 }
 
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream) {

@@ -42,6 +42,9 @@ struct CopyParams {
 constexpr int kPlanMaxRows = 1024;   // decode rows per launch
 constexpr int kPlanMaxCtas = 1024;   // CTAs per launch
 constexpr int kDecodeMaxItemsPerCta = 64;
+// Host-planned decode launches cut each CTA's segment into this many warp
+// segments (one per warp); the plan's segment length is a multiple of it.
+constexpr int kDecodeWarps = 4;
 struct DecodePlan {
   int32_t n_rows;                     // decode rows of this launch
   int32_t seg;                        // pages per segment
@@ -93,8 +96,9 @@ struct DecodeParams {
   int64_t prefix_rows;      // total_q * Hq: the stride between two partials' rows
   uint16_t* out;         // bf16 [total_q, Hq, D]
   float* lse;            // [total_q, Hq] natural log, or null
-  float* piece_o;        // fp32 [2 * grid, 4, D]: a CTA's partial of its first / last item
-  float* piece_lse;      // fp32 [2 * grid, 4], log2 domain
+  float* piece_o;        // fp32 [2 * grid * kDecodeWarps, 4, D]: a warp segment's (host plan) or a CTA's
+                         // (decode step) partial of its first / last item
+  float* piece_lse;      // fp32 [2 * grid * kDecodeWarps, 4], log2 domain
   int* counters;         // [num_reqs, Hkv] CTAs finished per item; zero between calls
   int* err;
   // decode step only: the new token of every row ([rows, Hkv, D] bf16) and

@@ -24,7 +24,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocBytes = size_t(8) << 20;  // PA_NOALLOC_SCRATCH_BYTES
+constexpr size_t kNoAllocBytes = size_t(24) << 20;  // PA_NOALLOC_SCRATCH_BYTES
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 

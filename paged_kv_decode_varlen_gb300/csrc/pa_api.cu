@@ -127,14 +127,17 @@ int grid_cap(int32_t num_reqs, int32_t num_kv_heads, int32_t max_seq_len) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: [error word | item counters (num_reqs x Hkv int32) |
-// partial o (2 x grid_cap x 4 heads x D fp32) | partial lse (fp32)].
+// partial o (2 x grid_cap x pieces_per_cta x 4 heads x D fp32) | partial lse
+// (fp32)].  A host-planned decode CTA publishes pieces per warp segment
+// (kDecodeWarps of them), the self-planned decode step per CTA.
 struct WorkspaceLayout {
   size_t counters, piece_o, piece_lse, total;
 };
 
-WorkspaceLayout layout_for_grid(int32_t num_reqs, int32_t hkv, int32_t head_dim, int grid) {
+WorkspaceLayout layout_for_grid(int32_t num_reqs, int32_t hkv, int32_t head_dim, int grid,
+                                int pieces_per_cta = pa::kDecodeWarps) {
   WorkspaceLayout w;
-  const size_t slots = (size_t)2 * grid * PA_GQA_GROUP;
+  const size_t slots = (size_t)2 * grid * pieces_per_cta * PA_GQA_GROUP;
   w.counters = PA_ERROR_WORD_BYTES;
   w.piece_o = w.counters + align256((size_t)std::max(num_reqs, 0) * (size_t)hkv * 4);
   w.piece_lse = w.piece_o + align256(slots * (size_t)std::max(head_dim, 0) * 4);
@@ -231,7 +234,9 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
   if (forced <= 0 && need > nseg) nseg = std::min<int64_t>((need + wave - 1) / wave * wave, seg_cap);
   int64_t seg = (total + nseg - 1) / nseg;
   seg = std::max<int64_t>(seg, (total + seg_cap - 1) / seg_cap);
+  seg = (seg + pa::kDecodeWarps - 1) / pa::kDecodeWarps * pa::kDecodeWarps;  // whole warp segments
   seg = std::min<int64_t>(seg, pa::kDecodeMaxPagesPerCta);  // more segments if one would be too long
+  static_assert(pa::kDecodeMaxPagesPerCta % pa::kDecodeWarps == 0, "segments hold whole warp segments");
   for (;;) {
     const int ns = (int)((total + seg - 1) / seg);
     if (ns > seg_cap) return -1;
@@ -261,8 +266,9 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
       }
       return ns * num_kv_heads;
     }
-    if (seg == 1) return -1;
-    seg = (seg + 1) / 2;  // shorter segments touch fewer rows
+    if (seg <= pa::kDecodeWarps) return -1;
+    // shorter segments touch fewer rows
+    seg = ((seg + 1) / 2 + pa::kDecodeWarps - 1) / pa::kDecodeWarps * pa::kDecodeWarps;
   }
 }
 
@@ -694,7 +700,7 @@ size_t pa_decode_step_workspace_size(int32_t num_reqs, int32_t num_q_heads, int3
   const int32_t hkv = num_q_heads / PA_GQA_GROUP;
   const int grid = step_grid(num_reqs, hkv, max_seq_len);
   if (grid < 0) return 0;
-  return layout_for_grid(num_reqs, hkv, head_dim, grid).total;
+  return layout_for_grid(num_reqs, hkv, head_dim, grid, 1).total;
 }
 
 int32_t pa_decode_step_bucket(int32_t num_reqs) {
@@ -729,7 +735,7 @@ pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, vo
   if (grid < 0)
     return fail(PA_ERR_UNSUPPORTED, "%d rows of up to %d tokens need more than %d CTAs", num_reqs, max_seq_len,
                 pa::kPlanMaxCtas);
-  const WorkspaceLayout wl = layout_for_grid(num_reqs, num_kv_heads, head_dim, grid);
+  const WorkspaceLayout wl = layout_for_grid(num_reqs, num_kv_heads, head_dim, grid, 1);
   if (workspace_bytes < wl.total)
     return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, wl.total);
   if (num_reqs == 0) return ok();

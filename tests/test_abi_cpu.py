@@ -34,11 +34,11 @@ def test_workspace_size_query():
     small = b.pa_attention_workspace_size(4, 4, 32, 128, 513)
     big = b.pa_attention_workspace_size(64, 64, 32, 128, 2303)
     assert small >= b.PA_ERROR_WORD_BYTES and big >= small and big % 256 == 0 and small % 256 == 0
-    # error word + counters (num_reqs x 8 int32) + two partial slots of 4 heads x 129 fp32 per CTA
-    # for a 480-CTA bound
-    slots = 2 * 480 * 4
-    assert b.pa_attention_workspace_size(1, 1, 32, 128, 16) == 256 + 256 + slots * 512 + 15360
-    assert b.pa_attention_workspace_size(100, 100, 32, 128, 16) == 256 + 3328 + slots * 512 + 15360
+    # error word + counters (num_reqs x 8 int32) + two partial slots of 4 heads x 129 fp32 per warp
+    # segment (4 per CTA) for a 480-CTA bound
+    slots = 2 * 480 * 4 * 4
+    assert b.pa_attention_workspace_size(1, 1, 32, 128, 16) == 256 + 256 + slots * 512 + slots * 4
+    assert b.pa_attention_workspace_size(100, 100, 32, 128, 16) == 256 + 3328 + slots * 512 + slots * 4
     # very long rows raise the grid bound (1024 pages per CTA at most)
     assert b.pa_attention_workspace_size(1024, 1024, 32, 128, 1 << 20) > big
 

@@ -81,10 +81,10 @@ def test_noalloc_reports_a_bad_block_id_and_then_recovers():
 
 
 def test_noalloc_scratch_bounds():
-    scratch = 8 << 20
+    scratch = 24 << 20
     # every batch of the pages' head shape (8 kv heads, 32 q heads) fits the
     # fixed scratch: at most 65,535 requests and a decode grid of at most
-    # 1,024 CTAs
+    # 1,024 CTAs (4 warp segments each)
     assert 0 < B.pa_attention_workspace_size(65535, 65535, 32, 128, 1 << 20) <= scratch
     # more requests than pa_attention_varlen accepts: rejected as an invalid
     # argument before any host array is read
