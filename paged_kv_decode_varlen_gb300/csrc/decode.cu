@@ -1083,17 +1083,34 @@ __device__ __forceinline__ float fold_prefix_wg(const DecodeParams& p, float (&o
 #pragma unroll
     for (int s = 4; s > 0; s >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s);
     wsum += ws;
-    for (int i = 0; i < nc; ++i) {
-      const float wi = __shfl_sync(0xffffffffu, w, gbase + i);
-      const float* y = p.prefix_o + ((size_t)(c0 + i) * p.prefix_rows + orow) * kHeadDim;
-      const float4 y0 = *reinterpret_cast<const float4*>(y + 8 * c);
-      const float4 y1 = *reinterpret_cast<const float4*>(y + 8 * c + 4);
-      const float4 y2 = *reinterpret_cast<const float4*>(y + 64 + 8 * c);
-      const float4 y3 = *reinterpret_cast<const float4*>(y + 64 + 8 * c + 4);
-      const float yy[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
-                            y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
+    // four partials' loads in flight at a time
 #pragma unroll
-      for (int j = 0; j < 16; ++j) a[j] = fmaf(wi, yy[j], a[j]);
+    for (int i0 = 0; i0 < 8; i0 += 4) {
+      if (i0 >= nc) break;
+      float4 y[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (i0 + u < nc) {
+          const float* yr = p.prefix_o + ((size_t)(c0 + i0 + u) * p.prefix_rows + orow) * kHeadDim;
+          y[u][0] = *reinterpret_cast<const float4*>(yr + 8 * c);
+          y[u][1] = *reinterpret_cast<const float4*>(yr + 8 * c + 4);
+          y[u][2] = *reinterpret_cast<const float4*>(yr + 64 + 8 * c);
+          y[u][3] = *reinterpret_cast<const float4*>(yr + 64 + 8 * c + 4);
+        } else {
+          y[u][0] = y[u][1] = y[u][2] = y[u][3] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float wi = __shfl_sync(0xffffffffu, w, gbase + i0 + u);  // 0 past nc
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          a[4 * v4 + 0] = fmaf(wi, y[u][v4].x, a[4 * v4 + 0]);
+          a[4 * v4 + 1] = fmaf(wi, y[u][v4].y, a[4 * v4 + 1]);
+          a[4 * v4 + 2] = fmaf(wi, y[u][v4].z, a[4 * v4 + 2]);
+          a[4 * v4 + 3] = fmaf(wi, y[u][v4].w, a[4 * v4 + 3]);
+        }
+      }
     }
   }
   const float inv = 1.f / wsum;
@@ -1559,17 +1576,34 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
           for (int s2 = 4; s2 > 0; s2 >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s2);
           wsum += ws;
-          for (int i = 0; i < nc; ++i) {
-            const float wi = __shfl_sync(0xffffffffu, w, gbase + i);
-            const float* y = p.piece_o + piece_slot(b0 + c0 + i) * kHeadDim;
-            const float4 y0 = __ldcg(reinterpret_cast<const float4*>(y + 8 * c));
-            const float4 y1 = __ldcg(reinterpret_cast<const float4*>(y + 8 * c + 4));
-            const float4 y2 = __ldcg(reinterpret_cast<const float4*>(y + 64 + 8 * c));
-            const float4 y3 = __ldcg(reinterpret_cast<const float4*>(y + 64 + 8 * c + 4));
-            const float yy[16] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w,
-                                  y2.x, y2.y, y2.z, y2.w, y3.x, y3.y, y3.z, y3.w};
+          // four pieces' loads in flight at a time
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) a4[jj] = fmaf(wi, yy[jj], a4[jj]);
+          for (int i0 = 0; i0 < 8; i0 += 4) {
+            if (i0 >= nc) break;
+            float4 y[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (i0 + u < nc) {
+                const float* yr = p.piece_o + piece_slot(b0 + c0 + i0 + u) * kHeadDim;
+                y[u][0] = __ldcg(reinterpret_cast<const float4*>(yr + 8 * c));
+                y[u][1] = __ldcg(reinterpret_cast<const float4*>(yr + 8 * c + 4));
+                y[u][2] = __ldcg(reinterpret_cast<const float4*>(yr + 64 + 8 * c));
+                y[u][3] = __ldcg(reinterpret_cast<const float4*>(yr + 64 + 8 * c + 4));
+              } else {
+                y[u][0] = y[u][1] = y[u][2] = y[u][3] = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float wi = __shfl_sync(0xffffffffu, w, gbase + i0 + u);  // 0 past nc
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                a4[4 * v4 + 0] = fmaf(wi, y[u][v4].x, a4[4 * v4 + 0]);
+                a4[4 * v4 + 1] = fmaf(wi, y[u][v4].y, a4[4 * v4 + 1]);
+                a4[4 * v4 + 2] = fmaf(wi, y[u][v4].z, a4[4 * v4 + 2]);
+                a4[4 * v4 + 3] = fmaf(wi, y[u][v4].w, a4[4 * v4 + 3]);
+              }
+            }
           }
         }
       }
