@@ -142,6 +142,20 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
   return old;
 }
 
+// Acquire load at GPU scope (pairs with a release by another CTA).
+__device__ __forceinline__ int ld_acquire_gpu(const int* addr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Release add at GPU scope: this thread's earlier writes (and those it has
+// observed, e.g. through a CTA barrier) are visible to a thread that
+// acquires the new value.
+__device__ __forceinline__ void red_add_release_gpu(int* addr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Kernels are launched with programmatic stream serialization: each CTA of
 // the short kernels lets the next kernel of the stream be scheduled as soon

@@ -1119,6 +1119,48 @@ __device__ __forceinline__ float fold_prefix_wg(const DecodeParams& p, float (&o
   return M + log2f(wsum);
 }
 
+// A prefix pass running beside the decode launch (p.prefix_done set): wait,
+// bounded, until the key chunks of token tok's query tile are all written.
+// Whole warp; false on a timeout (recorded), and the fold is left out.
+__device__ __forceinline__ bool prefix_ready(const DecodeParams& p, int tok, int kvh, int lane) {
+  if (!p.prefix_done) return true;
+  int ok = 1;
+  if (lane == 0) {
+    const int* f = p.prefix_done + (size_t)(tok / kPrefillQTile) * p.num_kv_heads + kvh;
+    if (ld_acquire_gpu(f) < p.prefix_n) {
+      const unsigned long long t0 = globaltimer();
+      while (ld_acquire_gpu(f) < p.prefix_n) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          record_error(p.err, PA_ERR_DEVICE_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();  // lane 0's acquire orders every lane's partial reads
+  return ok != 0;
+}
+
+// After a fold (whole warp): count the reader; the last reader of a tile's
+// kv head (one per query token of the tile) returns both counters to zero
+// for the next call.
+__device__ __forceinline__ void prefix_read_done(const DecodeParams& p, int tok, int kvh, int lane) {
+  if (!p.prefix_done) return;
+  __syncwarp();  // every lane's partial reads are done
+  if (lane == 0) {
+    const int t = tok / kPrefillQTile;
+    const size_t idx = (size_t)t * p.num_kv_heads + kvh;
+    const int readers = min(kPrefillQTile, p.total_q - t * kPrefillQTile);
+    if (atomicAdd(p.prefix_readers + idx, 1) == readers - 1) {
+      p.prefix_readers[idx] = 0;
+      p.prefix_done[idx] = 0;
+    }
+  }
+}
+
 // bf16 store of a lane's 16 dims (dims 8c .. 8c + 7 and 64 + 8c .. 64 + 8c + 7)
 __device__ __forceinline__ void store_row16(uint16_t* row, const float (&o)[16], int c) {
   uint4 lo, hi;
@@ -1219,7 +1261,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
   __syncthreads();
-  pdl_wait();
+  // Beside a prefix pass (prefix_done set) this launch starts once every CTA
+  // of the pass has passed its own wait, so the kernels before the pass are
+  // complete; waiting here would wait for the pass itself.
+  if (!p.prefix_done) pdl_wait();
   const int n_items = sm.n_items;
   if (n_items == 0) return;  // nothing covered (recorded above); no copy was issued
   // ---- block ids of the segment's pages; an id outside the pool (or a page
@@ -1522,7 +1567,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int head = kvh * kGroup + g;
     const size_t orow = (size_t)tok * p.num_q_heads + head;
     if (p0w == 0 && i1 - i0 == pages_r) {  // the whole row in this warp
-      if (p.prefix_o) lse2 = fold_prefix_wg(p, o, lse2, orow, c, lane);
+      if (p.prefix_o) {
+        if (prefix_ready(p, tok, kvh, lane)) lse2 = fold_prefix_wg(p, o, lse2, orow, c, lane);
+        prefix_read_done(p, tok, kvh, lane);
+      }
       store_row16(p.out + orow * kHeadDim, o, c);
       if (p.lse && c == 0) p.lse[orow] = lse2 * kLn2;
       continue;
@@ -1611,7 +1659,10 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
       for (int i = 0; i < 16; ++i) a4[i] *= winv;
       float l2 = wsum > 0.f ? Mx + log2f(wsum) : -INFINITY;
-      if (p.prefix_o) l2 = fold_prefix_wg(p, a4, l2, orow, c, lane);
+      if (p.prefix_o) {
+        if (prefix_ready(p, tok, kvh, lane)) l2 = fold_prefix_wg(p, a4, l2, orow, c, lane);
+        prefix_read_done(p, tok, kvh, lane);
+      }
       store_row16(p.out + orow * kHeadDim, a4, c);
       if (p.lse && c == 0) p.lse[orow] = l2 * kLn2;
     }

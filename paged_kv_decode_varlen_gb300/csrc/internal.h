@@ -45,6 +45,8 @@ constexpr int kDecodeMaxItemsPerCta = 64;
 // Host-planned decode launches cut each CTA's segment into this many warp
 // segments (one per warp); the plan's segment length is a multiple of it.
 constexpr int kDecodeWarps = 4;
+// Bytes of one (page, kv head) slab of K or V in bf16 (16 tokens x 128 dims).
+constexpr int kSlabBytesHost = 16 * 128 * 2;
 struct DecodePlan {
   int32_t n_rows;                     // decode rows of this launch
   int32_t seg;                        // pages per segment
@@ -94,6 +96,15 @@ struct DecodeParams {
   const float* prefix_lse;  // fp32 [prefix_n][total_q, Hq] their log2-domain lse
   int32_t prefix_n;         // partials to fold in (key chunks of the prefix; 1 once merged)
   int64_t prefix_rows;      // total_q * Hq: the stride between two partials' rows
+  // Prefix pass running at the same time as this launch (else null: its
+  // partials are complete before the launch).  prefix_done[t * Hkv + kvh]
+  // counts the key chunks of query tile t (kPrefillQTile tokens) written so
+  // far; a row's fold waits for prefix_n of them.  prefix_readers counts the
+  // folds done per (tile, kv head); the last of a tile's prefix_tile_rows(t)
+  // readers returns both counters to zero.
+  int* prefix_done;
+  int* prefix_readers;
+  int32_t total_q;
   uint16_t* out;         // bf16 [total_q, Hq, D]
   float* lse;            // [total_q, Hq] natural log, or null
   float* piece_o;        // fp32 [2 * grid * kDecodeWarps, 4, D]: a warp segment's (host plan) or a CTA's
@@ -170,6 +181,7 @@ struct PrefixParams {
   float* chunk_lse;
   float* prefix_o;
   float* prefix_lse;
+  int* done;  // per (query tile, kv head): chunks written (release), or null
   int* err;
 };
 

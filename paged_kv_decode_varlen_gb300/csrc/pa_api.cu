@@ -169,7 +169,8 @@ int step_grid(int32_t num_reqs, int32_t hkv, int32_t max_seq_len) {
 
 // Shared-prefix pass: the chunk count for a call and the workspace region
 // after the base layout: [prefix o (total_q x Hq x D fp32) | prefix lse |
-// chunk o (chunks x total_q x Hq x D) | chunk lse].  Chunks are sized so
+// chunk o (chunks x total_q x Hq x D) | chunk lse | 2 x query tiles x Hkv
+// int32 counters].  Chunks are sized so
 // that chunks x Hkv x query tiles gives about one CTA per SM; kPrefixCtaCap
 // bounds that for workspace sizing.
 constexpr int kPrefixCtaCap = 512;
@@ -184,7 +185,7 @@ int prefix_chunk_cap(int32_t total_q, int32_t hkv, int32_t prefix_pages) {
 }
 
 struct PrefixLayout {
-  size_t prefix_o, prefix_lse, chunk_o, chunk_lse, total;
+  size_t prefix_o, prefix_lse, chunk_o, chunk_lse, flags, total;
 };
 
 PrefixLayout prefix_layout(size_t base, int32_t total_q, int32_t num_q_heads, int32_t head_dim, int32_t prefix_pages) {
@@ -197,15 +198,45 @@ PrefixLayout prefix_layout(size_t base, int32_t total_q, int32_t num_q_heads, in
   w.prefix_lse = w.prefix_o + align256(rows * (size_t)std::max(head_dim, 0) * 4);
   w.chunk_o = w.prefix_lse + align256(rows * 4);
   w.chunk_lse = w.chunk_o + align256(chunk_rows * (size_t)std::max(head_dim, 0) * 4);
-  w.total = w.chunk_lse + align256(chunk_rows * 4);
+  // per (query tile, kv head): chunks written, then folds done (a pass that
+  // runs beside the decode launch); zero between calls
+  w.flags = w.chunk_lse + align256(chunk_rows * 4);
+  w.total = w.flags + align256((size_t)2 * prefix_qtiles(total_q) * hkv * 4);
   return w;
+}
+
+// Chunks of a shared-prefix pass that runs beside the decode launch, or 0
+// when running it first is faster.  The pass takes chunks x groups SMs (one
+// CTA each, groups = query tiles x kv heads) and the decode launch the other
+// SMs; both should end together.  Rates measured on GB300: a prefix CTA
+// takes ~1.05 us per 128-key tile after ~7 us of start-up and epilogue, and
+// ~11 us as the first kernel of the step (128 CTAs starting at once); a
+// decode SM streams ~46 GB/s after ~7 us of start-up and row ends.
+// decode_slabs counts (page, kv head) slabs of 8 KiB.
+int concurrent_prefix_chunks(int64_t key_tiles, int64_t groups, int64_t decode_slabs, int chunk_cap) {
+  const int sms = sm_count();
+  const double decode_bytes = (double)decode_slabs * 2 * pa::kSlabBytesHost;
+  auto decode_us = [&](int64_t free_sms) { return 7.0 + decode_bytes / ((double)free_sms * 46e3); };
+  const int64_t serial_chunks = std::min<int64_t>(chunk_cap, std::max<int64_t>(1, (sms + groups - 1) / groups));
+  const double serial = 11.0 + (double)((key_tiles + serial_chunks - 1) / serial_chunks) * 1.05 + decode_us(sms);
+  double best = serial;
+  int best_chunks = 0;
+  for (int ch = 1; ch <= chunk_cap && ch * groups <= sms / 2; ++ch) {
+    const double prefix = 7.0 + (double)((key_tiles + ch - 1) / ch) * 1.05;
+    const double t = std::max(prefix, decode_us(sms - ch * groups));
+    if (t < best) {
+      best = t;
+      best_chunks = ch;
+    }
+  }
+  return best_chunks;
 }
 
 // Plan one persistent decode launch over decode rows rows[0..n): fills
 // plan, returns the grid size (0 when there is nothing to do, -1 when no
 // valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
 int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
-                int page_offset, int num_kv_heads, int gcap, pa::DecodePlan& plan) {
+                int page_offset, int num_kv_heads, int gcap, int slots, pa::DecodePlan& plan) {
   std::vector<int32_t> pages(n);
   int64_t total = 0;  // pages of one kv head's stream
   int32_t longest = 0;
@@ -224,12 +255,11 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
   if (seg_cap < 1) return -1;
   const int forced = g_forced_ctas.load();
   int64_t nseg = forced > 0 ? (forced + num_kv_heads - 1) / num_kv_heads
-                            : std::min<int64_t>((int64_t)sm_count() * kDecodeCtasPerSm / num_kv_heads,
-                                                (total + min_seg - 1) / min_seg);
+                            : std::min<int64_t>(std::max(slots / num_kv_heads, 1), (total + min_seg - 1) / min_seg);
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, seg_cap));
   // a segment holds at most kDecodeMaxPagesPerCta pages; when that forces more
   // segments than one wave has slots, use whole waves so no wave runs part-empty
-  const int64_t wave = std::max<int64_t>(1, (int64_t)sm_count() * kDecodeCtasPerSm / num_kv_heads);
+  const int64_t wave = std::max<int64_t>(1, slots / num_kv_heads);
   const int64_t need = (total + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta;
   if (forced <= 0 && need > nseg) nseg = std::min<int64_t>((need + wave - 1) / wave * wave, seg_cap);
   int64_t seg = (total + nseg - 1) / nseg;
@@ -437,6 +467,16 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
   const float* dec_prefix_o = prefix_o;
   const float* dec_prefix_lse = prefix_lse;
   int32_t dec_prefix_n = 1;
+  // A decode-only batch (one decode launch, bf16 pages) may run the prefix
+  // pass beside its decode launch: the pass on a few SMs, the decode CTAs on
+  // the others, each row's fold waiting for its query tile's prefix chunks.
+  const bool decode_only = P > 0 && tiles.empty() && !decode_rows.empty() && !q8 &&
+                           decode_rows.size() <= (size_t)pa::kPlanMaxRows && g_forced_ctas.load() <= 0;
+  int64_t decode_pages_all = 0;  // pages of every decode row's own part (one kv head)
+  if (decode_only)
+    for (int32_t r : decode_rows) decode_pages_all += pages_of(seq_lens_host[r]) - P;
+  bool concurrent = false;
+  int decode_slots = sm_count() * kDecodeCtasPerSm;
   if (P > 0) {
     pa::PrefixParams xp;
     xp.q = static_cast<const uint16_t*>(q);
@@ -452,11 +492,21 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     xp.prefix_keys = P * pa::kPage;
     // about one CTA per SM over chunks x kv heads x query tiles
     const int64_t groups = prefix_qtiles(total_q) * num_kv_heads;
-    int n_chunks = (int)std::min<int64_t>(prefix_chunk_cap(total_q, num_kv_heads, P),
-                                          std::max<int64_t>(1, (sm_count() + groups - 1) / groups));
+    const int chunk_cap = prefix_chunk_cap(total_q, num_kv_heads, P);
+    int n_chunks = (int)std::min<int64_t>(chunk_cap, std::max<int64_t>(1, (sm_count() + groups - 1) / groups));
     const int64_t key_tiles = ((int64_t)xp.prefix_keys + kPrefixKeyTile - 1) / kPrefixKeyTile;
+    if (decode_only) {
+      // or beside the decode launch, when the pass is long enough to hide
+      const int conc = concurrent_prefix_chunks(key_tiles, groups, decode_pages_all * num_kv_heads, chunk_cap);
+      if (conc > 0) {
+        n_chunks = conc;
+        concurrent = true;
+      }
+    }
     xp.chunk_keys = (int32_t)((key_tiles + n_chunks - 1) / n_chunks * kPrefixKeyTile);
     n_chunks = (int)((xp.prefix_keys + xp.chunk_keys - 1) / xp.chunk_keys);
+    if (concurrent) decode_slots = std::max(1, sm_count() - (int)(n_chunks * groups)) * kDecodeCtasPerSm;
+    xp.done = concurrent ? reinterpret_cast<int*>(ws + pl.flags) : nullptr;
     xp.scale_log2 = scale_log2;
     xp.chunk_o = reinterpret_cast<float*>(ws + pl.chunk_o);
     xp.chunk_lse = reinterpret_cast<float*>(ws + pl.chunk_lse);
@@ -529,6 +579,10 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     dp.prefix_lse = dec_prefix_lse;
     dp.prefix_n = dec_prefix_n;
     dp.prefix_rows = (int64_t)total_q * num_q_heads;
+    dp.prefix_done = concurrent ? reinterpret_cast<int*>(ws + pl.flags) : nullptr;
+    dp.prefix_readers = concurrent ? reinterpret_cast<int*>(ws + pl.flags) + prefix_qtiles(total_q) * num_kv_heads
+                                   : nullptr;
+    dp.total_q = total_q;
     dp.out = static_cast<uint16_t*>(out);
     dp.lse = lse;
     dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
@@ -541,12 +595,13 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     // parameters); launches on one stream run in order and reuse the slots
     for (size_t d0 = 0; d0 < decode_rows.size(); d0 += pa::kPlanMaxRows) {
       const int n = (int)std::min(decode_rows.size() - d0, (size_t)pa::kPlanMaxRows);
-      // after the prefix pass or the prefill tiles, the decode CTAs go in
-      // plain stream order: resident early, waiting on the tile kernel's
-      // tail, they made the step 1-2 us longer, not shorter
-      const bool overlap = d0 > 0 || (P == 0 && tiles.empty());
+      // after a prefix pass that ends before it, or after the prefill tiles,
+      // the decode CTAs go in plain stream order: resident early, waiting on
+      // the tile kernel's tail, they made the step 1-2 us longer, not shorter.
+      // Beside a concurrent prefix pass they start as soon as it has.
+      const bool overlap = d0 > 0 || (P == 0 && tiles.empty()) || concurrent;
       const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
-                                   plan);
+                                   decode_slots, plan);
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
       const bool diag = !q8 && g_decode_fault.load() != 0;

@@ -474,8 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // log2 lse) for prefix_merge_kernel; with a single chunk it writes the
 // prefix partial itself.
 __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams p, const __grid_constant__ TcMaps maps) {
-  pdl_launch_dependents();
+  // the wait comes first: a decode launch that runs beside this pass (done
+  // != null) starts once every CTA here has released it, and so after the
+  // kernels before this one have completed
   pdl_wait();
+  pdl_launch_dependents();
   TcJob job;
   job.tok0 = blockIdx.z * kTok;
   job.nq = min(kTok, p.total_q - job.tok0);
@@ -484,7 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
   job.k_lo = blockIdx.x * p.chunk_keys;
   job.k_hi = min(p.prefix_keys, job.k_lo + p.chunk_keys);
   job.table = p.block_tables + (size_t)p.table_row * p.max_blocks_per_req;
-  if (job.nq <= 0 || job.k_hi <= job.k_lo) return;  // not planned on the host
+  int* done = p.done ? p.done + (size_t)blockIdx.z * p.num_kv_heads + blockIdx.y : nullptr;
+  if (job.nq <= 0 || job.k_hi <= job.k_lo) {  // not planned on the host
+    if (done && threadIdx.x == 0) {
+      record_error(p.err, PA_ERR_DEVICE_INDEX);
+      red_add_release_gpu(done, 1);  // a waiting fold gives up no later than its bound
+    }
+    return;
+  }
   const bool direct = gridDim.x == 1;
   float* dst_o = direct ? p.prefix_o : p.chunk_o + (size_t)blockIdx.x * p.total_q * p.num_q_heads * kHeadDim;
   float* dst_lse = direct ? p.prefix_lse : p.chunk_lse + (size_t)blockIdx.x * p.total_q * p.num_q_heads;
@@ -514,6 +524,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
               *reinterpret_cast<const float4*>(stg + row * 512 + ((c ^ (row & 31)) << 4));
         }
       });
+  // every store of the partial precedes run_tile's closing CTA barrier; the
+  // release publishes them to the folds that acquire the count (also after
+  // a recorded timeout, so no fold waits for a chunk that will not come)
+  if (done && threadIdx.x == 0) red_add_release_gpu(done, 1);
 }
 
 // Merge of the prefix pass's key-chunk partials: one warp per (query token,

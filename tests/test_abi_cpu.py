@@ -120,19 +120,21 @@ def test_shared_prefix_workspace_size():
     assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 0) == base
     # + prefix partial (16 x 32 rows of 128 fp32) + its lse
     # + 48 key-chunk partials (one per 128-key tile; the 512-CTA bound / 8 kv heads is larger)
+    # + two int32 counters per (query tile, kv head), in 256-byte units
     rows = 16 * 32
+    flags = lambda qtiles: (2 * qtiles * 8 * 4 + 255) // 256 * 256
     assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 384) == \
-        base + rows * 512 + rows * 4 + 48 * rows * 512 + 48 * rows * 4
+        base + rows * 512 + rows * 4 + 48 * rows * 512 + 48 * rows * 4 + flags(1)
     # a 5-page prefix is one 128-key tile: one chunk, no chunk partials
-    assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 5) == base + rows * 512 + rows * 4
+    assert b.pa_shared_prefix_workspace_size(16, 16, 32, 128, 8447, 5) == base + rows * 512 + rows * 4 + flags(1)
     # 64 query tiles of 32 tokens x 8 kv heads reach the CTA bound: one chunk
     base2 = b.pa_attention_workspace_size(4, 2048, 32, 128, 3000)
     assert b.pa_shared_prefix_workspace_size(4, 2048, 32, 128, 3000, 96) == \
-        base2 + 2048 * 32 * 512 + 2048 * 32 * 4
+        base2 + 2048 * 32 * 512 + 2048 * 32 * 4 + flags(64)
     # 32 query tiles x 8 kv heads: two chunks
     base3 = b.pa_attention_workspace_size(4, 1024, 32, 128, 3000)
     assert b.pa_shared_prefix_workspace_size(4, 1024, 32, 128, 3000, 96) == \
-        base3 + 3 * (1024 * 32 * 512 + 1024 * 32 * 4)
+        base3 + 3 * (1024 * 32 * 512 + 1024 * 32 * 4) + flags(32)
     assert b.pa_shared_prefix_workspace_size(4, 4, 32, 128, 100, -1) == 0
 
 
