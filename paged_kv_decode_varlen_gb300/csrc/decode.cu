@@ -1056,67 +1056,89 @@ static_assert(offsetof(WgSmem<kSlabBytes>, v) % 128 == 0 && offsetof(WgSmem<kQ8S
               "bulk copies land on 16-byte boundaries");
 static_assert(3 * (sizeof(WgSmem<kSlabBytes>) + 1024) <= 228 * 1024, "three decode CTAs per SM");
 
-// One head per 8-lane group (head g = lane >> 3), 16 dims per lane (dims
-// 8c .. 8c + 7 and 64 + 8c .. 64 + 8c + 7): folds the shared-prefix
-// partials of output row orow into the normalised partial o with log2 lse
-// lse2 by log-sum-exp; returns the merged lse.  The 8 lanes of a group read
-// the partials' lse in parallel, then every partial load is in flight at once.
-__device__ __forceinline__ float fold_prefix_wg(const DecodeParams& p, float (&o)[16], float lse2, size_t orow,
-                                                int c, int lane) {
-  const int n = p.prefix_n;
-  const int gbase = lane & ~7;
-  float M = lse2;
-  for (int c0 = 0; c0 < n; c0 += 8)
-    if (c0 + c < n) M = fmaxf(M, p.prefix_lse[(size_t)(c0 + c) * p.prefix_rows + orow]);
-#pragma unroll
-  for (int s = 4; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-  if (M == -INFINITY) return -INFINITY;
-  const float wo = exp2f(lse2 - M);  // own part (-inf -> 0)
-  float wsum = wo;
+// Online log-sum-exp merge of normalised partials (log2-domain lse) for one
+// head per 8-lane group (head g = lane >> 3), 16 dims per lane (dims
+// 8c .. 8c + 7 and 64 + 8c .. 64 + 8c + 7): m is the running max, w the sum
+// of weights relative to it and a the weighted sum of the partials.
+struct LseAcc {
+  float m, w;
   float a[16];
+};
+
+__device__ __forceinline__ void lse_acc_init(LseAcc& s, const float (&o)[16], float lse2) {
+  s.m = lse2;
+  s.w = lse2 == -INFINITY ? 0.f : 1.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) a[i] = o[i] * wo;
-  for (int c0 = 0; c0 < n; c0 += 8) {
-    const int nc = min(8, n - c0);
-    const float w = c < nc ? exp2f(p.prefix_lse[(size_t)(c0 + c) * p.prefix_rows + orow] - M) : 0.f;
-    float ws = w;
+  for (int i = 0; i < 16; ++i) s.a[i] = lse2 == -INFINITY ? 0.f : o[i];
+}
+
+// Adds up to 4 partials: row(u) points at partial u's 128 fp32 of this head,
+// lse_at(u) at its lse; every load of the batch is issued before any is used.
+template <bool kL2Only, class Row, class Lse>
+__device__ __forceinline__ void lse_acc_batch(LseAcc& s, int nb, int c, Row&& row, Lse&& lse_at) {
+  float l[4];
+  float4 y[4][4];
 #pragma unroll
-    for (int s = 4; s > 0; s >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s);
-    wsum += ws;
-    // four partials' loads in flight at a time
-#pragma unroll
-    for (int i0 = 0; i0 < 8; i0 += 4) {
-      if (i0 >= nc) break;
-      float4 y[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (i0 + u < nc) {
-          const float* yr = p.prefix_o + ((size_t)(c0 + i0 + u) * p.prefix_rows + orow) * kHeadDim;
-          y[u][0] = *reinterpret_cast<const float4*>(yr + 8 * c);
-          y[u][1] = *reinterpret_cast<const float4*>(yr + 8 * c + 4);
-          y[u][2] = *reinterpret_cast<const float4*>(yr + 64 + 8 * c);
-          y[u][3] = *reinterpret_cast<const float4*>(yr + 64 + 8 * c + 4);
-        } else {
-          y[u][0] = y[u][1] = y[u][2] = y[u][3] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+  for (int u = 0; u < 4; ++u) {
+    if (u < nb) {
+      const float* yr = row(u);
+      const float* lp = lse_at(u);
+      if constexpr (kL2Only) {
+        l[u] = __ldcg(lp);
+        y[u][0] = __ldcg(reinterpret_cast<const float4*>(yr + 8 * c));
+        y[u][1] = __ldcg(reinterpret_cast<const float4*>(yr + 8 * c + 4));
+        y[u][2] = __ldcg(reinterpret_cast<const float4*>(yr + 64 + 8 * c));
+        y[u][3] = __ldcg(reinterpret_cast<const float4*>(yr + 64 + 8 * c + 4));
+      } else {
+        l[u] = *lp;
+        y[u][0] = *reinterpret_cast<const float4*>(yr + 8 * c);
+        y[u][1] = *reinterpret_cast<const float4*>(yr + 8 * c + 4);
+        y[u][2] = *reinterpret_cast<const float4*>(yr + 64 + 8 * c);
+        y[u][3] = *reinterpret_cast<const float4*>(yr + 64 + 8 * c + 4);
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float wi = __shfl_sync(0xffffffffu, w, gbase + i0 + u);  // 0 past nc
-#pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          a[4 * v4 + 0] = fmaf(wi, y[u][v4].x, a[4 * v4 + 0]);
-          a[4 * v4 + 1] = fmaf(wi, y[u][v4].y, a[4 * v4 + 1]);
-          a[4 * v4 + 2] = fmaf(wi, y[u][v4].z, a[4 * v4 + 2]);
-          a[4 * v4 + 3] = fmaf(wi, y[u][v4].w, a[4 * v4 + 3]);
-        }
-      }
+    } else {
+      l[u] = -INFINITY;
+      y[u][0] = y[u][1] = y[u][2] = y[u][3] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  const float inv = 1.f / wsum;
+  const float mb = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+  const float mn = fmaxf(s.m, mb);
+  if (mn == -INFINITY) return;  // every partial so far is empty
+  const float sc = fast_exp2(s.m - mn);  // s.m = -inf -> 0
+  s.w *= sc;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i] = a[i] * inv;
-  return M + log2f(wsum);
+  for (int i = 0; i < 16; ++i) s.a[i] *= sc;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float wu = fast_exp2(l[u] - mn);  // -inf -> 0
+    s.w += wu;
+#pragma unroll
+    for (int v4 = 0; v4 < 4; ++v4) {
+      s.a[4 * v4 + 0] = fmaf(wu, y[u][v4].x, s.a[4 * v4 + 0]);
+      s.a[4 * v4 + 1] = fmaf(wu, y[u][v4].y, s.a[4 * v4 + 1]);
+      s.a[4 * v4 + 2] = fmaf(wu, y[u][v4].z, s.a[4 * v4 + 2]);
+      s.a[4 * v4 + 3] = fmaf(wu, y[u][v4].w, s.a[4 * v4 + 3]);
+    }
+  }
+  s.m = mn;
+}
+
+// Normalises the merged partial into o; returns its log2 lse.
+__device__ __forceinline__ float lse_acc_done(const LseAcc& s, float (&o)[16]) {
+  const float inv = s.w > 0.f ? 1.f / s.w : 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = s.a[i] * inv;
+  return s.w > 0.f ? s.m + log2f(s.w) : -INFINITY;
+}
+
+// Folds the shared-prefix partials of output row orow (p.prefix_n key-chunk
+// partials, or the merged one) into the merge state, four at a time.
+__device__ __forceinline__ void lse_acc_prefix(LseAcc& s, const DecodeParams& p, size_t orow, int c) {
+  for (int c0 = 0; c0 < p.prefix_n; c0 += 4)
+    lse_acc_batch<false>(
+        s, min(4, p.prefix_n - c0), c,
+        [&](int u) { return p.prefix_o + ((size_t)(c0 + u) * p.prefix_rows + orow) * kHeadDim; },
+        [&](int u) { return p.prefix_lse + (size_t)(c0 + u) * p.prefix_rows + orow; });
 }
 
 // A prefix pass running beside the decode launch (p.prefix_done set): wait,
@@ -1568,7 +1590,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     const size_t orow = (size_t)tok * p.num_q_heads + head;
     if (p0w == 0 && i1 - i0 == pages_r) {  // the whole row in this warp
       if (p.prefix_o) {
-        if (prefix_ready(p, tok, kvh, lane)) lse2 = fold_prefix_wg(p, o, lse2, orow, c, lane);
+        if (prefix_ready(p, tok, kvh, lane)) {
+          LseAcc acc;
+          lse_acc_init(acc, o, lse2);
+          lse_acc_prefix(acc, p, orow, c);
+          lse2 = lse_acc_done(acc, o);
+        }
         prefix_read_done(p, tok, kvh, lane);
       }
       store_row16(p.out + orow * kHeadDim, o, c);
@@ -1598,71 +1625,29 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     __syncwarp();  // lane 0's acquire orders the piece reads below
     if (!__shfl_sync(0xffffffffu, last, 0)) continue;
-    // the last piece to finish: merge all pieces of the row (8 lanes of a
-    // head read 8 pieces' lse in parallel, then every piece load is in flight)
+    // the last piece to finish: merge every piece of the row (and the
+    // prefix partials), four partials per batch with all their loads in flight
     {
       const int n_pc = b1 - b0 + 1;
-      const int gbase = lane & ~7;
       auto piece_slot = [&](int bb) {
         const int jj = (bb == b0 && b0 * sw < A) ? 1 : 0;
         return ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
       };
-      float Mx = -INFINITY;
-      for (int c0 = 0; c0 < n_pc; c0 += 8)
-        if (c0 + c < n_pc) Mx = fmaxf(Mx, __ldcg(p.piece_lse + piece_slot(b0 + c0 + c)));
+      LseAcc acc;
+      acc.m = -INFINITY;
+      acc.w = 0.f;
 #pragma unroll
-      for (int s2 = 4; s2 > 0; s2 >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, s2));
-      float wsum = 0.f;
-      float a4[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) a4[i] = 0.f;
-      if (Mx != -INFINITY) {
-        for (int c0 = 0; c0 < n_pc; c0 += 8) {
-          const int nc = min(8, n_pc - c0);
-          const float w = c < nc ? fast_exp2(__ldcg(p.piece_lse + piece_slot(b0 + c0 + c)) - Mx) : 0.f;
-          float ws = w;
-#pragma unroll
-          for (int s2 = 4; s2 > 0; s2 >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s2);
-          wsum += ws;
-          // four pieces' loads in flight at a time
-#pragma unroll
-          for (int i0 = 0; i0 < 8; i0 += 4) {
-            if (i0 >= nc) break;
-            float4 y[4][4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (i0 + u < nc) {
-                const float* yr = p.piece_o + piece_slot(b0 + c0 + i0 + u) * kHeadDim;
-                y[u][0] = __ldcg(reinterpret_cast<const float4*>(yr + 8 * c));
-                y[u][1] = __ldcg(reinterpret_cast<const float4*>(yr + 8 * c + 4));
-                y[u][2] = __ldcg(reinterpret_cast<const float4*>(yr + 64 + 8 * c));
-                y[u][3] = __ldcg(reinterpret_cast<const float4*>(yr + 64 + 8 * c + 4));
-              } else {
-                y[u][0] = y[u][1] = y[u][2] = y[u][3] = make_float4(0.f, 0.f, 0.f, 0.f);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float wi = __shfl_sync(0xffffffffu, w, gbase + i0 + u);  // 0 past nc
-#pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                a4[4 * v4 + 0] = fmaf(wi, y[u][v4].x, a4[4 * v4 + 0]);
-                a4[4 * v4 + 1] = fmaf(wi, y[u][v4].y, a4[4 * v4 + 1]);
-                a4[4 * v4 + 2] = fmaf(wi, y[u][v4].z, a4[4 * v4 + 2]);
-                a4[4 * v4 + 3] = fmaf(wi, y[u][v4].w, a4[4 * v4 + 3]);
-              }
-            }
-          }
-        }
-      }
-      const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) a4[i] *= winv;
-      float l2 = wsum > 0.f ? Mx + log2f(wsum) : -INFINITY;
+      for (int i = 0; i < 16; ++i) acc.a[i] = 0.f;
+      for (int c0 = 0; c0 < n_pc; c0 += 4)
+        lse_acc_batch<true>(
+            acc, min(4, n_pc - c0), c, [&](int u) { return p.piece_o + piece_slot(b0 + c0 + u) * kHeadDim; },
+            [&](int u) { return p.piece_lse + piece_slot(b0 + c0 + u); });
       if (p.prefix_o) {
-        if (prefix_ready(p, tok, kvh, lane)) l2 = fold_prefix_wg(p, a4, l2, orow, c, lane);
+        if (prefix_ready(p, tok, kvh, lane)) lse_acc_prefix(acc, p, orow, c);
         prefix_read_done(p, tok, kvh, lane);
       }
+      float a4[16];
+      const float l2 = lse_acc_done(acc, a4);
       store_row16(p.out + orow * kHeadDim, a4, c);
       if (p.lse && c == 0) p.lse[orow] = l2 * kLn2;
     }
