@@ -1668,12 +1668,15 @@ __global__ void __launch_bounds__(kThreads, 3)
 
 std::atomic<bool> g_decode_attr_set[4][kMaxDevices];
 
+std::atomic<bool> g_decode_cta_attr_set[3][kMaxDevices];
+
 template <bool kQ8, bool kStep, bool kDiag = false>
 cudaError_t launch_decode_as(const DecodeParams& p, const typename PlanOf<kStep>::type& plan, int grid,
                              bool overlap, cudaStream_t stream) {
   constexpr size_t kSmem = sizeof(DecodeSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
+  constexpr int kVariant = kStep ? 2 : (kQ8 ? 1 : 0);
   const cudaError_t e = set_smem_limit_once((const void*)decode_kernel<kQ8, kStep, kDiag>, (int)kSmem,
-                                            g_decode_attr_set[2]);
+                                            g_decode_cta_attr_set[kVariant]);
   if (e != cudaSuccess) return e;
   return launch_maybe_pdl(overlap, decode_kernel<kQ8, kStep, kDiag>, dim3(grid), dim3(kThreads), kSmem, stream, p,
                           plan);
@@ -1693,7 +1696,10 @@ cudaError_t launch_decode_wg(const DecodeParams& p, const DecodePlan& plan, int 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
-                          bool diag, cudaStream_t stream) {
+                          bool diag, bool cta_granular, cudaStream_t stream) {
+  if (cta_granular)  // short segments: the CTA-granular kernel (bf16 or q8_0 pages)
+    return q8 ? launch_decode_as<true, false>(p, plan, grid, overlap, stream)
+              : launch_decode_as<false, false>(p, plan, grid, overlap, stream);
   if (q8) return launch_decode_wg<true, false>(p, plan, grid, overlap, stream);
   return diag ? launch_decode_wg<false, true>(p, plan, grid, overlap, stream)
               : launch_decode_wg<false, false>(p, plan, grid, overlap, stream);

@@ -45,6 +45,12 @@ constexpr int kDecodeMaxItemsPerCta = 64;
 // Host-planned decode launches cut each CTA's segment into this many warp
 // segments (one per warp); the plan's segment length is a multiple of it.
 constexpr int kDecodeWarps = 4;
+// Host-planned launches whose warp segments would hold fewer pages than this
+// run the CTA-granular kernel: a row cut into many short warp pieces costs
+// its last piece a long merge, and few pages per warp leave its 2-page ring
+// latency-bound (measured: one 2048-token row per layer 12.6 us CTA-granular
+// against 18.6 us warp-granular; 32 rows 58.2 against 54.9 us).
+constexpr int kMinWarpSegPages = 8;
 // Bytes of one (page, kv head) slab of K or V in bf16 (16 tokens x 128 dims).
 constexpr int kSlabBytesHost = 16 * 128 * 2;
 struct DecodePlan {
@@ -220,9 +226,11 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_kv_append_q8(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 // overlap: programmatic launch after the stream's previous kernel; diag:
-// the timeout-path diagnostic instantiation (bf16 pages only)
+// the timeout-path diagnostic instantiation (bf16 pages, warp-granular);
+// cta_granular: the kernel whose 4 warps read every page of the CTA's
+// segment (no prefix pass beside it), for plans with short segments
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
-                          bool diag, cudaStream_t stream);
+                          bool diag, bool cta_granular, cudaStream_t stream);
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
                            cudaStream_t stream);

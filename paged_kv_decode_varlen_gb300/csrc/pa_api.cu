@@ -236,7 +236,7 @@ int concurrent_prefix_chunks(int64_t key_tiles, int64_t groups, int64_t decode_s
 // plan, returns the grid size (0 when there is nothing to do, -1 when no
 // valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
 int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
-                int page_offset, int num_kv_heads, int gcap, int slots, pa::DecodePlan& plan) {
+                int page_offset, int num_kv_heads, int gcap, int slots, int unit, pa::DecodePlan& plan) {
   std::vector<int32_t> pages(n);
   int64_t total = 0;  // pages of one kv head's stream
   int32_t longest = 0;
@@ -264,7 +264,7 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
   if (forced <= 0 && need > nseg) nseg = std::min<int64_t>((need + wave - 1) / wave * wave, seg_cap);
   int64_t seg = (total + nseg - 1) / nseg;
   seg = std::max<int64_t>(seg, (total + seg_cap - 1) / seg_cap);
-  seg = (seg + pa::kDecodeWarps - 1) / pa::kDecodeWarps * pa::kDecodeWarps;  // whole warp segments
+  seg = (seg + unit - 1) / unit * unit;  // whole warp segments for the warp-granular kernel (unit 4)
   seg = std::min<int64_t>(seg, pa::kDecodeMaxPagesPerCta);  // more segments if one would be too long
   static_assert(pa::kDecodeMaxPagesPerCta % pa::kDecodeWarps == 0, "segments hold whole warp segments");
   for (;;) {
@@ -296,9 +296,9 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
       }
       return ns * num_kv_heads;
     }
-    if (seg <= pa::kDecodeWarps) return -1;
+    if (seg <= unit) return -1;
     // shorter segments touch fewer rows
-    seg = ((seg + 1) / 2 + pa::kDecodeWarps - 1) / pa::kDecodeWarps * pa::kDecodeWarps;
+    seg = ((seg + 1) / 2 + unit - 1) / unit * unit;
   }
 }
 
@@ -600,13 +600,22 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
       // the tile kernel's tail, they made the step 1-2 us longer, not shorter.
       // Beside a concurrent prefix pass they start as soon as it has.
       const bool overlap = d0 > 0 || (P == 0 && tiles.empty()) || concurrent;
-      const int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
-                                   decode_slots, plan);
+      // segments of whole pages for the CTA-granular kernel; when they are
+      // long enough for four warp segments of kMinWarpSegPages (or a prefix
+      // pass runs beside the launch, or the timeout diagnostic is on), planned
+      // again in whole warp segments for the warp-granular kernel
+      const bool diag = !q8 && g_decode_fault.load() != 0;
+      int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
+                             decode_slots, 1, plan);
+      const bool cta_granular =
+          grid > 0 && !concurrent && !diag && plan.seg < pa::kDecodeWarps * pa::kMinWarpSegPages;
+      if (grid > 0 && !cta_granular)
+        grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
+                           decode_slots, pa::kDecodeWarps, plan);
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
-      const bool diag = !q8 && g_decode_fault.load() != 0;
       s = run_launch(PA_KERNEL_DECODE, "decode", stream,
-                     [&] { return pa::launch_decode(dp, plan, grid, q8, overlap, diag, stream); });
+                     [&] { return pa::launch_decode(dp, plan, grid, q8, overlap, diag, cta_granular, stream); });
       if (s != PA_OK) return s;
     }
   }
