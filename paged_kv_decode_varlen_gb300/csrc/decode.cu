@@ -301,7 +301,7 @@ __device__ __forceinline__ float fold_prefix(const DecodeParams& p, float4& o, f
 // the items win0 .. win0 + kDecodeMaxItemsPerCta - 1 of this CTA's segment
 // (all threads call it; it ends with a barrier).  Also writes the outputs of
 // padding rows (zero, lse -inf) and records rows outside the bounds.
-template <class Smem>
+template <int kUnit = 1, class Smem>
 __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& sm, int kvh, int sidx, int nseg_grid,
                             int win0) {
   constexpr int kRows = kPlanMaxRows / kThreads;  // rows per thread, consecutive
@@ -345,7 +345,8 @@ __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& s
   }
   int A = woff + incl - tsum;  // cost position of this thread's first row
   const int n_eff = max(1, min(nseg_grid, (total + kStepMinSegCost - 1) / kStepMinSegCost));
-  const int C = max(1, (total + n_eff - 1) / n_eff);
+  // segment length in stream units, whole warp segments for the warp-granular kernel (kUnit 4)
+  const int C = (max(1, (total + n_eff - 1) / n_eff) + kUnit - 1) / kUnit * kUnit;
   const int S = sidx * C, E = min(S + C, total);
   // this segment's part of each row: (first page p0, pages nn), packed with
   // an item count for the second scan: (pages << 16) | 1
@@ -1048,6 +1049,11 @@ struct __align__(128) WgSmem {
   int q_issued[kWarps];
   int n_items;
   int abort_flag;
+  // decode step (self-planned): see step_window
+  int scan[kWarps];
+  int n_items_all;
+  int seg_cost;
+  int seg_pages;
 };
 
 static_assert(offsetof(WgSmem<kSlabBytes>, v) % 128 == 0 && offsetof(WgSmem<kQ8SlabBytes>, v) % 16 == 0 &&
@@ -1203,25 +1209,29 @@ __device__ __forceinline__ void store_row16(uint16_t* row, const float (&o)[16],
 // issuing that page's copies, so the wait on it runs out; every wait of this
 // instantiation gives up after 1 ms instead of kWaitLimitNs.  No copy is
 // dropped anywhere else, and nothing is read out of bounds.
-template <bool kQ8, bool kDiag>
+template <bool kQ8, bool kDiag, bool kStep = false>
 __global__ void __launch_bounds__(kThreads, 3)
-    decode_wg_kernel(const DecodeParams p, const __grid_constant__ DecodePlan plan) {
+    decode_wg_kernel(const DecodeParams p, const __grid_constant__ typename PlanOf<kStep>::type plan) {
   static_assert(!(kDiag && kQ8), "the diagnostic instantiation reads bf16 pages");
+  static_assert(!(kStep && (kQ8 || kDiag)), "the decode step serves bf16 pages");
+  // the fixed cost of a row in the stream's units (the host plan cuts in
+  // pages, with no fixed cost)
+  constexpr int kAlpha = kStep ? kStepItemCost : 0;
   constexpr unsigned long long kLimit = kDiag ? 1000000ull : kWaitLimitNs;
   constexpr int kSlab = kQ8 ? kQ8SlabBytes : kSlabBytes;
   using Smem = WgSmem<kSlab>;
   // q of each item by a bulk copy into the warp's shared-memory slot, issued
   // an item ahead (bf16 pages); q8_0 pages read q from global memory
   constexpr bool kQSmem = !kQ8;
+  // the self-planned step reads lengths and tables that earlier kernels may
+  // write: it waits for them before anything else
+  if constexpr (kStep) pdl_wait();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.num_kv_heads;
   const int kvh = b % Hkv, sidx = b / Hkv;
-  const int S0 = sidx * plan.seg;
-  const int npg = min(plan.total, S0 + plan.seg) - S0;  // pages of this CTA's segment
-  if (npg <= 0) return;
   if (tid == 0) {
     for (int w = 0; w < kWarps; ++w) {
       for (int s = 0; s < kWgStages; ++s) {
@@ -1234,59 +1244,73 @@ __global__ void __launch_bounds__(kThreads, 3)
     sm.abort_flag = 0;
     fence_mbar_init();
   }
-  const int n_items_all = plan.n_rows;
-  // ---- item table of the CTA's segment (warp 0), 32 items per round; it
-  // comes from the kernel parameters alone, so it is built before the wait
-  // for the previous kernel
-  if (warp == 0) {
-    int base_q = 0, n_it = 0;
-    for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
-      const int item = plan.first_row[sidx] + k0 + lane;
-      const bool exists = item < n_items_all;
-      int r = 0, L = 0, size = 0, tok = 0;
-      const int p0 = (k0 + lane == 0) ? plan.first_page[sidx] : 0;
-      if (exists) {
-        r = plan.rows[item];
-        L = plan.seq[item];
-        tok = plan.tok[item];
-        size = max((L + kPage - 1) / kPage - p.page_offset - p0, 0);
-      }
-      int incl = size;
+  int seg_units;  // segment length in stream units (pages, or pages plus row costs)
+  if constexpr (kStep) {
+    // the CTA plans its own segment from the device seq_lens; a segment with
+    // more than kDecodeMaxItemsPerCta rows cannot occur for the launches the
+    // host sends here (it checks the bound) and is recorded
+    step_window<kWarps>(p, plan, sm, kvh, sidx, (int)gridDim.x / Hkv, 0);
+    seg_units = sm.seg_cost;
+    if (tid == 0 && sm.n_items_all > kDecodeMaxItemsPerCta) record_error(p.err, PA_ERR_DEVICE_INDEX);
+  } else {
+    const int S0 = sidx * plan.seg;
+    const int npg = min(plan.total, S0 + plan.seg) - S0;  // pages of this CTA's segment
+    if (npg <= 0) return;
+    seg_units = plan.seg;
+    const int n_items_all = plan.n_rows;
+    // ---- item table of the CTA's segment (warp 0), 32 items per round; it
+    // comes from the kernel parameters alone, so it is built before the wait
+    // for the previous kernel
+    if (warp == 0) {
+      int base_q = 0, n_it = 0;
+      for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
+        const int item = plan.first_row[sidx] + k0 + lane;
+        const bool exists = item < n_items_all;
+        int r = 0, L = 0, size = 0, tok = 0;
+        const int p0 = (k0 + lane == 0) ? plan.first_page[sidx] : 0;
+        if (exists) {
+          r = plan.rows[item];
+          L = plan.seq[item];
+          tok = plan.tok[item];
+          size = max((L + kPage - 1) / kPage - p.page_offset - p0, 0);
+        }
+        int incl = size;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int start = base_q + incl - size;
+        const bool in_seg = size > 0 && start < npg;
+        if (in_seg && k0 + lane < kDecodeMaxItemsPerCta) {
+          Item& it = sm.items[k0 + lane];
+          it.q_start = start;
+          it.n = min(size, npg - start);
+          it.p0 = p0;
+          it.r = r;
+          it.L = L;
+          it.tok = tok;
+          it.A = S0 + start - p0;  // stream position of the row's page 0
+          bulk_prefetch_l2(p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim,
+                           kGroup * kHeadDim * 2);
+        }
+        const unsigned covered = __ballot_sync(0xffffffffu, in_seg);
+        const int prefix = (~covered == 0u) ? 32 : (__ffs((int)~covered) - 1);
+        n_it = k0 + prefix;
+        base_q += __shfl_sync(0xffffffffu, incl, 31);
+        if (prefix < 32 || base_q >= npg) break;
       }
-      const int start = base_q + incl - size;
-      const bool in_seg = size > 0 && start < npg;
-      if (in_seg && k0 + lane < kDecodeMaxItemsPerCta) {
-        Item& it = sm.items[k0 + lane];
-        it.q_start = start;
-        it.n = min(size, npg - start);
-        it.p0 = p0;
-        it.r = r;
-        it.L = L;
-        it.tok = tok;
-        it.A = S0 + start - p0;  // stream position of the row's page 0
-        bulk_prefetch_l2(p.q + ((size_t)tok * p.num_q_heads + (size_t)kvh * kGroup) * kHeadDim,
-                         kGroup * kHeadDim * 2);
+      if (lane == 0) {
+        if (base_q < npg) record_error(p.err, PA_ERR_DEVICE_INDEX);  // metadata differ from the plan
+        sm.n_items = min(n_it, kDecodeMaxItemsPerCta);
       }
-      const unsigned covered = __ballot_sync(0xffffffffu, in_seg);
-      const int prefix = (~covered == 0u) ? 32 : (__ffs((int)~covered) - 1);
-      n_it = k0 + prefix;
-      base_q += __shfl_sync(0xffffffffu, incl, 31);
-      if (prefix < 32 || base_q >= npg) break;
     }
-    if (lane == 0) {
-      if (base_q < npg) record_error(p.err, PA_ERR_DEVICE_INDEX);  // metadata differ from the plan
-      sm.n_items = min(n_it, kDecodeMaxItemsPerCta);
-    }
+    __syncthreads();
+    // Beside a prefix pass (prefix_done set) this launch starts once every CTA
+    // of the pass has passed its own wait, so the kernels before the pass are
+    // complete; waiting here would wait for the pass itself.
+    if (!p.prefix_done) pdl_wait();
   }
-  __syncthreads();
-  // Beside a prefix pass (prefix_done set) this launch starts once every CTA
-  // of the pass has passed its own wait, so the kernels before the pass are
-  // complete; waiting here would wait for the pass itself.
-  if (!p.prefix_done) pdl_wait();
   const int n_items = sm.n_items;
   if (n_items == 0) return;  // nothing covered (recorded above); no copy was issued
   // ---- block ids of the segment's pages; an id outside the pool (or a page
@@ -1312,10 +1336,24 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   const bool ids_ok = __syncthreads_and(ok) != 0;
 
-  // ---- this warp's part of the segment: pages [a, e)
-  const int sw = plan.seg / kWarps;
-  const int a = warp * sw;
-  const int e = min(a + sw, n_cov);
+  // ---- this warp's part of the segment: stream units [cs, cs + sw), its
+  // pages [a, e) of the segment (with the host plan a unit is a page)
+  const int sw = seg_units / kWarps;
+  int a, e;
+  if constexpr (kStep) {
+    const int cs = sidx * seg_units + warp * sw, ce = cs + sw;
+    a = n_cov;
+    e = n_cov;
+    for (int kk = n_items - 1; kk >= 0; --kk) {  // the first page at or past cs, resp. ce
+      const Item& it = sm.items[kk];
+      const int u0 = it.A + kAlpha + it.p0;  // stream position of the item's first page
+      if (u0 + it.n > cs) a = it.q_start + max(0, cs - u0);
+      if (u0 + it.n > ce) e = it.q_start + max(0, ce - u0);
+    }
+  } else {
+    a = warp * sw;
+    e = min(a + sw, n_cov);
+  }
   if (a >= e) return;
   int k = 0;  // first item holding page a
   {
@@ -1348,6 +1386,27 @@ __global__ void __launch_bounds__(kThreads, 3)
     bulk_g2s(sm.qs[warp], p.q + qoff, kGroup * kHeadDim * 2, &sm.q_full[warp]);
     sm.q_issued[warp] += 1;
   };
+  if constexpr (kStep) {
+    // decode step: the warp that reads a row's last page stores the row's
+    // new token (position L - 1) for its kv head before any copy it issues;
+    // the proxy fence orders the stores before those bulk copies
+    for (int kk = k; kk < n_items; ++kk) {
+      const Item& it = sm.items[kk];
+      if (it.q_start >= e) break;
+      if (it.p0 + it.n != (it.L + kPage - 1) / kPage) continue;  // not the row's last page
+      const int qlast = it.q_start + it.n - 1;
+      if (qlast < a || qlast >= e) continue;  // another warp's page
+      const int pos = it.L - 1;
+      const int blk = p.block_tables[(size_t)it.r * p.max_blocks_per_req + pos / kPage];
+      if (blk < 0 || blk >= p.num_blocks) continue;  // recorded by the id check above
+      const size_t src = ((size_t)it.r * Hkv + kvh) * kHeadDim;
+      const size_t dst = (((size_t)blk * Hkv + kvh) * kPage + pos % kPage) * kHeadDim;
+      const uint4 x = reinterpret_cast<const uint4*>((lane < 16 ? p.k_new : p.v_new) + src)[lane & 15];
+      reinterpret_cast<uint4*>((lane < 16 ? p.k_store : p.v_store) + dst)[lane & 15] = x;
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+  }
   if (lane == 0) {
     if constexpr (kQSmem) issue_q(k);
     for (int q = a; q < min(e, a + kWgStages); ++q) issue(q);
@@ -1603,8 +1662,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       continue;
     }
     // the item is cut by warp-segment boundaries: publish this warp's partial
-    const int A = it.A;
-    const int b0 = A / sw, b1 = (A + pages_r - 1) / sw;  // warp segments holding the row's pages
+    const int A = it.A;  // stream position of the row's start; its pages start at A + kAlpha
+    const int b0 = (A + kAlpha) / sw, b1 = (A + kAlpha + pages_r - 1) / sw;  // warp segments holding them
     const int jslot = (k == k_first) ? 0 : 1;
     {
       const size_t slot = ((size_t)(gw * Hkv + kvh) * 2 + jslot) * kGroup + g;
@@ -1682,15 +1741,16 @@ cudaError_t launch_decode_as(const DecodeParams& p, const typename PlanOf<kStep>
                           plan);
 }
 
-template <bool kQ8, bool kDiag>
-cudaError_t launch_decode_wg(const DecodeParams& p, const DecodePlan& plan, int grid, bool overlap,
+template <bool kQ8, bool kDiag, bool kStep = false>
+cudaError_t launch_decode_wg(const DecodeParams& p, const typename PlanOf<kStep>::type& plan, int grid, bool overlap,
                              cudaStream_t stream) {
   constexpr size_t kSmem = sizeof(WgSmem<kQ8 ? kQ8SlabBytes : kSlabBytes>);
-  constexpr int kVariant = kDiag ? 3 : (kQ8 ? 1 : 0);
-  const cudaError_t e =
-      set_smem_limit_once((const void*)decode_wg_kernel<kQ8, kDiag>, (int)kSmem, g_decode_attr_set[kVariant]);
+  constexpr int kVariant = kStep ? 2 : kDiag ? 3 : (kQ8 ? 1 : 0);
+  const cudaError_t e = set_smem_limit_once((const void*)decode_wg_kernel<kQ8, kDiag, kStep>, (int)kSmem,
+                                            g_decode_attr_set[kVariant]);
   if (e != cudaSuccess) return e;
-  return launch_maybe_pdl(overlap, decode_wg_kernel<kQ8, kDiag>, dim3(grid), dim3(kThreads), kSmem, stream, p, plan);
+  return launch_maybe_pdl(overlap, decode_wg_kernel<kQ8, kDiag, kStep>, dim3(grid), dim3(kThreads), kSmem, stream,
+                          p, plan);
 }
 
 }  // namespace
@@ -1705,8 +1765,10 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int gri
               : launch_decode_wg<false, false>(p, plan, grid, overlap, stream);
 }
 
-cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream) {
-  return launch_decode_as<false, true>(p, plan, grid, true, stream);
+cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, bool warp_granular,
+                               cudaStream_t stream) {
+  return warp_granular ? launch_decode_wg<false, false, true>(p, plan, grid, true, stream)
+                       : launch_decode_as<false, true>(p, plan, grid, true, stream);
 }
 
 }  // namespace pa

@@ -231,7 +231,10 @@ cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 // segment (no prefix pass beside it), for plans with short segments
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
                           bool diag, bool cta_granular, cudaStream_t stream);
-cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, cudaStream_t stream);
+// warp_granular: the warp-granular kernel (no segment may hold more than
+// kDecodeMaxItemsPerCta rows), else the CTA-granular one (windows of rows)
+cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, bool warp_granular,
+                               cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
                            cudaStream_t stream);
 cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream);

@@ -167,6 +167,19 @@ int step_grid(int32_t num_reqs, int32_t hkv, int32_t max_seq_len) {
   return (int)(nseg * hkv);
 }
 
+// Decode step: whether every segment of the launch holds at most
+// kDecodeMaxItemsPerCta rows, for any lengths within the call's bounds (so the
+// warp-granular kernel, which plans one window, serves it).  A row costs at
+// least 1 + kStepItemCost units and a segment is at most C units, C bounded by
+// the largest total cost over the segments (or the minimum segment).
+bool step_one_window(int32_t num_reqs, int32_t hkv, int32_t max_seq_len, int grid) {
+  if (num_reqs <= pa::kDecodeMaxItemsPerCta) return true;
+  const int64_t nseg = std::max(1, grid / std::max(hkv, 1));
+  const int64_t total_max = (int64_t)num_reqs * (pages_of(max_seq_len) + pa::kStepItemCost);
+  const int64_t c_max = std::max<int64_t>(pa::kStepMinSegCost, (total_max + nseg - 1) / nseg) + pa::kDecodeWarps;
+  return c_max / (1 + pa::kStepItemCost) + 2 <= pa::kDecodeMaxItemsPerCta;
+}
+
 // Shared-prefix pass: the chunk count for a call and the workspace region
 // after the base layout: [prefix o (total_q x Hq x D fp32) | prefix lse |
 // chunk o (chunks x total_q x Hq x D) | chunk lse | 2 x query tiles x Hkv
@@ -764,7 +777,7 @@ size_t pa_decode_step_workspace_size(int32_t num_reqs, int32_t num_q_heads, int3
   const int32_t hkv = num_q_heads / PA_GQA_GROUP;
   const int grid = step_grid(num_reqs, hkv, max_seq_len);
   if (grid < 0) return 0;
-  return layout_for_grid(num_reqs, hkv, head_dim, grid, 1).total;
+  return layout_for_grid(num_reqs, hkv, head_dim, grid).total;
 }
 
 int32_t pa_decode_step_bucket(int32_t num_reqs) {
@@ -799,7 +812,7 @@ pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, vo
   if (grid < 0)
     return fail(PA_ERR_UNSUPPORTED, "%d rows of up to %d tokens need more than %d CTAs", num_reqs, max_seq_len,
                 pa::kPlanMaxCtas);
-  const WorkspaceLayout wl = layout_for_grid(num_reqs, num_kv_heads, head_dim, grid, 1);
+  const WorkspaceLayout wl = layout_for_grid(num_reqs, num_kv_heads, head_dim, grid);
   if (workspace_bytes < wl.total)
     return fail(PA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, wl.total);
   if (num_reqs == 0) return ok();
@@ -829,8 +842,16 @@ pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, vo
   pa::StepPlan plan;
   plan.n_rows = num_reqs;
   plan.max_seq_len = max_seq_len;
+  // the warp-granular kernel when every segment fits one window and the
+  // segments the bounds allow hold four warp segments of kMinWarpSegPages
+  // (the same rule as the host plan's; from the bounds, so a captured launch
+  // keeps its kernel)
+  const int64_t nseg = std::max(1, grid / num_kv_heads);
+  const int64_t seg_est = ((int64_t)num_reqs * (pages_of(max_seq_len) + pa::kStepItemCost) + nseg - 1) / nseg;
+  const bool warp_granular = step_one_window(num_reqs, num_kv_heads, max_seq_len, grid) &&
+                             seg_est >= pa::kDecodeWarps * pa::kMinWarpSegPages;
   s = run_launch(PA_KERNEL_DECODE_STEP, "decode_step", stream,
-                 [&] { return pa::launch_decode_step(dp, plan, grid, stream); });
+                 [&] { return pa::launch_decode_step(dp, plan, grid, warp_granular, stream); });
   return s == PA_OK ? ok() : s;
 }
 
