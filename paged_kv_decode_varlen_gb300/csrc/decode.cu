@@ -254,38 +254,49 @@ __device__ __forceinline__ void bar_all() { __syncthreads(); }
 // Whole warp (lane = 4 dims at d0): folds the shared-prefix partials of
 // output row orow (p.prefix_n key-chunk partials, or the merged one) into
 // the normalised partial o with log2 lse lse2 by log-sum-exp; returns the
-// merged lse.  Lanes read the partials' lse in parallel, then every partial
-// load is in flight at once.
+// merged lse.  Eight partials per round, every load of the round (lane i:
+// partial i's lse; all lanes: 4 dims of each) in flight at once, with a
+// running max across rounds.
 __device__ __forceinline__ float fold_prefix(const DecodeParams& p, float4& o, float lse2, size_t orow, int d0,
                                              int lane) {
+  constexpr int kRound = 8;
   const int n = p.prefix_n;
   float M = lse2;
-  for (int c0 = 0; c0 < n; c0 += 32)
-    if (c0 + lane < n) M = fmaxf(M, p.prefix_lse[(size_t)(c0 + lane) * p.prefix_rows + orow]);
+  float wsum = lse2 == -INFINITY ? 0.f : 1.f;
+  float4 a = lse2 == -INFINITY ? make_float4(0.f, 0.f, 0.f, 0.f) : o;
+  for (int c0 = 0; c0 < n; c0 += kRound) {
+    const int nc = min(kRound, n - c0);
+    const float lv = lane < nc ? p.prefix_lse[(size_t)(c0 + lane) * p.prefix_rows + orow] : -INFINITY;
+    float4 y[kRound];
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-  if (M == -INFINITY) return -INFINITY;
-  const float wo = exp2f(lse2 - M);  // own part (-inf -> 0)
-  float wsum = wo;
-  float4 a = make_float4(o.x * wo, o.y * wo, o.z * wo, o.w * wo);
-  for (int c0 = 0; c0 < n; c0 += 32) {
-    const int nc = min(32, n - c0);
-    const float w = lane < nc ? exp2f(p.prefix_lse[(size_t)(c0 + lane) * p.prefix_rows + orow] - M) : 0.f;
+    for (int i = 0; i < kRound; ++i)
+      y[i] = i < nc ? *reinterpret_cast<const float4*>(p.prefix_o + ((size_t)(c0 + i) * p.prefix_rows + orow) * kHeadDim +
+                                                       d0)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mb = lv;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, s));
+    const float mn = fmaxf(M, mb);
+    if (mn == -INFINITY) continue;  // every partial so far is empty
+    const float sc = exp2f(M - mn);  // M = -inf -> 0
+    wsum *= sc;
+    a = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
+    const float w = exp2f(lv - mn);  // -inf -> 0
     float ws = w;
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, s);
     wsum += ws;
-#pragma unroll 4
-    for (int i = 0; i < nc; ++i) {
+#pragma unroll
+    for (int i = 0; i < kRound; ++i) {
       const float wi = __shfl_sync(0xffffffffu, w, i);
-      const float4 y =
-          *reinterpret_cast<const float4*>(p.prefix_o + ((size_t)(c0 + i) * p.prefix_rows + orow) * kHeadDim + d0);
-      a.x = fmaf(wi, y.x, a.x);
-      a.y = fmaf(wi, y.y, a.y);
-      a.z = fmaf(wi, y.z, a.z);
-      a.w = fmaf(wi, y.w, a.w);
+      a.x = fmaf(wi, y[i].x, a.x);
+      a.y = fmaf(wi, y[i].y, a.y);
+      a.z = fmaf(wi, y[i].z, a.z);
+      a.w = fmaf(wi, y[i].w, a.w);
     }
+    M = mn;
   }
+  if (M == -INFINITY) return -INFINITY;
   const float inv = 1.f / wsum;
   o = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
   return M + log2f(wsum);
@@ -944,46 +955,47 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     bar_all();  // tid 0's acquire orders the piece reads below
     if (sm.is_last) {
-      // lane-parallel weights, then every piece load in flight at once
+      // kRound pieces per round with every load of the round (lane i: the
+      // lse of piece i; all lanes: 4 dims of each piece) in flight at once,
+      // merged by log-sum-exp with a running max across rounds
+      constexpr int kRound = 16;
       const int n_pc = b1 - b0 + 1;
-      float Mx = -INFINITY;
-      for (int c0 = 0; c0 < n_pc; c0 += 32) {
-        const int bb = b0 + c0 + lane;
-        if (c0 + lane < n_pc) {
-          const int jj = (bb == b0 && b0 * seg_len < A) ? 1 : 0;
-          Mx = fmaxf(Mx, __ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g));
-        }
-      }
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o2));
-      float wsum = 0.f;
+      auto piece_slot = [&](int bb) {
+        const int jj = (bb == b0 && b0 * seg_len < A) ? 1 : 0;
+        return ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
+      };
+      float Mx = -INFINITY, wsum = 0.f;
       float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (Mx != -INFINITY) {
-        for (int c0 = 0; c0 < n_pc; c0 += 32) {
-          const int nc = min(32, n_pc - c0);
-          float w = 0.f;
-          if (lane < nc) {
-            const int bb = b0 + c0 + lane;
-            const int jj = (bb == b0 && b0 * seg_len < A) ? 1 : 0;
-            w = fast_exp2(__ldcg(p.piece_lse + ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g) - Mx);
-          }
-          float ws = w;
+      for (int c0 = 0; c0 < n_pc; c0 += kRound) {
+        const int nc = min(kRound, n_pc - c0);
+        const float lv = lane < nc ? __ldcg(p.piece_lse + piece_slot(b0 + c0 + lane)) : -INFINITY;
+        float4 x[kRound];
 #pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o2);
-          wsum += ws;
-#pragma unroll 4
-          for (int i = 0; i < nc; ++i) {
-            const int bb = b0 + c0 + i;
-            const int jj = (bb == b0 && b0 * seg_len < A) ? 1 : 0;
-            const size_t sl = ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
-            const float wi = __shfl_sync(0xffffffffu, w, i);
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(p.piece_o + sl * kHeadDim + d0));
-            a4.x = fmaf(wi, x.x, a4.x);
-            a4.y = fmaf(wi, x.y, a4.y);
-            a4.z = fmaf(wi, x.z, a4.z);
-            a4.w = fmaf(wi, x.w, a4.w);
-          }
+        for (int i = 0; i < kRound; ++i)
+          x[i] = i < nc ? __ldcg(reinterpret_cast<const float4*>(p.piece_o + piece_slot(b0 + c0 + i) * kHeadDim + d0))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        float mb = lv;
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o2));
+        const float mn = fmaxf(Mx, mb);
+        if (mn == -INFINITY) continue;  // every piece so far is empty
+        const float sc = fast_exp2(Mx - mn);  // Mx = -inf -> 0
+        wsum *= sc;
+        a4 = make_float4(a4.x * sc, a4.y * sc, a4.z * sc, a4.w * sc);
+        const float w = fast_exp2(lv - mn);  // -inf -> 0
+        float ws = w;
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o2);
+        wsum += ws;
+#pragma unroll
+        for (int i = 0; i < kRound; ++i) {
+          const float wi = __shfl_sync(0xffffffffu, w, i);
+          a4.x = fmaf(wi, x[i].x, a4.x);
+          a4.y = fmaf(wi, x[i].y, a4.y);
+          a4.z = fmaf(wi, x[i].z, a4.z);
+          a4.w = fmaf(wi, x[i].w, a4.w);
         }
+        Mx = mn;
       }
       const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
       a4.x *= winv;
