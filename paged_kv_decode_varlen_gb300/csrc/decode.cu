@@ -1216,6 +1216,28 @@ __device__ __forceinline__ void store_row16(uint16_t* row, const float (&o)[16],
   *reinterpret_cast<uint4*>(row + 64 + 8 * c) = hi;
 }
 
+// The merge of a cut row's pieces by its last piece (whole warp), four
+// partials per batch with all their loads in flight; kept out of line so that
+// its registers do not weigh on the page loop.
+__device__ __noinline__ void wg_merge_pieces(const float* piece_o, const float* piece_lse, int b0, int b1, int A,
+                                             int sw, int Hkv, int kvh, int g, int c, LseAcc& out) {
+  const int n_pc = b1 - b0 + 1;
+  auto piece_slot = [&](int bb) {
+    const int jj = (bb == b0 && b0 * sw < A) ? 1 : 0;
+    return ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
+  };
+  LseAcc acc;
+  acc.m = -INFINITY;
+  acc.w = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc.a[i] = 0.f;
+  for (int c0 = 0; c0 < n_pc; c0 += 4)
+    lse_acc_batch<true>(
+        acc, min(4, n_pc - c0), c, [&](int u) { return piece_o + piece_slot(b0 + c0 + u) * kHeadDim; },
+        [&](int u) { return piece_lse + piece_slot(b0 + c0 + u); });
+  out = acc;
+}
+
 // kDiag: the diagnostic instantiation that tests the timeout path (bf16
 // pages).  Warp 0 of CTA 0 arms the barrier of its second page without
 // issuing that page's copies, so the wait on it runs out; every wait of this
@@ -1697,22 +1719,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     __syncwarp();  // lane 0's acquire orders the piece reads below
     if (!__shfl_sync(0xffffffffu, last, 0)) continue;
     // the last piece to finish: merge every piece of the row (and the
-    // prefix partials), four partials per batch with all their loads in flight
+    // prefix partials)
     {
-      const int n_pc = b1 - b0 + 1;
-      auto piece_slot = [&](int bb) {
-        const int jj = (bb == b0 && b0 * sw < A) ? 1 : 0;
-        return ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
-      };
       LseAcc acc;
-      acc.m = -INFINITY;
-      acc.w = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) acc.a[i] = 0.f;
-      for (int c0 = 0; c0 < n_pc; c0 += 4)
-        lse_acc_batch<true>(
-            acc, min(4, n_pc - c0), c, [&](int u) { return p.piece_o + piece_slot(b0 + c0 + u) * kHeadDim; },
-            [&](int u) { return p.piece_lse + piece_slot(b0 + c0 + u); });
+      wg_merge_pieces(p.piece_o, p.piece_lse, b0, b1, A, sw, Hkv, kvh, g, c, acc);
       if (p.prefix_o) {
         if (prefix_ready(p, tok, kvh, lane)) lse_acc_prefix(acc, p, orow, c);
         prefix_read_done(p, tok, kvh, lane);
