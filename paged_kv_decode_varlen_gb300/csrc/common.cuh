@@ -149,6 +149,15 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* addr) {
   return v;
 }
 
+// Relaxed load at GPU scope: with fence_acq_rel_gpu() after it, an acquire
+// (the load can be issued early and its latency hidden behind other loads).
+__device__ __forceinline__ int ld_relaxed_gpu(const int* addr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Release add at GPU scope: this thread's earlier writes (and those it has
 // observed, e.g. through a CTA barrier) are visible to a thread that
 // acquires the new value.

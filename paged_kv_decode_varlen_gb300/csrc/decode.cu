@@ -309,13 +309,14 @@ __device__ __forceinline__ float fold_prefix(const DecodeParams& p, float4& o, f
 // a row's pages sit after its fixed cost, and segment s holds the pages
 // whose units fall in [s C, (s + 1) C).  The fixed cost stands for the item-
 // end merge work, so segments with many short rows hold fewer pages.  Fills
-// the items win0 .. win0 + kDecodeMaxItemsPerCta - 1 of this CTA's segment
-// (all threads call it; it ends with a barrier).  Also writes the outputs of
+// the items win0 .. win0 + kMaxItems - 1 of this CTA's segment (kNThreads
+// threads, all of which call it; it ends with a barrier).  Also writes the outputs of
 // padding rows (zero, lse -inf) and records rows outside the bounds.
-template <int kUnit = 1, class Smem>
+template <int kUnit, int kNThreads, int kMaxItems, int kMaxPages, class Smem>
 __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& sm, int kvh, int sidx, int nseg_grid,
                             int win0) {
-  constexpr int kRows = kPlanMaxRows / kThreads;  // rows per thread, consecutive
+  constexpr int kRows = (kPlanMaxRows + kNThreads - 1) / kNThreads;  // rows per thread, consecutive
+  constexpr int kNWarps = kNThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.num_kv_heads;
   int pg[kRows], len[kRows];
@@ -349,14 +350,14 @@ __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& s
   __syncthreads();
   int total = 0, woff = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < kNWarps; ++w) {
     const int v = sm.scan[w];
     woff += (w < warp) ? v : 0;
     total += v;
   }
   int A = woff + incl - tsum;  // cost position of this thread's first row
   const int n_eff = max(1, min(nseg_grid, (total + kStepMinSegCost - 1) / kStepMinSegCost));
-  // segment length in stream units, whole warp segments for the warp-granular kernel (kUnit 4)
+  // segment length in stream units, whole warp segments for the warp-granular kernel (kUnit warps)
   const int C = (max(1, (total + n_eff - 1) / n_eff) + kUnit - 1) / kUnit * kUnit;
   const int S = sidx * C, E = min(S + C, total);
   // this segment's part of each row: (first page p0, pages nn), packed with
@@ -384,7 +385,7 @@ __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& s
   __syncthreads();
   int tot2 = 0, woff2 = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < kNWarps; ++w) {
     const int v = sm.scan[w];
     woff2 += (w < warp) ? v : 0;
     tot2 += v;
@@ -395,7 +396,7 @@ __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& s
   for (int i = 0; i < kRows; ++i) {
     if (nnv[i] > 0) {
       const int idx = (e2 & 0xffff) - win0;
-      if (idx >= 0 && idx < kDecodeMaxItemsPerCta) {
+      if (idx >= 0 && idx < kMaxItems) {
         const int r = tid * kRows + i;
         Item& it = sm.items[idx];
         it.q_start = e2 >> 16;
@@ -417,11 +418,11 @@ __device__ void step_window(const DecodeParams& p, const StepPlan& plan, Smem& s
     }
   }
   if (tid == 0) {
-    sm.n_items = max(0, min(n_all - win0, kDecodeMaxItemsPerCta));
+    sm.n_items = max(0, min(n_all - win0, kMaxItems));
     sm.n_items_all = n_all;
     sm.seg_cost = C;
     sm.seg_pages = tot2 >> 16;
-    if (tot2 >> 16 > kDecodeMaxPagesPerCta) {  // bounded by the host's grid choice
+    if (tot2 >> 16 > kMaxPages) {  // bounded by the host's grid choice
       record_error(p.err, PA_ERR_DEVICE_INDEX);
       sm.n_items = 0;
     }
@@ -474,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       sm.abort_flag = 0;
       fence_mbar_init();
     }
-    step_window(p, plan, sm, kvh, sidx, (int)gridDim.x / Hkv, 0);
+    step_window<1, kThreads, kDecodeMaxItemsPerCta, kDecodeMaxPagesPerCta>(p, plan, sm, kvh, sidx,
+                                                                          (int)gridDim.x / Hkv, 0);
     npg = sm.seg_pages;
   } else {
     const int S0 = sidx * plan.seg;
@@ -944,8 +946,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int b0 = (A + kAlpha) / seg_len, b1 = (A + kAlpha + pages_r - 1) / seg_len;
     const int jslot = ((kStep ? win0 : 0) + k == 0) ? 0 : 1;
     const size_t slot = ((size_t)b * 2 + jslot) * kGroup + g;
-    *reinterpret_cast<float4*>(p.piece_o + slot * kHeadDim + d0) = o;
-    if (lane == 0) p.piece_lse[slot] = lse2;
+    if ((int64_t)slot < p.piece_slots) {
+      *reinterpret_cast<float4*>(p.piece_o + slot * kHeadDim + d0) = o;
+      if (lane == 0) p.piece_lse[slot] = lse2;
+    } else if (lane == 0) {
+      record_error(p.err, PA_ERR_DEVICE_INDEX);  // the host sized the workspace for fewer pieces
+    }
     bar_all();  // every piece write of the CTA precedes tid 0's release below
     if (tid == 0) {
       int* cnt = p.counters + (size_t)it.r * Hkv + kvh;
@@ -1017,7 +1023,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   // and its pages are consumed, so the ring is empty
   win0 += n_items;
   if (win0 >= sm.n_items_all) break;
-  if constexpr (kStep) step_window(p, plan, sm, kvh, sidx, (int)gridDim.x / Hkv, win0);
+  if constexpr (kStep)
+    step_window<1, kThreads, kDecodeMaxItemsPerCta, kDecodeMaxPagesPerCta>(p, plan, sm, kvh, sidx,
+                                                                          (int)gridDim.x / Hkv, win0);
   }
 
   __syncthreads();  // every thread has left the item loop
@@ -1035,34 +1043,35 @@ __global__ void __launch_bounds__(kThreads, 3)
 }
 
 
-// ------------------------------------------------- warp-granular host plan
-// Host-planned launches (pa_attention_varlen and its q8_0 / shared-prefix
-// forms) cut every CTA segment into kWarps equal warp segments: warp w of
-// CTA b streams pages [w sw, (w + 1) sw) of the CTA's segment (sw = seg /
-// kWarps) through its own kWgStages-deep ring and finishes its items on its
-// own.  A warp's item end (the merge of its 4 token slots, the partial of a
-// cut row, the count of finished pieces, the merge of all pieces by the
-// last one) then stalls only that warp: the other warps of the SM keep
-// streaming, and no CTA-wide barrier follows the prologue.  The page loop is
-// the same arithmetic as above; a warp takes the 16 tokens of a page as two
-// pairs per lane (tokens ts + 8 h and ts + 4 + 8 h, h = 0, 1).
+// ---------------------------------------------------- warp-granular kernel
+// One CTA of kWgWarps warps per SM.  Every CTA segment is cut into kWgWarps
+// equal warp segments: warp w of CTA b streams pages [w sw, (w + 1) sw) of
+// the CTA's segment (sw = seg / kWgWarps) through its own kWgStages-deep
+// ring and finishes its items on its own.  A warp's item end (the merge of
+// its 4 token slots, the partial of a cut row, the count of finished pieces,
+// the merge of all pieces by the last one) then stalls only that warp: the
+// other warps of the SM keep streaming, and no CTA-wide barrier follows the
+// prologue.  The page loop is the same arithmetic as above; a warp takes the
+// 16 tokens of a page as two pairs per lane (tokens ts + 8 h and ts + 4 + 8
+// h, h = 0, 1).
 constexpr int kWgStages = 2;  // pages in flight per warp
+constexpr int kWgThreads = kWgWarps * 32;
 
 template <int kSlab>
 struct __align__(128) WgSmem {
-  uint8_t k[kWarps][kWgStages][kSlab];
-  uint8_t v[kWarps][kWgStages][kSlab];
-  uint16_t qs[kWarps][kGroup * kHeadDim];  // each warp's current item's q (bulk copy)
-  uint64_t full[kWarps][kWgStages];        // TMA landed
-  uint64_t q_full[kWarps];                 // q landed
-  int32_t ids[kDecodeMaxPagesPerCta];
-  Item items[kDecodeMaxItemsPerCta];
-  int stage_page[kWarps][kWgStages];  // last warp page issued into each stage (-1: none)
-  int q_issued[kWarps];
+  uint8_t k[kWgWarps][kWgStages][kSlab];
+  uint8_t v[kWgWarps][kWgStages][kSlab];
+  uint16_t qs[kWgWarps][kGroup * kHeadDim];  // each warp's current item's q (bulk copy)
+  uint64_t full[kWgWarps][kWgStages];        // TMA landed
+  uint64_t q_full[kWgWarps];                 // q landed
+  int32_t ids[kWgMaxPagesPerCta];
+  Item items[kWgMaxItemsPerCta];
+  int stage_page[kWgWarps][kWgStages];  // last warp page issued into each stage (-1: none)
+  int q_issued[kWgWarps];
   int n_items;
   int abort_flag;
   // decode step (self-planned): see step_window
-  int scan[kWarps];
+  int scan[kWgWarps];
   int n_items_all;
   int seg_cost;
   int seg_pages;
@@ -1072,7 +1081,7 @@ static_assert(offsetof(WgSmem<kSlabBytes>, v) % 128 == 0 && offsetof(WgSmem<kQ8S
                   offsetof(WgSmem<kSlabBytes>, qs) % 16 == 0 && offsetof(WgSmem<kQ8SlabBytes>, qs) % 16 == 0 &&
                   (kWgStages * kSlabBytes) % 16 == 0 && (kWgStages * kQ8SlabBytes) % 16 == 0,
               "bulk copies land on 16-byte boundaries");
-static_assert(3 * (sizeof(WgSmem<kSlabBytes>) + 1024) <= 228 * 1024, "three decode CTAs per SM");
+static_assert(sizeof(WgSmem<kSlabBytes>) <= 227 * 1024, "one decode CTA per SM");
 
 // Online log-sum-exp merge of normalised partials (log2-domain lse) for one
 // head per 8-lane group (head g = lane >> 3), 16 dims per lane (dims
@@ -1159,15 +1168,29 @@ __device__ __forceinline__ void lse_acc_prefix(LseAcc& s, const DecodeParams& p,
         [&](int u) { return p.prefix_lse + (size_t)(c0 + u) * p.prefix_rows + orow; });
 }
 
-// A prefix pass running beside the decode launch (p.prefix_done set): wait,
-// bounded, until the key chunks of token tok's query tile are all written.
-// Whole warp; false on a timeout (recorded), and the fold is left out.
-__device__ __forceinline__ bool prefix_ready(const DecodeParams& p, int tok, int kvh, int lane) {
+// A prefix pass running beside the decode launch (p.prefix_done set): the
+// count of key chunks written for token tok's query tile and kv head.
+__device__ __forceinline__ const int* prefix_flag(const DecodeParams& p, int tok, int kvh) {
+  return p.prefix_done ? p.prefix_done + (size_t)(tok / kPrefillQTile) * p.num_kv_heads + kvh : nullptr;
+}
+
+// Whole warp, before a fold: completes the wait for every key chunk of the
+// tile, begun by lane 0's relaxed read `peek` of the count (issued early, so
+// its latency hides behind other loads): a bounded acquire spin if the count
+// was short, else an acquire fence.  False on a timeout (recorded; the fold
+// is left out).  Then counts this reader, its result (lane 0) in *readers_old
+// for prefix_read_done: every reader has passed its wait when the count is
+// full, so the last one may return the counters to zero while the others
+// still read the partials (which the counters do not guard).
+__device__ __forceinline__ bool prefix_ready(const DecodeParams& p, int tok, int kvh, int lane, int peek,
+                                             int* readers_old) {
   if (!p.prefix_done) return true;
   int ok = 1;
   if (lane == 0) {
-    const int* f = p.prefix_done + (size_t)(tok / kPrefillQTile) * p.num_kv_heads + kvh;
-    if (ld_acquire_gpu(f) < p.prefix_n) {
+    const int* f = prefix_flag(p, tok, kvh);
+    if (peek >= p.prefix_n) {
+      fence_acq_rel_gpu();
+    } else if (ld_acquire_gpu(f) < p.prefix_n) {
       const unsigned long long t0 = globaltimer();
       while (ld_acquire_gpu(f) < p.prefix_n) {
         if (globaltimer() - t0 > kWaitLimitNs) {
@@ -1178,26 +1201,24 @@ __device__ __forceinline__ bool prefix_ready(const DecodeParams& p, int tok, int
         __nanosleep(128);
       }
     }
+    *readers_old = atomicAdd(p.prefix_readers + (size_t)(tok / kPrefillQTile) * p.num_kv_heads + kvh, 1);
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();  // lane 0's acquire orders every lane's partial reads
   return ok != 0;
 }
 
-// After a fold (whole warp): count the reader; the last reader of a tile's
-// kv head (one per query token of the tile) returns both counters to zero
-// for the next call.
-__device__ __forceinline__ void prefix_read_done(const DecodeParams& p, int tok, int kvh, int lane) {
-  if (!p.prefix_done) return;
-  __syncwarp();  // every lane's partial reads are done
-  if (lane == 0) {
-    const int t = tok / kPrefillQTile;
+// After a fold (lane 0's count from prefix_ready): the last reader of a
+// tile's kv head (one per query token of the tile) returns both counters to
+// zero for the next call.
+__device__ __forceinline__ void prefix_read_done(const DecodeParams& p, int tok, int kvh, int lane, int readers_old) {
+  if (!p.prefix_done || lane != 0) return;
+  const int t = tok / kPrefillQTile;
+  const int readers = min(kPrefillQTile, p.total_q - t * kPrefillQTile);
+  if (readers_old == readers - 1) {
     const size_t idx = (size_t)t * p.num_kv_heads + kvh;
-    const int readers = min(kPrefillQTile, p.total_q - t * kPrefillQTile);
-    if (atomicAdd(p.prefix_readers + idx, 1) == readers - 1) {
-      p.prefix_readers[idx] = 0;
-      p.prefix_done[idx] = 0;
-    }
+    p.prefix_readers[idx] = 0;
+    p.prefix_done[idx] = 0;
   }
 }
 
@@ -1218,13 +1239,17 @@ __device__ __forceinline__ void store_row16(uint16_t* row, const float (&o)[16],
 
 // The merge of a cut row's pieces by its last piece (whole warp), four
 // partials per batch with all their loads in flight; kept out of line so that
-// its registers do not weigh on the page loop.
-__device__ __noinline__ void wg_merge_pieces(const float* piece_o, const float* piece_lse, int b0, int b1, int A,
-                                             int sw, int Hkv, int kvh, int g, int c, LseAcc& out) {
+// its registers do not weigh on the page loop.  With a prefix pass beside
+// the launch, lane 0 first reads the row's prefix chunk count (relaxed; its
+// latency hides behind the piece loads) and returns it.
+__device__ __noinline__ int wg_merge_pieces(const float* piece_o, const float* piece_lse, int64_t piece_slots, int b0,
+                                            int b1, int A, int sw, int Hkv, int kvh, int g, int c, int lane,
+                                            const int* flag, LseAcc& out) {
+  const int peek = (flag && lane == 0) ? ld_relaxed_gpu(flag) : 0;
   const int n_pc = b1 - b0 + 1;
-  auto piece_slot = [&](int bb) {
+  auto piece_slot = [&](int bb) {  // (a slot past the workspace was recorded and is read clamped)
     const int jj = (bb == b0 && b0 * sw < A) ? 1 : 0;
-    return ((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g;
+    return min(((size_t)(bb * Hkv + kvh) * 2 + jj) * kGroup + g, (size_t)piece_slots - 1);
   };
   LseAcc acc;
   acc.m = -INFINITY;
@@ -1236,6 +1261,7 @@ __device__ __noinline__ void wg_merge_pieces(const float* piece_o, const float* 
         acc, min(4, n_pc - c0), c, [&](int u) { return piece_o + piece_slot(b0 + c0 + u) * kHeadDim; },
         [&](int u) { return piece_lse + piece_slot(b0 + c0 + u); });
   out = acc;
+  return peek;
 }
 
 // kDiag: the diagnostic instantiation that tests the timeout path (bf16
@@ -1244,7 +1270,7 @@ __device__ __noinline__ void wg_merge_pieces(const float* piece_o, const float* 
 // instantiation gives up after 1 ms instead of kWaitLimitNs.  No copy is
 // dropped anywhere else, and nothing is read out of bounds.
 template <bool kQ8, bool kDiag, bool kStep = false>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kWgThreads, 1)
     decode_wg_kernel(const DecodeParams p, const __grid_constant__ typename PlanOf<kStep>::type plan) {
   static_assert(!(kDiag && kQ8), "the diagnostic instantiation reads bf16 pages");
   static_assert(!(kStep && (kQ8 || kDiag)), "the decode step serves bf16 pages");
@@ -1267,7 +1293,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int Hkv = p.num_kv_heads;
   const int kvh = b % Hkv, sidx = b / Hkv;
   if (tid == 0) {
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kWgWarps; ++w) {
       for (int s = 0; s < kWgStages; ++s) {
         mbar_init(&sm.full[w][s], 1);
         sm.stage_page[w][s] = -1;
@@ -1281,11 +1307,12 @@ __global__ void __launch_bounds__(kThreads, 3)
   int seg_units;  // segment length in stream units (pages, or pages plus row costs)
   if constexpr (kStep) {
     // the CTA plans its own segment from the device seq_lens; a segment with
-    // more than kDecodeMaxItemsPerCta rows cannot occur for the launches the
+    // more than kWgMaxItemsPerCta rows cannot occur for the launches the
     // host sends here (it checks the bound) and is recorded
-    step_window<kWarps>(p, plan, sm, kvh, sidx, (int)gridDim.x / Hkv, 0);
+    step_window<kWgWarps, kWgThreads, kWgMaxItemsPerCta, kWgMaxPagesPerCta>(p, plan, sm, kvh, sidx,
+                                                                           (int)gridDim.x / Hkv, 0);
     seg_units = sm.seg_cost;
-    if (tid == 0 && sm.n_items_all > kDecodeMaxItemsPerCta) record_error(p.err, PA_ERR_DEVICE_INDEX);
+    if (tid == 0 && sm.n_items_all > kWgMaxItemsPerCta) record_error(p.err, PA_ERR_DEVICE_INDEX);
   } else {
     const int S0 = sidx * plan.seg;
     const int npg = min(plan.total, S0 + plan.seg) - S0;  // pages of this CTA's segment
@@ -1297,7 +1324,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     // for the previous kernel
     if (warp == 0) {
       int base_q = 0, n_it = 0;
-      for (int k0 = 0; k0 < kDecodeMaxItemsPerCta; k0 += 32) {
+      for (int k0 = 0; k0 < kWgMaxItemsPerCta; k0 += 32) {
         const int item = plan.first_row[sidx] + k0 + lane;
         const bool exists = item < n_items_all;
         int r = 0, L = 0, size = 0, tok = 0;
@@ -1316,7 +1343,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         }
         const int start = base_q + incl - size;
         const bool in_seg = size > 0 && start < npg;
-        if (in_seg && k0 + lane < kDecodeMaxItemsPerCta) {
+        if (in_seg && k0 + lane < kWgMaxItemsPerCta) {
           Item& it = sm.items[k0 + lane];
           it.q_start = start;
           it.n = min(size, npg - start);
@@ -1336,7 +1363,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       if (lane == 0) {
         if (base_q < npg) record_error(p.err, PA_ERR_DEVICE_INDEX);  // metadata differ from the plan
-        sm.n_items = min(n_it, kDecodeMaxItemsPerCta);
+        sm.n_items = min(n_it, kWgMaxItemsPerCta);
       }
     }
     __syncthreads();
@@ -1351,7 +1378,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   // past the table) is recorded and masked, and fetched from block 0
   const int n_cov = sm.items[n_items - 1].q_start + sm.items[n_items - 1].n;
   int ok = 1;
-  for (int q = tid; q < n_cov; q += kThreads) {
+  for (int q = tid; q < n_cov; q += kWgThreads) {
     int lo = 0, hi = n_items - 1;
     while (lo < hi) {  // last item with q_start <= q
       const int mid = (lo + hi + 1) >> 1;
@@ -1372,7 +1399,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   // ---- this warp's part of the segment: stream units [cs, cs + sw), its
   // pages [a, e) of the segment (with the host plan a unit is a page)
-  const int sw = seg_units / kWarps;
+  const int sw = seg_units / kWgWarps;
   int a, e;
   if constexpr (kStep) {
     const int cs = sidx * seg_units + warp * sw, ce = cs + sw;
@@ -1399,7 +1426,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     k = lo;
   }
   const int k_first = k;
-  const int gw = sidx * kWarps + warp;  // warp segment of the stream
+  const int gw = sidx * kWgWarps + warp;  // warp segment of the stream
   const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k_cache);
   const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v_cache);
   // segment page q in [a, e) -> warp page j = q - a -> stage j % kWgStages
@@ -1682,17 +1709,20 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int head = kvh * kGroup + g;
     const size_t orow = (size_t)tok * p.num_q_heads + head;
     if (p0w == 0 && i1 - i0 == pages_r) {  // the whole row in this warp
+      int rd = 0;
       if (p.prefix_o) {
-        if (prefix_ready(p, tok, kvh, lane)) {
+        const int* f = prefix_flag(p, tok, kvh);
+        const int peek = (f && lane == 0) ? ld_relaxed_gpu(f) : 0;
+        if (prefix_ready(p, tok, kvh, lane, peek, &rd)) {
           LseAcc acc;
           lse_acc_init(acc, o, lse2);
           lse_acc_prefix(acc, p, orow, c);
           lse2 = lse_acc_done(acc, o);
         }
-        prefix_read_done(p, tok, kvh, lane);
       }
       store_row16(p.out + orow * kHeadDim, o, c);
       if (p.lse && c == 0) p.lse[orow] = lse2 * kLn2;
+      if (p.prefix_o) prefix_read_done(p, tok, kvh, lane, rd);
       continue;
     }
     // the item is cut by warp-segment boundaries: publish this warp's partial
@@ -1701,12 +1731,16 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int jslot = (k == k_first) ? 0 : 1;
     {
       const size_t slot = ((size_t)(gw * Hkv + kvh) * 2 + jslot) * kGroup + g;
-      float* dst = p.piece_o + slot * kHeadDim;
-      *reinterpret_cast<float4*>(dst + 8 * c) = make_float4(o[0], o[1], o[2], o[3]);
-      *reinterpret_cast<float4*>(dst + 8 * c + 4) = make_float4(o[4], o[5], o[6], o[7]);
-      *reinterpret_cast<float4*>(dst + 64 + 8 * c) = make_float4(o[8], o[9], o[10], o[11]);
-      *reinterpret_cast<float4*>(dst + 64 + 8 * c + 4) = make_float4(o[12], o[13], o[14], o[15]);
-      if (c == 0) p.piece_lse[slot] = lse2;
+      if ((int64_t)slot < p.piece_slots) {
+        float* dst = p.piece_o + slot * kHeadDim;
+        *reinterpret_cast<float4*>(dst + 8 * c) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(dst + 8 * c + 4) = make_float4(o[4], o[5], o[6], o[7]);
+        *reinterpret_cast<float4*>(dst + 64 + 8 * c) = make_float4(o[8], o[9], o[10], o[11]);
+        *reinterpret_cast<float4*>(dst + 64 + 8 * c + 4) = make_float4(o[12], o[13], o[14], o[15]);
+        if (c == 0) p.piece_lse[slot] = lse2;
+      } else if (c == 0) {
+        record_error(p.err, PA_ERR_DEVICE_INDEX);  // the host sized the workspace for fewer pieces
+      }
     }
     __syncwarp();  // every lane's piece write precedes lane 0's release below
     int last = 0;
@@ -1722,15 +1756,16 @@ __global__ void __launch_bounds__(kThreads, 3)
     // prefix partials)
     {
       LseAcc acc;
-      wg_merge_pieces(p.piece_o, p.piece_lse, b0, b1, A, sw, Hkv, kvh, g, c, acc);
-      if (p.prefix_o) {
-        if (prefix_ready(p, tok, kvh, lane)) lse_acc_prefix(acc, p, orow, c);
-        prefix_read_done(p, tok, kvh, lane);
-      }
+      const int peek =
+          wg_merge_pieces(p.piece_o, p.piece_lse, p.piece_slots, b0, b1, A, sw, Hkv, kvh, g, c, lane,
+                          prefix_flag(p, tok, kvh), acc);
+      int rd = 0;
+      if (p.prefix_o && prefix_ready(p, tok, kvh, lane, peek, &rd)) lse_acc_prefix(acc, p, orow, c);
       float a4[16];
       const float l2 = lse_acc_done(acc, a4);
       store_row16(p.out + orow * kHeadDim, a4, c);
       if (p.lse && c == 0) p.lse[orow] = l2 * kLn2;
+      if (p.prefix_o) prefix_read_done(p, tok, kvh, lane, rd);
     }
   }
 
@@ -1771,7 +1806,7 @@ cudaError_t launch_decode_wg(const DecodeParams& p, const typename PlanOf<kStep>
   const cudaError_t e = set_smem_limit_once((const void*)decode_wg_kernel<kQ8, kDiag, kStep>, (int)kSmem,
                                             g_decode_attr_set[kVariant]);
   if (e != cudaSuccess) return e;
-  return launch_maybe_pdl(overlap, decode_wg_kernel<kQ8, kDiag, kStep>, dim3(grid), dim3(kThreads), kSmem, stream,
+  return launch_maybe_pdl(overlap, decode_wg_kernel<kQ8, kDiag, kStep>, dim3(grid), dim3(kWgThreads), kSmem, stream,
                           p, plan);
 }
 

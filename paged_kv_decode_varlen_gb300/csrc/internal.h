@@ -42,8 +42,10 @@ struct CopyParams {
 constexpr int kPlanMaxRows = 1024;   // decode rows per launch
 constexpr int kPlanMaxCtas = 1024;   // CTAs per launch
 constexpr int kDecodeMaxItemsPerCta = 64;
-// Host-planned decode launches cut each CTA's segment into this many warp
-// segments (one per warp); the plan's segment length is a multiple of it.
+// Warps of the CTA-granular decode kernel (three CTAs per SM).  Workspaces
+// hold kDecodeWarps pieces per CTA of the largest CTA-granular grid, which
+// also covers the warp-granular launches (a third of the CTAs, kWgWarps
+// pieces each).
 constexpr int kDecodeWarps = 4;
 // Host-planned launches whose warp segments would hold fewer pages than this
 // run the CTA-granular kernel: a row cut into many short warp pieces costs
@@ -51,6 +53,14 @@ constexpr int kDecodeWarps = 4;
 // latency-bound (measured: one 2048-token row per layer 12.6 us CTA-granular
 // against 18.6 us warp-granular; 32 rows 58.2 against 54.9 us).
 constexpr int kMinWarpSegPages = 8;
+// The warp-granular decode kernel runs one CTA of kWgWarps warps per SM,
+// one warp segment per warp: the warps of an SM then share one CTA, which
+// measured faster than three CTAs of four warps (the later CTAs on an SM
+// streamed up to 9 % slower).  A segment may hold kWgMaxPagesPerCta pages and
+// kWgMaxItemsPerCta rows.
+constexpr int kWgWarps = 12;
+constexpr int kWgMaxPagesPerCta = 3072;
+constexpr int kWgMaxItemsPerCta = 192;
 // Bytes of one (page, kv head) slab of K or V in bf16 (16 tokens x 128 dims).
 constexpr int kSlabBytesHost = 16 * 128 * 2;
 struct DecodePlan {
@@ -113,9 +123,10 @@ struct DecodeParams {
   int32_t total_q;
   uint16_t* out;         // bf16 [total_q, Hq, D]
   float* lse;            // [total_q, Hq] natural log, or null
-  float* piece_o;        // fp32 [2 * grid * kDecodeWarps, 4, D]: a warp segment's (host plan) or a CTA's
-                         // (decode step) partial of its first / last item
-  float* piece_lse;      // fp32 [2 * grid * kDecodeWarps, 4], log2 domain
+  float* piece_o;        // fp32 [2 x warp segments (warp-granular) or CTAs (CTA-granular), 4, D]: the
+                         // partial of a segment's first / last item
+  float* piece_lse;      // fp32 [2 x the same, 4], log2 domain
+  int64_t piece_slots;   // (piece, head) slots the two arrays hold; a write past them is recorded, not made
   int* counters;         // [num_reqs, Hkv] CTAs finished per item; zero between calls
   int* err;
   // decode step only: the new token of every row ([rows, Hkv, D] bf16) and
@@ -228,11 +239,13 @@ cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 // overlap: programmatic launch after the stream's previous kernel; diag:
 // the timeout-path diagnostic instantiation (bf16 pages, warp-granular);
 // cta_granular: the kernel whose 4 warps read every page of the CTA's
-// segment (no prefix pass beside it), for plans with short segments
+// segment (no prefix pass beside it), for plans with short segments; else
+// the warp-granular kernel (plan in whole warp segments of kWgWarps warps)
 cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int grid, bool q8, bool overlap,
                           bool diag, bool cta_granular, cudaStream_t stream);
-// warp_granular: the warp-granular kernel (no segment may hold more than
-// kDecodeMaxItemsPerCta rows), else the CTA-granular one (windows of rows)
+// warp_granular: the warp-granular kernel (grid: one CTA per SM at most; no
+// segment may hold more than kWgMaxItemsPerCta rows or kWgMaxPagesPerCta
+// pages), else the CTA-granular one (windows of rows)
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, bool warp_granular,
                                cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,

@@ -128,16 +128,19 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: [error word | item counters (num_reqs x Hkv int32) |
 // partial o (2 x grid_cap x pieces_per_cta x 4 heads x D fp32) | partial lse
-// (fp32)].  A host-planned decode CTA publishes pieces per warp segment
-// (kDecodeWarps of them), the self-planned decode step per CTA.
+// (fp32)].  Sized for kDecodeWarps pieces per CTA of the CTA-granular grid
+// bound: a CTA-granular CTA publishes fewer (one per CTA), a warp-granular
+// launch (at most a third of the CTAs) one per warp segment (kWgWarps).
 struct WorkspaceLayout {
   size_t counters, piece_o, piece_lse, total;
+  int64_t slots;  // (piece, head) slots
 };
 
 WorkspaceLayout layout_for_grid(int32_t num_reqs, int32_t hkv, int32_t head_dim, int grid,
                                 int pieces_per_cta = pa::kDecodeWarps) {
   WorkspaceLayout w;
   const size_t slots = (size_t)2 * grid * pieces_per_cta * PA_GQA_GROUP;
+  w.slots = (int64_t)slots;
   w.counters = PA_ERROR_WORD_BYTES;
   w.piece_o = w.counters + align256((size_t)std::max(num_reqs, 0) * (size_t)hkv * 4);
   w.piece_lse = w.piece_o + align256(slots * (size_t)std::max(head_dim, 0) * 4);
@@ -167,17 +170,19 @@ int step_grid(int32_t num_reqs, int32_t hkv, int32_t max_seq_len) {
   return (int)(nseg * hkv);
 }
 
-// Decode step: whether every segment of the launch holds at most
-// kDecodeMaxItemsPerCta rows, for any lengths within the call's bounds (so the
-// warp-granular kernel, which plans one window, serves it).  A row costs at
-// least 1 + kStepItemCost units and a segment is at most C units, C bounded by
-// the largest total cost over the segments (or the minimum segment).
-bool step_one_window(int32_t num_reqs, int32_t hkv, int32_t max_seq_len, int grid) {
-  if (num_reqs <= pa::kDecodeMaxItemsPerCta) return true;
-  const int64_t nseg = std::max(1, grid / std::max(hkv, 1));
-  const int64_t total_max = (int64_t)num_reqs * (pages_of(max_seq_len) + pa::kStepItemCost);
-  const int64_t c_max = std::max<int64_t>(pa::kStepMinSegCost, (total_max + nseg - 1) / nseg) + pa::kDecodeWarps;
-  return c_max / (1 + pa::kStepItemCost) + 2 <= pa::kDecodeMaxItemsPerCta;
+// Decode step: whether a launch of nseg segments per kv head fits a kernel
+// whose CTA holds at most max_items rows and max_pages pages of its segment
+// in one window, for any lengths within the call's bounds.  A row costs at
+// least 1 + kStepItemCost units and a segment is at most C units (C rounded
+// up to a multiple of unit), C bounded by the largest total cost over the
+// segments (or the minimum segment).
+bool step_one_window(int32_t num_reqs, int64_t nseg, int32_t max_seq_len, int max_items, int max_pages, int unit) {
+  const int64_t total_max = (int64_t)std::max(num_reqs, 0) * (pages_of(max_seq_len) + pa::kStepItemCost);
+  const int64_t c_max =
+      std::max<int64_t>(pa::kStepMinSegCost, (total_max + std::max<int64_t>(nseg, 1) - 1) / std::max<int64_t>(nseg, 1)) +
+      unit;
+  const bool items_fit = num_reqs + 1 <= max_items || c_max / (1 + pa::kStepItemCost) + 2 <= max_items;
+  return items_fit && c_max <= max_pages;
 }
 
 // Shared-prefix pass: the chunk count for a call and the workspace region
@@ -249,7 +254,8 @@ int concurrent_prefix_chunks(int64_t key_tiles, int64_t groups, int64_t decode_s
 // plan, returns the grid size (0 when there is nothing to do, -1 when no
 // valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
 int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
-                int page_offset, int num_kv_heads, int gcap, int slots, int unit, pa::DecodePlan& plan) {
+                int page_offset, int num_kv_heads, int gcap, int slots, int unit, int max_pages, int max_items,
+                pa::DecodePlan& plan) {
   std::vector<int32_t> pages(n);
   int64_t total = 0;  // pages of one kv head's stream
   int32_t longest = 0;
@@ -270,22 +276,22 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
   int64_t nseg = forced > 0 ? (forced + num_kv_heads - 1) / num_kv_heads
                             : std::min<int64_t>(std::max(slots / num_kv_heads, 1), (total + min_seg - 1) / min_seg);
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, seg_cap));
-  // a segment holds at most kDecodeMaxPagesPerCta pages; when that forces more
-  // segments than one wave has slots, use whole waves so no wave runs part-empty
+  // a segment holds at most max_pages pages; when that forces more segments
+  // than one wave has slots, use whole waves so no wave runs part-empty
   const int64_t wave = std::max<int64_t>(1, slots / num_kv_heads);
-  const int64_t need = (total + pa::kDecodeMaxPagesPerCta - 1) / pa::kDecodeMaxPagesPerCta;
+  const int64_t need = (total + max_pages - 1) / max_pages;
   if (forced <= 0 && need > nseg) nseg = std::min<int64_t>((need + wave - 1) / wave * wave, seg_cap);
   int64_t seg = (total + nseg - 1) / nseg;
   seg = std::max<int64_t>(seg, (total + seg_cap - 1) / seg_cap);
-  seg = (seg + unit - 1) / unit * unit;  // whole warp segments for the warp-granular kernel (unit 4)
-  seg = std::min<int64_t>(seg, pa::kDecodeMaxPagesPerCta);  // more segments if one would be too long
-  static_assert(pa::kDecodeMaxPagesPerCta % pa::kDecodeWarps == 0, "segments hold whole warp segments");
+  seg = (seg + unit - 1) / unit * unit;  // whole warp segments for the warp-granular kernel (unit kWgWarps)
+  seg = std::min<int64_t>(seg, max_pages / unit * unit);  // more segments if one would be too long
+  static_assert(pa::kWgMaxPagesPerCta % pa::kWgWarps == 0, "segments hold whole warp segments");
   for (;;) {
     const int ns = (int)((total + seg - 1) / seg);
     if (ns > seg_cap) return -1;
     // walk the row stream once: first row / page of every segment and the
     // most rows any segment touches
-    int64_t d = 0, d_start = 0, max_items = 0;
+    int64_t d = 0, d_start = 0, max_items_seen = 0;
     for (int sidx = 0; sidx < ns; ++sidx) {
       const int64_t S = (int64_t)sidx * seg, E = std::min(total, S + seg);
       while (d_start + pages[d] <= S) d_start += pages[d++];
@@ -296,9 +302,9 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
         ++cnt;
         st2 += pages[d2++];
       }
-      max_items = std::max(max_items, cnt);
+      max_items_seen = std::max(max_items_seen, cnt);
     }
-    if (max_items <= pa::kDecodeMaxItemsPerCta) {
+    if (max_items_seen <= max_items) {
       plan.n_rows = n;
       plan.seg = (int32_t)seg;
       plan.total = (int32_t)total;
@@ -600,6 +606,7 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     dp.lse = lse;
     dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
     dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
+    dp.piece_slots = wl.slots;
     dp.counters = reinterpret_cast<int*>(ws + wl.counters);
     dp.err = err;
     static thread_local pa::DecodePlan plan;
@@ -618,13 +625,24 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
       // pass runs beside the launch, or the timeout diagnostic is on), planned
       // again in whole warp segments for the warp-granular kernel
       const bool diag = !q8 && g_decode_fault.load() != 0;
-      int grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
-                             decode_slots, 1, plan);
-      const bool cta_granular =
-          grid > 0 && !concurrent && !diag && plan.seg < pa::kDecodeWarps * pa::kMinWarpSegPages;
-      if (grid > 0 && !cta_granular)
-        grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
-                           decode_slots, pa::kDecodeWarps, plan);
+      auto plan_cta = [&] {
+        return plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
+                           decode_slots, 1, pa::kDecodeMaxPagesPerCta, pa::kDecodeMaxItemsPerCta, plan);
+      };
+      int grid = plan_cta();
+      bool cta_granular = grid > 0 && !concurrent && !diag && plan.seg < pa::kDecodeWarps * pa::kMinWarpSegPages;
+      // the warp-granular kernel: one CTA per SM (a third of the CTA-granular
+      // slots and grid bound, so the workspace's pieces cover its warps)
+      static_assert(pa::kWgWarps <= kDecodeCtasPerSm * pa::kDecodeWarps, "warp-granular pieces fit the workspace");
+      if (grid > 0 && !cta_granular) {
+        grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads,
+                           gcap / kDecodeCtasPerSm, decode_slots / kDecodeCtasPerSm, pa::kWgWarps,
+                           pa::kWgMaxPagesPerCta, pa::kWgMaxItemsPerCta, plan);
+        if (grid < 0 && !concurrent && !diag) {  // no warp-granular plan within its limits
+          grid = plan_cta();
+          cta_granular = grid > 0;
+        }
+      }
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
       s = run_launch(PA_KERNEL_DECODE, "decode", stream,
@@ -833,6 +851,7 @@ pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, vo
   dp.lse = lse;
   dp.piece_o = reinterpret_cast<float*>(ws + wl.piece_o);
   dp.piece_lse = reinterpret_cast<float*>(ws + wl.piece_lse);
+  dp.piece_slots = wl.slots;
   dp.counters = reinterpret_cast<int*>(ws + wl.counters);
   dp.err = reinterpret_cast<int*>(ws);
   dp.k_new = static_cast<const uint16_t*>(k_new);
@@ -842,16 +861,23 @@ pa_status pa_decode_step(const void* q, const void* k_new, const void* v_new, vo
   pa::StepPlan plan;
   plan.n_rows = num_reqs;
   plan.max_seq_len = max_seq_len;
-  // the warp-granular kernel when every segment fits one window and the
+  // the warp-granular kernel (one CTA per SM: a third of the segments, so
+  // that its kWgWarps pieces per CTA fit the workspace's kDecodeWarps per
+  // CTA-granular CTA) when its segments fit one window and the CTA-granular
   // segments the bounds allow hold four warp segments of kMinWarpSegPages
   // (the same rule as the host plan's; from the bounds, so a captured launch
   // keeps its kernel)
   const int64_t nseg = std::max(1, grid / num_kv_heads);
+  const int64_t nseg_wg = nseg / kDecodeCtasPerSm;
+  static_assert(pa::kWgWarps <= kDecodeCtasPerSm * pa::kDecodeWarps, "warp-granular pieces fit the workspace");
   const int64_t seg_est = ((int64_t)num_reqs * (pages_of(max_seq_len) + pa::kStepItemCost) + nseg - 1) / nseg;
-  const bool warp_granular = step_one_window(num_reqs, num_kv_heads, max_seq_len, grid) &&
-                             seg_est >= pa::kDecodeWarps * pa::kMinWarpSegPages;
+  const bool warp_granular =
+      nseg_wg >= 1 &&
+      step_one_window(num_reqs, nseg_wg, max_seq_len, pa::kWgMaxItemsPerCta, pa::kWgMaxPagesPerCta, pa::kWgWarps) &&
+      seg_est >= pa::kDecodeWarps * pa::kMinWarpSegPages;
+  const int launch_grid = warp_granular ? (int)(nseg_wg * num_kv_heads) : grid;
   s = run_launch(PA_KERNEL_DECODE_STEP, "decode_step", stream,
-                 [&] { return pa::launch_decode_step(dp, plan, grid, warp_granular, stream); });
+                 [&] { return pa::launch_decode_step(dp, plan, launch_grid, warp_granular, stream); });
   return s == PA_OK ? ok() : s;
 }
 
