@@ -1367,10 +1367,10 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       }
     }
     __syncthreads();
-    // Beside a prefix pass (prefix_done set) this launch starts once every CTA
-    // of the pass has passed its own wait, so the kernels before the pass are
-    // complete; waiting here would wait for the pass itself.
-    if (!p.prefix_done) pdl_wait();
+    // Beside a tile kernel (p.beside) this launch starts once every CTA of
+    // that kernel has passed its own wait, so the kernels before it are
+    // complete; waiting here would wait for the tile kernel itself.
+    if (!p.beside) pdl_wait();
   }
   const int n_items = sm.n_items;
   if (n_items == 0) return;  // nothing covered (recorded above); no copy was issued
@@ -1780,6 +1780,9 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     }
     if (sm.q_issued[warp] > 0) mbar_wait_bounded(&sm.q_full[warp], (uint32_t)(sm.q_issued[warp] - 1) & 1u, kLimit);
   }
+  // beside a tile kernel: this launch completes after it (a warp that ends
+  // here waits for it; it never waits on this launch, so this ends)
+  if (p.beside) pdl_wait();
 }
 
 std::atomic<bool> g_decode_attr_set[4][kMaxDevices];

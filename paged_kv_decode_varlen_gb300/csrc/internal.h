@@ -120,6 +120,12 @@ struct DecodeParams {
   // readers returns both counters to zero.
   int* prefix_done;
   int* prefix_readers;
+  // 1: the tile kernel launched just before runs beside this launch (a
+  // prefix pass, or chunked-prefill jobs on SMs of their own).  Its CTAs
+  // waited for the kernels before it and then released this launch, which
+  // therefore skips its own wait at the start, and waits for that kernel at
+  // its end, so that this launch completes after it (stream order).
+  int32_t beside;
   int32_t total_q;
   uint16_t* out;         // bf16 [total_q, Hq, D]
   float* lse;            // [total_q, Hq] natural log, or null
@@ -248,7 +254,9 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodePlan& plan, int gri
 // pages), else the CTA-granular one (windows of rows)
 cudaError_t launch_decode_step(const DecodeParams& p, const StepPlan& plan, int grid, bool warp_granular,
                                cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
+// ctas: CTAs of the launch (0: one per (item, kv head) job; fewer run
+// several jobs each)
+cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps, int ctas,
                            cudaStream_t stream);
 cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream);
 cudaError_t launch_prefix_merge(const PrefixParams& p, int n_chunks, cudaStream_t stream);

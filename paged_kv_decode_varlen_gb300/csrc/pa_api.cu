@@ -250,6 +250,44 @@ int concurrent_prefix_chunks(int64_t key_tiles, int64_t groups, int64_t decode_s
   return best_chunks;
 }
 
+// Chunked-prefill jobs of a batch with decode rows: how many CTAs run them
+// beside the decode launch, which takes the other SMs (0: the jobs run first,
+// one CTA per job, and the decode launch after them on every SM).  job_tiles
+// holds each job's key tiles in the kernel's job order; CTA b of G takes job
+// b of every round of G jobs, in reverse order on odd rounds.  Measured
+// rates: a job takes ~5 us plus ~1 us per 128-key tile when it runs alone,
+// ~1.3x that beside the decode stream (the two share the DRAM), after ~4 us
+// of start; the decode launch streams ~54 GB/s per SM, at most ~6.5 TB/s,
+// plus ~12 us of start and row ends.  Of the CTA counts within 1 us of the
+// best the smallest is taken (the decode keeps the most SMs).  decode_slabs
+// counts (page, kv head) slabs of 8 KiB.
+int prefill_beside_ctas(const std::vector<int32_t>& job_tiles, int64_t decode_slabs) {
+  const int sms = sm_count();
+  const int64_t n = (int64_t)job_tiles.size();
+  if (n == 0 || decode_slabs == 0) return 0;
+  const double decode_bytes = (double)decode_slabs * 2 * pa::kSlabBytesHost;
+  auto decode_us = [&](int64_t free_sms) { return 12.0 + decode_bytes / std::min((double)free_sms * 54e3, 6.5e6); };
+  auto tiles_us = [&](int64_t G) {
+    std::vector<double> t((size_t)G, 0.0);
+    for (int64_t u = 0; u < n; ++u) {
+      const int64_t rnd = u / G, b = (rnd & 1) ? G - 1 - u % G : u % G;
+      t[(size_t)b] += 5.0 + 1.0 * job_tiles[(size_t)u];
+    }
+    return 4.0 + *std::max_element(t.begin(), t.end());
+  };
+  const double serial = tiles_us(std::min<int64_t>(n, sms)) + decode_us(sms);
+  std::vector<double> beside(sms / 2 + 1, INFINITY);
+  double best = INFINITY;
+  for (int g = 1; g <= sms / 2 && g < n; ++g) {
+    beside[g] = std::max(1.3 * tiles_us(g), decode_us(sms - g));
+    best = std::min(best, beside[g]);
+  }
+  if (best >= serial - 2.0) return 0;  // a clear gain only
+  for (int g = 1; g <= sms / 2; ++g)
+    if (beside[g] <= best + 1.0) return g;
+  return 0;
+}
+
 // Plan one persistent decode launch over decode rows rows[0..n): fills
 // plan, returns the grid size (0 when there is nothing to do, -1 when no
 // valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
@@ -546,9 +584,27 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     }
   }
 
+  int prefill_ctas = 0;  // CTAs of the prefill launch (0: one per job)
   if (!tiles.empty()) {
     // longest key extent first, so the big tiles do not form the tail
     std::stable_sort(tiles.begin(), tiles.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+    // The jobs beside the decode launch (decode rows of bf16 pages, no shared
+    // prefix, one launch of each): the tiles on a few SMs, the decode stream
+    // on the others.
+    if (P == 0 && !q8 && !decode_rows.empty() && decode_rows.size() <= (size_t)pa::kPlanMaxRows &&
+        tiles.size() <= (size_t)pa::kMaxPrefillItems && g_forced_ctas.load() <= 0 && g_decode_fault.load() == 0) {
+      std::vector<int32_t> job_tiles;
+      job_tiles.reserve(tiles.size() * num_kv_heads);
+      for (int h = 0; h < num_kv_heads; ++h)  // the kernel's job order when it runs several per CTA
+        for (const auto& t : tiles) job_tiles.push_back((t.first + pa::kTcKeyTile - 1) / pa::kTcKeyTile);
+      int64_t decode_pages = 0;
+      for (int32_t r : decode_rows) decode_pages += pages_of(seq_lens_host[r]);
+      prefill_ctas = prefill_beside_ctas(job_tiles, decode_pages * num_kv_heads);
+      if (prefill_ctas > 0) {
+        concurrent = true;
+        decode_slots = std::max(1, sm_count() - prefill_ctas) * kDecodeCtasPerSm;
+      }
+    }
     pa::PrefillParams pp;
     pp.q = static_cast<const uint16_t*>(q);
     pp.k_cache = static_cast<const uint16_t*>(k_cache);
@@ -575,7 +631,8 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
         items.req[i] = item_req[idx];
         items.q_start[i] = item_q0[idx];
       }
-      s = run_launch(PA_KERNEL_PREFILL, "prefill", stream, [&] { return pa::launch_prefill(pp, items, maps, stream); });
+      s = run_launch(PA_KERNEL_PREFILL, "prefill", stream,
+                     [&] { return pa::launch_prefill(pp, items, maps, prefill_ctas, stream); });
       if (s != PA_OK) return s;
     }
   }
@@ -598,9 +655,11 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     dp.prefix_lse = dec_prefix_lse;
     dp.prefix_n = dec_prefix_n;
     dp.prefix_rows = (int64_t)total_q * num_q_heads;
-    dp.prefix_done = concurrent ? reinterpret_cast<int*>(ws + pl.flags) : nullptr;
-    dp.prefix_readers = concurrent ? reinterpret_cast<int*>(ws + pl.flags) + prefix_qtiles(total_q) * num_kv_heads
-                                   : nullptr;
+    dp.prefix_done = concurrent && P > 0 ? reinterpret_cast<int*>(ws + pl.flags) : nullptr;
+    dp.prefix_readers = concurrent && P > 0
+                            ? reinterpret_cast<int*>(ws + pl.flags) + prefix_qtiles(total_q) * num_kv_heads
+                            : nullptr;
+    dp.beside = concurrent ? 1 : 0;
     dp.total_q = total_q;
     dp.out = static_cast<uint16_t*>(out);
     dp.lse = lse;

@@ -13,10 +13,15 @@
 // query) and merged with each request's own part by log-sum-exp.
 //
 // Design (QK^T and PV are dense contractions):
-//   * One CTA per (32-query tile, kv head [, key chunk]).  The 4 q heads of
-//     the GQA group are packed into the M dimension: 32 tokens x 4 heads =
-//     128 rows = the M of one tcgen05.mma, so every K/V tile serves all four
-//     heads.  Keys go in tiles of 128 (8 pages).
+//   * One CTA per (32-query tile, kv head [, key chunk]), or, for the
+//     chunked-prefill jobs of a batch that also has decode rows, a few
+//     persistent CTAs that run the jobs one after another beside the decode
+//     launch on the other SMs (a chunked-prefill step mixes compute-bound
+//     and memory-bound work: the serving page "vLLM, SGLang и непрерывный
+//     батчинг", section "Непрерывный батчинг").  The 4 q heads of the GQA
+//     group are packed into the M dimension: 32 tokens x 4 heads = 128 rows
+//     = the M of one tcgen05.mma, so every K/V tile serves all four heads.
+//     Keys go in tiles of 128 (8 pages).
 //   * Warp roles: warps 4 and 6 issue tiled TMA copies (Q once; per key tile
 //     the two 64-dim halves of each page's K slab, resp. V slab, 128-byte
 //     swizzled, into a 4-stage K ring and a 2-stage V ring: a K stage is
@@ -39,6 +44,8 @@
 //     returns.
 #include <math.h>
 #include <stddef.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -124,16 +131,32 @@ struct TcJob {
   const int32_t* table;
 };
 
-// Runs the tile.  Each softmax thread calls `stage(row, o, m, l, smem)` with
+// A CTA's place in its pipelines, carried from one job to the next: the key
+// tiles and jobs it has run.  Every ring stage, barrier phase and tensor-
+// memory buffer is indexed by the CTA's running tile count J (tile j of a
+// job is J = tiles + j) and bar_q by the job count, so a persistent CTA runs
+// job after job without re-initialising anything.
+struct TcPos {
+  int tiles = 0;
+  int jobs = 0;
+};
+
+// Runs one job.  Each softmax thread calls `stage(row, o, m, l, smem)` with
 // its row's unnormalised O (4 x 32 fp32), running max (log2 domain) and
 // sum, to leave its output row in the 64 KiB staging area `smem`; after a
 // barrier of the softmax warps each of their threads calls `store(t, smem)`
-// (t = 0 .. 127) to copy the staged rows out with contiguous stores.
+// (t = 0 .. 127) to copy the staged rows out with contiguous stores.  The
+// CTA's first job initialises the barriers and allocates the tensor memory
+// (tc_finish frees it); every job ends with a CTA barrier, after which the
+// staging area, Q and the tensor memory are free for the next.
 template <bool kCausal, class Stage, class Store>
 __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, int num_kv_heads, int64_t num_blocks,
-                                         float scale_log2, int* err, Stage&& stage, Store&& store) {
+                                         float scale_log2, int* err, TcPos& pos, Stage&& stage, Store&& store) {
   TcSmem& sm = tc_smem();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int J0 = pos.tiles;
+  const bool first = pos.jobs == 0;
+  const uint32_t q_par = (uint32_t)pos.jobs & 1u;
   const int n_tiles = (job.k_hi - job.k_lo + kKeys - 1) / kKeys;
   const int first_page = job.k_lo / kPage;
   const int last_page = (job.k_hi - 1) / kPage;
@@ -161,29 +184,34 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
   }
 
   if (is_k && lane == 0) {
-    mbar_init(&sm.bar_q, 1);
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
+    if (first) {
+      mbar_init(&sm.bar_q, 1);
+      for (int s = 0; s < kKStages; ++s) {
+        mbar_init(&sm.k_full[s], 1);
+        mbar_init(&sm.k_empty[s], 1);
+      }
+      for (int s = 0; s < kVStages; ++s) mbar_init(&sm.v_full[s], 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&sm.s_full[b], 1);
+        mbar_init(&sm.p_full[b], kSoftmaxWarps * 32);
+        mbar_init(&sm.pv_done[b], 1);
+      }
+      sm.abort = 0;
+      fence_mbar_init();
+      prefetch_tensormap(&maps.q);
     }
-    for (int s = 0; s < kVStages; ++s) mbar_init(&sm.v_full[s], 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.p_full[b], kSoftmaxWarps * 32);
-      mbar_init(&sm.pv_done[b], 1);
-    }
-    sm.abort = 0;
-    fence_mbar_init();
-    // Q first: its copy overlaps the rest of the set-up
-    prefetch_tensormap(&maps.q);
+    // Q first: its copy overlaps the rest of the set-up (the previous job's
+    // closing barrier freed the buffer)
     mbar_arrive_expect_tx(&sm.bar_q, kTileBytes);
     tma_load_3d(sm.q, &maps.q, 0, job.kvh * kGroup, job.tok0, &sm.bar_q);
     tma_load_3d(sm.q + kHalf, &maps.q, 64, job.kvh * kGroup, job.tok0, &sm.bar_q);
   }
-  if (warp == kMmaWarp) tmem_alloc(&sm.tmem, kTmemCols);
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+  if (first) {
+    if (warp == kMmaWarp) tmem_alloc(&sm.tmem, kTmemCols);
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+  }
   const uint32_t tmem = sm.tmem;
 
   if (is_producer) {
@@ -201,8 +229,9 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
     for (int s = 0; s < kKStages; ++s) last_issued[s] = -1;
     if (lane == 0) prefetch_tensormap(map);
     for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % n_st;
-      if (j >= n_st && !__all_sync(0xffffffffu, tc_wait(sm, &empty[s], ((j / n_st) - 1) & 1, err))) break;
+      const int J = J0 + j;
+      const int s = J % n_st;
+      if (J >= n_st && !__all_sync(0xffffffffu, tc_wait(sm, &empty[s], ((J / n_st) - 1) & 1, err))) break;
       if (j > 0 && (j & 3) == 0) {
         grp_cur = grp_next;
         grp_next = load_group((j >> 2) + 1);
@@ -216,11 +245,11 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
         tma_load_2d(dst + off, map, 0, row, &full[s]);
         tma_load_2d(dst + kHalf + off, map, 64, row, &full[s]);
       }
-      last_issued[s] = j;
+      last_issued[s] = J;
     }
     if (*reinterpret_cast<volatile int*>(&sm.abort) && lane == 0) {
       // let the copies in flight land before the CTA leaves (bounded)
-      if (is_k) mbar_wait_bounded(&sm.bar_q, 0);
+      if (is_k) mbar_wait_bounded(&sm.bar_q, q_par);
       for (int s = 0; s < n_st; ++s)
         if (last_issued[s] >= 0) mbar_wait_bounded(&full[s], (last_issued[s] / n_st) & 1);
     }
@@ -230,39 +259,41 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       const uint32_t qb = smem_addr(sm.q);
       int last_s = -1, last_pv = -1;  // last S / PV issued
       auto issue_s = [&](int j) -> bool {
-        const int s = j % kKStages;
-        if (!tc_wait(sm, &sm.k_full[s], (j / kKStages) & 1, err)) return false;
+        const int J = J0 + j;
+        const int s = J % kKStages;
+        if (!tc_wait(sm, &sm.k_full[s], (J / kKStages) & 1, err)) return false;
         fence_after_sync();
-        last_s = j;
+        last_s = J;
         const uint32_t kb = smem_addr(sm.k[s]);
-        const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * kKeys;
+        const uint32_t d = tmem + kColS + (uint32_t)(J & 1) * kKeys;
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;  // 64-dim half, 16-dim step in it
           mma_bf16(d, desc_sw128(qb + off, 16, 1024), desc_sw128(kb + off, 16, 1024), kIdescS, ks > 0);
         }
-        commit(&sm.s_full[j & 1]);  // one commit per MMA group and barrier
+        commit(&sm.s_full[J & 1]);  // one commit per MMA group and barrier
         commit(&sm.k_empty[s]);
         return true;
       };
       // S runs one tile ahead: S(j + 1) is queued before PV(j), which waits
       // for the softmax of tile j
-      bool ok = tc_wait(sm, &sm.bar_q, 0, err) && issue_s(0);
+      bool ok = tc_wait(sm, &sm.bar_q, q_par, err) && issue_s(0);
       for (int j = 0; ok && j < n_tiles; ++j) {
         if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-        const int s = j % kVStages;
-        ok = tc_wait(sm, &sm.p_full[j & 1], (j >> 1) & 1, err) && tc_wait(sm, &sm.v_full[s], (j / kVStages) & 1, err);
+        const int J = J0 + j;
+        const int s = J % kVStages;
+        ok = tc_wait(sm, &sm.p_full[J & 1], (J >> 1) & 1, err) && tc_wait(sm, &sm.v_full[s], (J / kVStages) & 1, err);
         if (!ok) break;
         fence_after_sync();
-        const uint32_t pt = tmem + kColP + (uint32_t)(j & 1) * (kKeys / 2), vb = smem_addr(sm.v[s]);
+        const uint32_t pt = tmem + kColP + (uint32_t)(J & 1) * (kKeys / 2), vb = smem_addr(sm.v[s]);
 #pragma unroll
         for (int ks = 0; ks < kKeys / 16; ++ks) {
           const uint32_t va = vb + ks * 2 * 1024;  // 16 keys = two 8-row groups
           // A = P in tensor memory: 16 keys = 8 columns of bf16 pairs
           mma_bf16_ts(tmem + kColO, pt + 8 * ks, desc_sw128(va, kHalf, 1024), kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        commit(&sm.pv_done[j & 1]);
-        last_pv = j;
+        commit(&sm.pv_done[J & 1]);
+        last_pv = J;
       }
       // every MMA issued has completed before the CTA frees its tensor memory:
       // the PVs form one chain on O, and the S products were each waited for
@@ -279,7 +310,8 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.s_full[j & 1], (j >> 1) & 1, err));
+      const int J = J0 + j;
+      ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.s_full[J & 1], (J >> 1) & 1, err));
       if (!ok) break;
       fence_after_sync();
       // scores of this row, scaled into the log2 domain in pairs
@@ -287,7 +319,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       {
         uint32_t raw[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32_async(lane_base + kColS + (uint32_t)(j & 1) * kKeys + 32 * c, raw[c]);
+        for (int c = 0; c < 4; ++c) tmem_ld32_async(lane_base + kColS + (uint32_t)(J & 1) * kKeys + 32 * c, raw[c]);
         tmem_wait_ld(raw[0], raw[1], raw[2], raw[3]);
         const float2 sc2 = make_float2(scale_log2, scale_log2);
 #pragma unroll
@@ -323,7 +355,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O is rescaled: PV of tile j - 1 must be done (and with it every
         // earlier PV: they form one chain on O), so O is stable
-        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, err));
+        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[(J - 1) & 1], ((J - 1) >> 1) & 1, err));
         if (!ok) break;
         fence_after_sync();
         // rescale the rows of O whose running max grew
@@ -336,11 +368,13 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
           tmem_st32(lane_base + kColO + 32 * c, o);
         }
       } else if (j >= 2) {
-        // P buffer j & 1 was last read by PV of tile j - 2, which must be done
+        // P buffer J & 1 was last read by PV of tile J - 2, which must be done
         // before it is rewritten (an S product goes to another accumulator
-        // and may finish before it).  PV of tile j - 1 may still run: the
-        // exponentials below overlap it.
-        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[j & 1], ((j - 2) >> 1) & 1, err));
+        // and may finish before it).  PV of tile J - 1 may still run: the
+        // exponentials below overlap it.  (The previous job's PVs are all
+        // done: its softmax waited for the last one before its closing
+        // barrier.)
+        ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[J & 1], ((J - 2) >> 1) & 1, err));
         if (!ok) break;
         fence_after_sync();
       }
@@ -350,7 +384,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
 #pragma unroll
       for (int i = 0; i < 4; ++i) ls4[i] = make_float2(0.f, 0.f);
       // P of this row: 128 bf16 keys as 64 pairs, into this lane's P columns
-      const uint32_t prow = lane_base + kColP + (uint32_t)(j & 1) * (kKeys / 2);
+      const uint32_t prow = lane_base + kColP + (uint32_t)(J & 1) * (kKeys / 2);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {  // keys 64 hf .. + 63 = P columns 32 hf .. + 31
         uint32_t w[32];
@@ -366,9 +400,10 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       const float2 l2 = __fadd2_rn(__fadd2_rn(ls4[0], ls4[1]), __fadd2_rn(ls4[2], ls4[3]));
       l_run += l2.x + l2.y;
       fence_before_sync();  // the tensor-memory reads / writes above precede the arrive
-      mbar_arrive(&sm.p_full[j & 1]);
+      mbar_arrive(&sm.p_full[J & 1]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, err));
+    const int J_last = J0 + n_tiles - 1;
+    if (ok) ok = __all_sync(0xffffffffu, tc_wait(sm, &sm.pv_done[J_last & 1], (J_last >> 1) & 1, err));
     if (ok) {
       fence_after_sync();
       float o[4][32];
@@ -385,40 +420,66 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  pos.tiles += n_tiles;
+  pos.jobs += 1;
 }
 
-// Chunked-prefill rows: grid (work item, kv head); item = (request, first
-// query of a 32-token tile).  Keys [kv_key_offset, position of the tile's
-// last query] with the causal mask; the shared-prefix partial, if given, is
-// folded in before the bf16 rounding.
+// After a CTA's last job (all threads): frees the tensor memory.
+__device__ __forceinline__ void tc_finish(const TcPos& pos) {
+  if (pos.jobs > 0 && (threadIdx.x >> 5) == kMmaWarp) tmem_dealloc(tc_smem().tmem, kTmemCols);
+}
+
+// Chunked-prefill rows: jobs (work item, kv head), item = (request, first
+// query of a 32-token tile), items sorted by key extent, longest first.  Keys
+// [kv_key_offset, position of the tile's last query] with the causal mask;
+// the shared-prefix partial, if given, is folded in before the bf16
+// rounding.  One CTA per job, or fewer CTAs that run several jobs each (a
+// prefill pass beside a decode launch on the other SMs): CTA b takes job b
+// of every round of gridDim.x jobs, in reverse order on odd rounds, so the
+// long and the short jobs even out.
+// kPersist: a grid of fewer CTAs than jobs (a separate instantiation: the
+// job loop's registers would weigh on the one-job launches).
+template <bool kPersist>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const PrefillParams p, const __grid_constant__ PrefillItems items,
                    const __grid_constant__ TcMaps maps) {
-  pdl_launch_dependents();
+  // the wait comes first: a decode launch that runs beside this pass starts
+  // once every CTA here has released it, and so after the kernels before
+  // this one have completed
   pdl_wait();
-  const int r = items.req[blockIdx.x];
-  const int j0 = items.q_start[blockIdx.x];
-  const int qo0 = p.qo_indptr[r];
-  const int c = p.qo_indptr[r + 1] - qo0;
-  const int L = p.seq_lens[r];
-  TcJob job;
-  job.tok0 = qo0 + j0;
-  job.nq = min(kTok, c - j0);
-  job.kvh = blockIdx.y;
-  job.pos0 = L - c + j0;
-  job.k_lo = p.kv_key_offset;
-  job.k_hi = job.pos0 + job.nq;
-  job.table = p.block_tables + (size_t)r * p.max_blocks_per_req;
-  // metadata that differ from the host plan: record and leave (uniformly,
-  // before any barrier or tensor memory is touched)
-  if (job.nq <= 0 || job.k_hi <= job.k_lo || (job.k_hi - 1) / kPage >= p.max_blocks_per_req) {
-    if (threadIdx.x == 0) record_error(p.err, PA_ERR_DEVICE_INDEX);
-    return;
-  }
-  // staged bf16 rows: 256 B per row, 16-byte chunk c at c ^ (row & 15)
-  run_tile<true>(
-      job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err,
+  pdl_launch_dependents();
+  const int n_jobs = items.count * p.num_kv_heads;
+  const int G = kPersist ? (int)gridDim.x : n_jobs;
+  TcPos pos;
+  for (int rnd = 0; rnd * G < n_jobs; ++rnd) {
+    const int u = kPersist ? rnd * G + ((rnd & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x) : (int)blockIdx.x;
+    if (u >= n_jobs) continue;
+    // one job per CTA: (item, kv head), kv head fastest (dispatch order:
+    // the longest items first); several per CTA: kv-head-major, so the jobs
+    // running at the same time share a kv head's keys in L2
+    const int it = kPersist ? u % items.count : u / p.num_kv_heads;
+    const int r = items.req[it];
+    const int j0 = items.q_start[it];
+    const int qo0 = p.qo_indptr[r];
+    const int c = p.qo_indptr[r + 1] - qo0;
+    const int L = p.seq_lens[r];
+    TcJob job;
+    job.tok0 = qo0 + j0;
+    job.nq = min(kTok, c - j0);
+    job.kvh = kPersist ? u / items.count : u % p.num_kv_heads;
+    job.pos0 = L - c + j0;
+    job.k_lo = p.kv_key_offset;
+    job.k_hi = job.pos0 + job.nq;
+    job.table = p.block_tables + (size_t)r * p.max_blocks_per_req;
+    // metadata that differ from the host plan: record and skip the job
+    // (uniformly: every thread of the CTA reads the same values)
+    if (job.nq <= 0 || job.k_hi <= job.k_lo || (job.k_hi - 1) / kPage >= p.max_blocks_per_req) {
+      if (threadIdx.x == 0) record_error(p.err, PA_ERR_DEVICE_INDEX);
+      continue;
+    }
+    // staged bf16 rows: 256 B per row, 16-byte chunk c at c ^ (row & 15)
+    run_tile<true>(
+        job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err, pos,
       [&](int row, float (&o)[4][32], float m, float l, uint8_t* stg) {
         const size_t orow = (size_t)(job.tok0 + (row >> 2)) * p.num_q_heads + job.kvh * kGroup + (row & 3);
         const bool valid = (row >> 2) < job.nq;
@@ -467,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<const uint4*>(stg + row * 256 + ((c ^ (row & 15)) << 4));
         }
       });
+    if (!kPersist || *reinterpret_cast<volatile int*>(&tc_smem().abort)) break;  // (a wait gave up: recorded)
+  }
+  tc_finish(pos);
 }
 
 // Shared-prefix pass: grid (key chunk, kv head, 32-token tile of all the
@@ -499,8 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
   float* dst_o = direct ? p.prefix_o : p.chunk_o + (size_t)blockIdx.x * p.total_q * p.num_q_heads * kHeadDim;
   float* dst_lse = direct ? p.prefix_lse : p.chunk_lse + (size_t)blockIdx.x * p.total_q * p.num_q_heads;
   // staged fp32 rows: 512 B per row, 16-byte chunk c at c ^ (row & 31)
+  TcPos pos;
   run_tile<false>(
-      job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err,
+      job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err, pos,
       [&](int row, float (&o)[4][32], float m, float l, uint8_t* stg) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -528,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
   // release publishes them to the folds that acquire the count (also after
   // a recorded timeout, so no fold waits for a chunk that will not come)
   if (done && threadIdx.x == 0) red_add_release_gpu(done, 1);
+  tc_finish(pos);
 }
 
 // Merge of the prefix pass's key-chunk partials: one warp per (query token,
@@ -580,7 +646,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) prefix_merge_kernel(const Pr
   if (lane == 0) p.prefix_lse[row] = wsum > 0.f ? M + log2f(wsum) : -INFINITY;
 }
 
-std::atomic<bool> g_prefill_attr_set[kMaxDevices];
+std::atomic<bool> g_prefill_attr_set[2][kMaxDevices];
 std::atomic<bool> g_prefix_attr_set[kMaxDevices];
 
 cudaError_t set_smem_attr(const void* fn, std::atomic<bool>* done) {
@@ -589,13 +655,18 @@ cudaError_t set_smem_attr(const void* fn, std::atomic<bool>* done) {
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps,
+cudaError_t launch_prefill(const PrefillParams& p, const PrefillItems& items, const TcMaps& maps, int ctas,
                            cudaStream_t stream) {
   if (items.count <= 0) return cudaSuccess;
-  cudaError_t e = set_smem_attr((const void*)prefill_kernel, g_prefill_attr_set);
+  const int jobs = items.count * p.num_kv_heads;
+  if (ctas > 0 && ctas < jobs) {
+    cudaError_t e = set_smem_attr((const void*)prefill_kernel<true>, g_prefill_attr_set[1]);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(prefill_kernel<true>, dim3(ctas), dim3(kThreads), kSmemBytes, stream, p, items, maps);
+  }
+  cudaError_t e = set_smem_attr((const void*)prefill_kernel<false>, g_prefill_attr_set[0]);
   if (e != cudaSuccess) return e;
-  return launch_pdl(prefill_kernel, dim3(items.count, p.num_kv_heads), dim3(kThreads), kSmemBytes, stream, p, items,
-                    maps);
+  return launch_pdl(prefill_kernel<false>, dim3(jobs), dim3(kThreads), kSmemBytes, stream, p, items, maps);
 }
 
 cudaError_t launch_prefix(const PrefixParams& p, int n_chunks, const TcMaps& maps, cudaStream_t stream) {
