@@ -111,3 +111,24 @@ def test_noalloc_scratch_bounds():
                                       seq.cuda(), ind.cuda(), 0.088, seq_lens_host=seq, qo_indptr_host=ind)
     assert e.value.status == B.PA_ERR_UNSUPPORTED
     assert "scratch" in str(e.value)
+
+
+def test_noalloc_in_a_captured_graph_replays_exactly():
+    # the first call on a device looks up the scratch array (before any
+    # capture); a call captured into a CUDA graph then replays with the same
+    # results as the workspace call, replay after replay
+    B.pa_set_decode_ctas(0)
+    args, kw, ref_out, ref_lse = _prepared("short", 0.25)
+    ws_out, ws_lse = B.pa_attention_varlen(*args, **kw)
+    B.pa_attention_varlen_noalloc(*args, **kw)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        out, lse = B.pa_attention_varlen_noalloc(*args, **kw)
+    for replay in range(2):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ws_out), f"replay {replay}: differs from pa_attention_varlen"
+        assert torch.equal(lse, ws_lse), f"replay {replay}: lse differs from pa_attention_varlen"
+    compare(out, ref_out, lse, ref_lse, what="noalloc graph replay vs oracle")
