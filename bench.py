@@ -411,6 +411,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="short")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-ctas", type=int, default=0, help="force the persistent decode grid size (0 = automatic)")
+    ap.add_argument("--prefill-ctas", type=int, default=0,
+                    help="CTAs of the prefill jobs beside the decode launch (0 = automatic, -1 = the jobs first)")
     ap.add_argument("--sweep", action="store_true",
                     help="36-layer decode sweep (b in 1..128 at 2048 and 8192-with-shared-prefix), one JSON line "
                          "per point, 36 x (append + attention) captured in a CUDA graph")
@@ -442,6 +444,7 @@ def main():
     from paged_kv_decode_varlen_gb300 import binding as B
 
     B.pa_set_decode_ctas(args.decode_ctas)
+    B.pa_set_prefill_ctas(args.prefill_ctas)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     if world > 1:
@@ -643,7 +646,8 @@ def main():
                    "attention_call": ("pa_decode_step (append + attention in one launch)" if use_step
                                       else call_name(ppages)),
                    "bytes_per_step": sb["unique"], "logical_bytes_per_step": sb["logical"],
-                   "query_tokens_per_step": sb["query_tokens"]},
+                   "query_tokens_per_step": sb["query_tokens"],
+                   **({"prefill_ctas": args.prefill_ctas} if args.prefill_ctas else {})},
         "tokens_per_layer_step_per_s": round(sb["query_tokens"] * world / (t_step * 1e-3), 1),
         "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
         "roofline": {"bound": bound, "kernel": dom, "achieved": round(achieved, 2) if achieved else None,

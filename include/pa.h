@@ -426,9 +426,17 @@ pa_status pa_clear_device_error(void* workspace, pa_stream_t stream);
  * Tuning and diagnostics.
  *   pa_set_decode_ctas(n): n > 0 asks for a persistent decode grid of n CTAs
  *     (capped by the plan limits and the workspace bound), 0 restores the
- *     automatic plan (3 CTAs per SM).  Process-wide.  pa_decode_step and
+ *     automatic plan (one CTA per SM for the warp-granular kernel, three
+ *     per SM for the CTA-granular one).  Process-wide.  pa_decode_step and
  *     pa_decode_step_workspace_size use it too (rounded up to whole kv
  *     heads, and raised where a segment would exceed 1024 pages).
+ *   pa_set_prefill_ctas(n): for a call whose batch has decode rows and rows
+ *     with qo_len > 1 (bf16 pages, no shared prefix, no forced decode grid):
+ *     n > 0 runs the tensor-core jobs of the qo_len > 1 rows on n persistent
+ *     CTAs beside the decode launch (at most one fewer than the jobs and
+ *     half the SMs), -1 never (the jobs first, one CTA each, then the decode
+ *     launch), 0 restores the automatic choice (a cost model).
+ *     Process-wide; n outside [-1, 1024] gives PA_ERR_INVALID_ARG.
  *   pa_launch_count(): kernels this library has launched in this process.
  *   pa_trace_enable(1): from now on every launch records a CUDA event before
  *     and after itself on its stream (at most 16384 launches are kept; the
@@ -450,6 +458,7 @@ typedef enum {
 } pa_kernel_kind;
 
 pa_status pa_set_decode_ctas(int32_t n);
+pa_status pa_set_prefill_ctas(int32_t n);
 /*
  * pa_set_decode_fault_injection(on) -- a test of the bounded-wait path, off
  * (0) by default, process-wide.  With on = 1, decode launches of

@@ -69,6 +69,7 @@ _SIGS = {
     "pa_get_device_error": (_i32, [_P, ctypes.POINTER(_i32)]),
     "pa_clear_device_error": (_i32, [_P, _P]),
     "pa_set_decode_ctas": (_i32, [_i32]),
+    "pa_set_prefill_ctas": (_i32, [_i32]),
     "pa_set_decode_fault_injection": (_i32, [_i32]),
     "pa_launch_count": (_i64, []),
     "pa_trace_enable": (_i32, [_i32]),
@@ -439,6 +440,12 @@ def pa_clear_device_error(workspace, stream=None):
 
 def pa_set_decode_ctas(n: int):
     _check(_lib.pa_set_decode_ctas(int(n)))
+
+
+def pa_set_prefill_ctas(n: int):
+    """Prefill jobs beside the decode launch: n > 0 CTAs, -1 never, 0
+    automatic (see include/pa.h)."""
+    _check(_lib.pa_set_prefill_ctas(int(n)))
 
 
 def pa_set_decode_fault_injection(on: bool):

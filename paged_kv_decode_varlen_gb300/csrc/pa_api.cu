@@ -24,6 +24,7 @@ namespace {
 thread_local char g_msg[512] = "";
 std::atomic<int64_t> g_launches{0};
 std::atomic<int32_t> g_forced_ctas{0};
+std::atomic<int32_t> g_prefill_ctas{0};  // pa_set_prefill_ctas: > 0 forced, -1 never, 0 automatic
 std::atomic<int32_t> g_decode_fault{0};  // pa_set_decode_fault_injection
 
 pa_status fail(pa_status s, const char* fmt, ...) {
@@ -591,15 +592,22 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     // The jobs beside the decode launch (decode rows of bf16 pages, no shared
     // prefix, one launch of each): the tiles on a few SMs, the decode stream
     // on the others.
+    const int forced_p = g_prefill_ctas.load();
     if (P == 0 && !q8 && !decode_rows.empty() && decode_rows.size() <= (size_t)pa::kPlanMaxRows &&
-        tiles.size() <= (size_t)pa::kMaxPrefillItems && g_forced_ctas.load() <= 0 && g_decode_fault.load() == 0) {
-      std::vector<int32_t> job_tiles;
-      job_tiles.reserve(tiles.size() * num_kv_heads);
-      for (int h = 0; h < num_kv_heads; ++h)  // the kernel's job order when it runs several per CTA
-        for (const auto& t : tiles) job_tiles.push_back((t.first + pa::kTcKeyTile - 1) / pa::kTcKeyTile);
-      int64_t decode_pages = 0;
-      for (int32_t r : decode_rows) decode_pages += pages_of(seq_lens_host[r]);
-      prefill_ctas = prefill_beside_ctas(job_tiles, decode_pages * num_kv_heads);
+        tiles.size() <= (size_t)pa::kMaxPrefillItems && g_forced_ctas.load() <= 0 && g_decode_fault.load() == 0 &&
+        forced_p >= 0) {
+      const int jobs = (int)tiles.size() * num_kv_heads;
+      if (forced_p > 0) {
+        prefill_ctas = std::min(forced_p, std::min(jobs - 1, sm_count() / 2));
+      } else {
+        std::vector<int32_t> job_tiles;
+        job_tiles.reserve((size_t)jobs);
+        for (int h = 0; h < num_kv_heads; ++h)  // the kernel's job order when it runs several per CTA
+          for (const auto& t : tiles) job_tiles.push_back((t.first + pa::kTcKeyTile - 1) / pa::kTcKeyTile);
+        int64_t decode_pages = 0;
+        for (int32_t r : decode_rows) decode_pages += pages_of(seq_lens_host[r]);
+        prefill_ctas = prefill_beside_ctas(job_tiles, decode_pages * num_kv_heads);
+      }
       if (prefill_ctas > 0) {
         concurrent = true;
         decode_slots = std::max(1, sm_count() - prefill_ctas) * kDecodeCtasPerSm;
@@ -1011,6 +1019,13 @@ pa_status pa_set_decode_ctas(int32_t n) {
   if (n < 0 || n > pa::kPlanMaxCtas)
     return fail(PA_ERR_INVALID_ARG, "decode grid %d outside [0, %d]", n, pa::kPlanMaxCtas);
   g_forced_ctas.store(n);
+  return ok();
+}
+
+pa_status pa_set_prefill_ctas(int32_t n) {
+  if (n < -1 || n > pa::kPlanMaxCtas)
+    return fail(PA_ERR_INVALID_ARG, "prefill CTAs %d outside [-1, %d]", n, pa::kPlanMaxCtas);
+  g_prefill_ctas.store(n);
   return ok();
 }
 
