@@ -705,7 +705,11 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
         grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads,
                            gcap / kDecodeCtasPerSm, decode_slots / kDecodeCtasPerSm, pa::kWgWarps,
                            pa::kWgMaxPagesPerCta, pa::kWgMaxItemsPerCta, plan);
-        if (grid < 0 && !concurrent && !diag) {  // no warp-granular plan within its limits
+        // no warp-granular plan within its limits: the CTA-granular kernel
+        // (beside prefill jobs too: it waits for them at its start, so they
+        // run first; beside a prefix pass it cannot run, as it does not fold
+        // the pass's chunks)
+        if (grid < 0 && (!concurrent || P == 0) && !diag) {
           grid = plan_cta();
           cta_granular = grid > 0;
         }
