@@ -107,6 +107,11 @@ def test_grid_override_bounds():
     assert lib.pa_set_decode_ctas(1025) == b.PA_ERR_INVALID_ARG
     assert lib.pa_set_decode_ctas(-1) == b.PA_ERR_INVALID_ARG
     assert lib.pa_set_decode_ctas(0) == b.PA_OK
+    assert lib.pa_set_prefill_ctas(-2) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_prefill_ctas(1025) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_set_prefill_ctas(-1) == b.PA_OK
+    assert lib.pa_set_prefill_ctas(16) == b.PA_OK
+    assert lib.pa_set_prefill_ctas(0) == b.PA_OK
 
 
 def test_fault_injection_switch_bounds():
