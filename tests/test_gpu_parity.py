@@ -167,6 +167,10 @@ EDGE = {
     "mixed_prefill_decode": ([300, 2000, 1500, 17], [33, 1, 64, 1]),
     "long_prefill_chunk": ([2048], [512]),
     "all_empty": ([10, 20], [0, 0]),
+    # more decode rows than one launch's plan carries (1024): two launches
+    "decode_rows_over_one_launch": ([int(x) for x in np.random.default_rng(5).integers(1, 60, 1100)], [1] * 1100),
+    # one 128K-token row: 8192 pages cut over every segment of each kv head
+    "one_long_row_128k": ([131072], [1]),
 }
 
 
