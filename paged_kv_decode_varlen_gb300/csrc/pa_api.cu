@@ -612,6 +612,18 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
         concurrent = true;
         decode_slots = std::max(1, sm_count() - prefill_ctas) * kDecodeCtasPerSm;
       }
+    } else if (P == 0 && decode_rows.empty() && forced_p >= 0 && !q8 &&
+               tiles.size() <= (size_t)pa::kMaxPrefillItems && g_forced_ctas.load() <= 0 &&
+               g_decode_fault.load() == 0) {
+      // a batch of tile jobs alone: with at least two jobs per SM (or when
+      // forced), persistent CTAs, one per SM, each running its jobs in turn
+      // with the next one's start overlapping this one's end (verify rows:
+      // 118.3 -> 116.3 us); fewer jobs keep one CTA each
+      const int jobs = (int)tiles.size() * num_kv_heads;
+      if (forced_p > 0)
+        prefill_ctas = std::min(forced_p, jobs - 1);
+      else if (jobs >= 2 * sm_count())
+        prefill_ctas = sm_count();
     }
     pa::PrefillParams pp;
     pp.q = static_cast<const uint16_t*>(q);

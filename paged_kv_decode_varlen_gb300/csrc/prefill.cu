@@ -88,6 +88,8 @@ struct __align__(1024) TcSmem {
   uint64_t pv_done[2];  // PV of tile j done: phase j / 2 of pv_done[j % 2]
   uint64_t s_full[2];
   uint64_t p_full[2];
+  uint64_t q_free;  // a job's last S product done: Q may be reloaded (jobs in turn without a CTA barrier)
+  uint64_t o_free;  // the softmax warps have read a job's O: the next job's first PV may overwrite it
   uint32_t tmem;
   int abort;
 };
@@ -149,7 +151,16 @@ struct TcPos {
 // CTA's first job initialises the barriers and allocates the tensor memory
 // (tc_finish frees it); every job ends with a CTA barrier, after which the
 // staging area, Q and the tensor memory are free for the next.
-template <bool kCausal, class Stage, class Store>
+//
+// kOverlap (several jobs per CTA): no barrier between jobs, so the next
+// job's block ids, Q, first K and V tiles and first S product overlap this
+// job's last tile and epilogue.  Q is reloaded once the job's last S product
+// has completed (q_free), the next job's first PV overwrites O once every
+// softmax thread has read it (o_free), and the epilogue stores each row from
+// registers (`stage(row, o, m, l, nullptr)`, no staging area: the K and V
+// stages already hold the next job's tiles; `store` is not called).  The
+// caller ends the last job with a CTA barrier before tc_finish.
+template <bool kCausal, bool kOverlap, class Stage, class Store>
 __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, int num_kv_heads, int64_t num_blocks,
                                          float scale_log2, int* err, TcPos& pos, Stage&& stage, Store&& store) {
   TcSmem& sm = tc_smem();
@@ -178,6 +189,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
     return (b * num_kv_heads + job.kvh) * kPage;
   };
   int grp_cur = 0, grp_next = 0;
+  bool q_pending = false;  // (K warp, lane 0) this job's Q copy was issued
   if (is_producer) {  // in flight during the set-up below
     grp_cur = load_group(0);
     grp_next = load_group(1);
@@ -196,15 +208,21 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
         mbar_init(&sm.p_full[b], kSoftmaxWarps * 32);
         mbar_init(&sm.pv_done[b], 1);
       }
+      mbar_init(&sm.q_free, 1);
+      mbar_init(&sm.o_free, kSoftmaxWarps * 32);
       sm.abort = 0;
       fence_mbar_init();
       prefetch_tensormap(&maps.q);
     }
     // Q first: its copy overlaps the rest of the set-up (the previous job's
-    // closing barrier freed the buffer)
-    mbar_arrive_expect_tx(&sm.bar_q, kTileBytes);
-    tma_load_3d(sm.q, &maps.q, 0, job.kvh * kGroup, job.tok0, &sm.bar_q);
-    tma_load_3d(sm.q + kHalf, &maps.q, 64, job.kvh * kGroup, job.tok0, &sm.bar_q);
+    // closing barrier freed the buffer; with kOverlap its last S product)
+    if (first || !kOverlap || tc_wait(sm, &sm.q_free, ((uint32_t)pos.jobs - 1u) & 1u, err)) {
+      fence_after_sync();
+      mbar_arrive_expect_tx(&sm.bar_q, kTileBytes);
+      tma_load_3d(sm.q, &maps.q, 0, job.kvh * kGroup, job.tok0, &sm.bar_q);
+      tma_load_3d(sm.q + kHalf, &maps.q, 64, job.kvh * kGroup, job.tok0, &sm.bar_q);
+      q_pending = true;
+    }
   }
   if (first) {
     if (warp == kMmaWarp) tmem_alloc(&sm.tmem, kTmemCols);
@@ -249,7 +267,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
     }
     if (*reinterpret_cast<volatile int*>(&sm.abort) && lane == 0) {
       // let the copies in flight land before the CTA leaves (bounded)
-      if (is_k) mbar_wait_bounded(&sm.bar_q, q_par);
+      if (is_k && q_pending) mbar_wait_bounded(&sm.bar_q, q_par);
       for (int s = 0; s < n_st; ++s)
         if (last_issued[s] >= 0) mbar_wait_bounded(&full[s], (last_issued[s] / n_st) & 1);
     }
@@ -273,6 +291,7 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
         }
         commit(&sm.s_full[J & 1]);  // one commit per MMA group and barrier
         commit(&sm.k_empty[s]);
+        if (kOverlap && j == n_tiles - 1) commit(&sm.q_free);  // the job's last read of Q
         return true;
       };
       // S runs one tile ahead: S(j + 1) is queued before PV(j), which waits
@@ -283,6 +302,9 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
         const int J = J0 + j;
         const int s = J % kVStages;
         ok = tc_wait(sm, &sm.p_full[J & 1], (J >> 1) & 1, err) && tc_wait(sm, &sm.v_full[s], (J / kVStages) & 1, err);
+        // the first PV overwrites O: the previous job's epilogue has read it
+        if (kOverlap && ok && j == 0 && !first)
+          ok = tc_wait(sm, &sm.o_free, ((uint32_t)pos.jobs - 1u) & 1u, err);
         if (!ok) break;
         fence_after_sync();
         const uint32_t pt = tmem + kColP + (uint32_t)(J & 1) * (kKeys / 2), vb = smem_addr(sm.v[s]);
@@ -409,17 +431,27 @@ __device__ __forceinline__ void run_tile(const TcJob& job, const TcMaps& maps, i
       float o[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + kColO + 32 * c, o[c]);
-      // the K stages are free (every S and PV is done, no copy is in
-      // flight): the first two are the staging area
-      stage(r, o, m_run, l_run, sm.k[0]);
+      if constexpr (kOverlap) {
+        fence_before_sync();  // the tensor-memory reads above precede the arrive
+        mbar_arrive(&sm.o_free);
+        stage(r, o, m_run, l_run, nullptr);
+      } else {
+        // the K stages are free (every S and PV is done, no copy is in
+        // flight): the first two are the staging area
+        stage(r, o, m_run, l_run, sm.k[0]);
+      }
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
-    if (!*reinterpret_cast<volatile int*>(&sm.abort)) store(r, sm.k[0]);
+    if constexpr (!kOverlap) {
+      asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxWarps * 32) : "memory");
+      if (!*reinterpret_cast<volatile int*>(&sm.abort)) store(r, sm.k[0]);
+    }
   }
 
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
+  if constexpr (!kOverlap) {
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+  }
   pos.tiles += n_tiles;
   pos.jobs += 1;
 }
@@ -477,8 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (threadIdx.x == 0) record_error(p.err, PA_ERR_DEVICE_INDEX);
       continue;
     }
-    // staged bf16 rows: 256 B per row, 16-byte chunk c at c ^ (row & 15)
-    run_tile<true>(
+    // staged bf16 rows: 256 B per row, 16-byte chunk c at c ^ (row & 15);
+    // with several jobs per CTA each row straight from registers to out
+    run_tile<true, kPersist>(
         job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err, pos,
       [&](int row, float (&o)[4][32], float m, float l, uint8_t* stg) {
         const size_t orow = (size_t)(job.tok0 + (row >> 2)) * p.num_q_heads + job.kvh * kGroup + (row & 3);
@@ -509,9 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             y[6] = fmaf(wp, b.z, y[6]);
             y[7] = fmaf(wp, b.w, y[7]);
           }
-          *reinterpret_cast<uint4*>(stg + row * 256 + ((c8 ^ (row & 15)) << 4)) =
-              make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                         pack_bf16x2(y[6], y[7]));
+          const uint4 w = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                     pack_bf16x2(y[6], y[7]));
+          if (!kPersist)
+            *reinterpret_cast<uint4*>(stg + row * 256 + ((c8 ^ (row & 15)) << 4)) = w;
+          else if (valid)
+            *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * c8) = w;
         }
         if (p.lse && valid) p.lse[orow] = lse2 * kLn2;
       },
@@ -529,6 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       });
     if (!kPersist || *reinterpret_cast<volatile int*>(&tc_smem().abort)) break;  // (a wait gave up: recorded)
+  }
+  if (kPersist) {  // the jobs ran without a barrier between them: every warp is done before the free
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
   }
   tc_finish(pos);
 }
@@ -564,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
   float* dst_lse = direct ? p.prefix_lse : p.chunk_lse + (size_t)blockIdx.x * p.total_q * p.num_q_heads;
   // staged fp32 rows: 512 B per row, 16-byte chunk c at c ^ (row & 31)
   TcPos pos;
-  run_tile<false>(
+  run_tile<false, false>(
       job, maps, p.num_kv_heads, p.num_blocks, p.scale_log2, p.err, pos,
       [&](int row, float (&o)[4][32], float m, float l, uint8_t* stg) {
         const float inv = l > 0.f ? 1.f / l : 0.f;

@@ -219,6 +219,34 @@ def test_prefill_jobs_beside_the_decode_launch(ctas):
     assert torch.equal(outs[0][0], outs[1][0])
 
 
+@pytest.mark.parametrize("ctas", [1, 5, 37])
+def test_prefill_only_batch_on_persistent_ctas(ctas):
+    """A batch of rows with qo_len > 1 only (chunks, verify rows, a ragged
+    tail) forced onto `ctas` persistent CTAs: each runs its jobs in turn with
+    no CTA barrier between them (the next job's copies and first products
+    overlap this one's end); the same results as the oracle on two calls, no
+    device error."""
+    seq, qo = [300, 2000, 1500, 900, 1200, 64, 2048], [33, 5, 64, 5, 40, 64, 512]
+    need = sum(-(-L // 16) for L in seq)
+    b = W.make_batch(seq, qo, num_blocks=need + 7, seed=W.SEED0 + 83)
+    d = DevBatch(b)
+    B.pa_kv_append(d.k_new, d.v_new, d.slot_mapping, d.k_cache, d.v_cache)
+    ws = B.new_workspace(B.pa_attention_workspace_size(b.num_reqs, b.total_q, 32, 128, max(seq)), "cuda")
+    B.pa_set_prefill_ctas(ctas)
+    try:
+        outs = [B.pa_attention_varlen(d.q, d.k_cache, d.v_cache, d.block_tables, d.seq_lens, d.qo_indptr,
+                                      b.sm_scale, seq_lens_host=d.seq_lens_host, qo_indptr_host=d.qo_indptr_host,
+                                      workspace=ws, return_lse=True) for _ in range(2)]
+        torch.cuda.synchronize()
+    finally:
+        B.pa_set_prefill_ctas(0)
+    assert B.pa_get_device_error(ws) == 0
+    ref, ref_lse, _, _ = oracle_step(b)
+    for i, (out, lse) in enumerate(outs):
+        compare(out, ref, lse, ref_lse, what=f"prefill-only jobs on {ctas} CTAs, call {i}")
+    assert torch.equal(outs[0][0], outs[1][0])
+
+
 def test_shared_prefix_mixed_with_prefill():
     b = W.make_batch([800, 900, 700, 1000], [1, 48, 1, 1], num_blocks=300, seed=33, shared_prefix_tokens=512)
     d = DevBatch(b)
