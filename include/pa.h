@@ -439,10 +439,11 @@ pa_status pa_clear_device_error(void* workspace, pa_stream_t stream);
  *     whose batch has only rows with qo_len > 1 (bf16 pages, no shared
  *     prefix, no forced decode grid), n > 0 runs its jobs on n persistent
  *     CTAs (at most one fewer than the jobs), each running its jobs in turn
- *     with the next one's start overlapping this one's end; 0 does so on one
- *     CTA per SM when there are at least two jobs per SM, else one CTA per
- *     job; -1 always one CTA per job.  Process-wide; n outside [-1, 1024]
- *     gives PA_ERR_INVALID_ARG.
+ *     with the next one's start overlapping this one's end; 0 does so when
+ *     every such row has at most 32 queries (verify rows) and there are at
+ *     least two jobs per SM, on a grid a cost model picks (at most one CTA
+ *     per SM), else one CTA per job; -1 always one CTA per job.
+ *     Process-wide; n outside [-1, 1024] gives PA_ERR_INVALID_ARG.
  *   pa_launch_count(): kernels this library has launched in this process.
  *   pa_trace_enable(1): from now on every launch records a CUDA event before
  *     and after itself on its stream (at most 16384 launches are kept; the

@@ -289,6 +289,46 @@ int prefill_beside_ctas(const std::vector<int32_t>& job_tiles, int64_t decode_sl
   return 0;
 }
 
+// Persistent CTAs for a batch of tile jobs alone, each job one query tile
+// of a row that reads its keys once (verify rows): such a launch is bound by
+// one CTA's stream (its copy, MMA and softmax chain: ~1.44 us per 128-key
+// tile) and by HBM shared among the CTAs running (~0.013 us per tile per
+// CTA).  Over rounds of G jobs in the kernel's order, a round takes its
+// longest job's tiles x max(1.44, CTAs in the round x 0.013) us; the grid is
+// the one with the shortest sum, among the smallest grids for 1, 2, 3 ...
+// more rounds than one CTA per SM gives.  Verify batch (512 jobs of 16
+// tiles), G = 104 / 116 / 128 / 136 / 144 / 152: measured 115.3 / 121.1 /
+// 106.6 / 108.3 / 109.9 / 114.1 us, modelled 115.2 / 119.5 / 106.5 / 107.9 /
+// 112.9 / 117.9 us; the model picks 128.
+int prefill_alone_ctas(const std::vector<int32_t>& job_tiles) {
+  const int sms = sm_count();
+  const int64_t n = (int64_t)job_tiles.size();
+  if (n == 0) return 0;
+  auto cost = [&](int64_t g) {
+    double t = 0.0;
+    for (int64_t r0 = 0; r0 < n; r0 += g) {
+      const int64_t r1 = std::min(n, r0 + g);
+      int32_t longest = 0;
+      for (int64_t u = r0; u < r1; ++u) longest = std::max(longest, job_tiles[(size_t)u]);
+      t += longest * std::max(1.44, (double)(r1 - r0) * 0.013);
+    }
+    return t;
+  };
+  const int64_t k0 = (n + sms - 1) / sms;  // rounds with one CTA per SM
+  int64_t best_g = std::min<int64_t>(n, sms);
+  double best = cost(best_g);
+  for (int64_t k = k0; k <= k0 + 3; ++k) {
+    const int64_t g = (n + k - 1) / k;  // the smallest grid with k rounds
+    if (g < 1 || g > sms) continue;
+    const double c = cost(g);
+    if (c < best) {
+      best = c;
+      best_g = g;
+    }
+  }
+  return (int)best_g;
+}
+
 // Plan one persistent decode launch over decode rows rows[0..n): fills
 // plan, returns the grid size (0 when there is nothing to do, -1 when no
 // valid plan exists within the limits).  The grid is n_seg x Hkv CTAs.
@@ -615,15 +655,27 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
     } else if (P == 0 && decode_rows.empty() && forced_p >= 0 && !q8 &&
                tiles.size() <= (size_t)pa::kMaxPrefillItems && g_forced_ctas.load() <= 0 &&
                g_decode_fault.load() == 0) {
-      // a batch of tile jobs alone: with at least two jobs per SM (or when
-      // forced), persistent CTAs, one per SM, each running its jobs in turn
-      // with the next one's start overlapping this one's end (verify rows:
-      // 118.3 -> 116.3 us); fewer jobs keep one CTA each
+      // a batch of tile jobs alone: persistent CTAs, each running its jobs
+      // in turn with the next one's start overlapping this one's end, when
+      // forced, or when every row is one query tile (verify rows) and there
+      // are at least two jobs per SM, on the grid prefill_alone_ctas picks
+      // (verify: one CTA per job 118.3 us, 152 persistent CTAs 116.3, 128
+      // 110.0); chunks of longer prompts keep one CTA per job
       const int jobs = (int)tiles.size() * num_kv_heads;
-      if (forced_p > 0)
+      bool single_tiles = true;
+      for (const auto& t : tiles) single_tiles = single_tiles && item_q0[(size_t)t.second] == 0 &&
+                                               qo_indptr_host[item_req[(size_t)t.second] + 1] -
+                                                       qo_indptr_host[item_req[(size_t)t.second]] <=
+                                                   pa::kPrefillQTile;
+      if (forced_p > 0) {
         prefill_ctas = std::min(forced_p, jobs - 1);
-      else if (jobs >= 2 * sm_count())
-        prefill_ctas = sm_count();
+      } else if (single_tiles && jobs >= 2 * sm_count()) {
+        std::vector<int32_t> job_tiles;
+        job_tiles.reserve((size_t)jobs);
+        for (int h = 0; h < num_kv_heads; ++h)  // the kernel's job order
+          for (const auto& t : tiles) job_tiles.push_back((t.first + pa::kTcKeyTile - 1) / pa::kTcKeyTile);
+        prefill_ctas = std::min(prefill_alone_ctas(job_tiles), jobs - 1);
+      }
     }
     pa::PrefillParams pp;
     pp.q = static_cast<const uint16_t*>(q);
