@@ -431,15 +431,17 @@ pa_status pa_clear_device_error(void* workspace, pa_stream_t stream);
  *     pa_decode_step_workspace_size use it too (rounded up to whole kv
  *     heads, and raised where a segment would exceed 1024 pages).
  *   pa_set_prefill_ctas(n): for a call whose batch has decode rows and rows
- *     with qo_len > 1 (bf16 pages, no shared prefix, no forced decode grid):
+ *     with qo_len > 1 (bf16 pages, no shared prefix, no forced decode grid,
+ *     at most 1536 query tiles of 32 and 1024 decode rows: one launch each):
  *     n > 0 runs the tensor-core jobs of the qo_len > 1 rows on n persistent
  *     CTAs beside the decode launch (at most one fewer than the jobs and
  *     half the SMs), -1 never (the jobs first, one CTA each, then the decode
  *     launch), 0 restores the automatic choice (a cost model).  For a call
  *     whose batch has only rows with qo_len > 1 (bf16 pages, no shared
- *     prefix, no forced decode grid), n > 0 runs its jobs on n persistent
- *     CTAs (at most one fewer than the jobs), each running its jobs in turn
- *     with the next one's start overlapping this one's end; 0 does so when
+ *     prefix, no forced decode grid, at most 1536 query tiles of 32), n > 0
+ *     runs its jobs on n persistent CTAs (at most one fewer than the jobs),
+ *     each running its jobs in turn with the next one's start overlapping
+ *     this one's end; 0 does so when
  *     every such row has at most 32 queries (verify rows) and there are at
  *     least two jobs per SM, on a grid a cost model picks (at most one CTA
  *     per SM), else one CTA per job; -1 always one CTA per job.
