@@ -171,6 +171,10 @@ EDGE = {
     "decode_rows_over_one_launch": ([int(x) for x in np.random.default_rng(5).integers(1, 60, 1100)], [1] * 1100),
     # one 128K-token row: 8192 pages cut over every segment of each kv head
     "one_long_row_128k": ([131072], [1]),
+    # more query tiles than one tile launch carries (1536): two launches
+    "prefill_items_over_one_launch": ([int(x) for x in np.random.default_rng(7).integers(2, 40, 1600)], [2] * 1600),
+    # verify rows of unequal lengths, enough jobs for the persistent tile grid
+    "verify_rows_persistent_grid": ([int(x) for x in np.random.default_rng(9).integers(6, 300, 400)], [5] * 400),
 }
 
 
