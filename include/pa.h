@@ -469,6 +469,24 @@ typedef enum {
 pa_status pa_set_decode_ctas(int32_t n);
 pa_status pa_set_prefill_ctas(int32_t n);
 /*
+ * pa_plan_tile_grid(job_tiles, n_jobs, decode_slabs, sms, ctas) -- the
+ * persistent CTA count the library picks for a batch's tensor-core jobs
+ * (rows with qo_len > 1), computed on the host alone (no device is touched):
+ * job_tiles[i] is job i's number of 128-key tiles in the kernel's job order
+ * (for each kv head, the batch's 32-query tiles by decreasing key extent),
+ * sms the device's SM count.  With decode_slabs > 0 (the batch's decode rows
+ * hold that many 8 KiB (page, kv head) K+V slabs) it is the count beside the
+ * decode launch that pa_set_prefill_ctas(0) leads to (0: the jobs first, one
+ * CTA each); with decode_slabs = 0 the count for the jobs alone, which
+ * pa_attention_varlen uses when every such row has at most 32 queries (0:
+ * one CTA per job).  Ownership: job_tiles is read, *ctas written; both host
+ * memory.  Errors: PA_ERR_INVALID_ARG for a null ctas, n_jobs < 0, a null
+ * job_tiles with n_jobs > 0, a tile count below 1, sms outside [1, 1024] or
+ * decode_slabs < 0 (*ctas is then 0).
+ */
+pa_status pa_plan_tile_grid(const int32_t* job_tiles, int32_t n_jobs, int64_t decode_slabs, int32_t sms,
+                            int32_t* ctas);
+/*
  * pa_set_decode_fault_injection(on) -- a test of the bounded-wait path, off
  * (0) by default, process-wide.  With on = 1, decode launches of
  * pa_attention_varlen and pa_attention_varlen_shared_prefix over bf16 pages

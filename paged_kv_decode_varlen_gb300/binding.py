@@ -70,6 +70,7 @@ _SIGS = {
     "pa_clear_device_error": (_i32, [_P, _P]),
     "pa_set_decode_ctas": (_i32, [_i32]),
     "pa_set_prefill_ctas": (_i32, [_i32]),
+    "pa_plan_tile_grid": (_i32, [ctypes.POINTER(_i32), _i32, _i64, _i32, ctypes.POINTER(_i32)]),
     "pa_set_decode_fault_injection": (_i32, [_i32]),
     "pa_launch_count": (_i64, []),
     "pa_trace_enable": (_i32, [_i32]),
@@ -446,6 +447,18 @@ def pa_set_prefill_ctas(n: int):
     """Prefill jobs beside the decode launch: n > 0 CTAs, -1 never, 0
     automatic (see include/pa.h)."""
     _check(_lib.pa_set_prefill_ctas(int(n)))
+
+
+def pa_plan_tile_grid(job_tiles, decode_slabs: int, sms: int) -> int:
+    """The persistent CTA count the library picks for tensor-core jobs of
+    job_tiles[i] 128-key tiles (kernel order), beside decode_slabs (page, kv
+    head) slabs of decode rows (0: the jobs alone), on sms SMs; 0 = one CTA
+    per job (see include/pa.h).  Host only."""
+    n = len(job_tiles)
+    arr = (_i32 * max(n, 1))(*[int(t) for t in job_tiles])
+    out = _i32(0)
+    _check(_lib.pa_plan_tile_grid(arr if n else None, n, int(decode_slabs), int(sms), ctypes.byref(out)))
+    return out.value
 
 
 def pa_set_decode_fault_injection(on: bool):

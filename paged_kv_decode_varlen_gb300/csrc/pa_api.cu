@@ -262,8 +262,7 @@ int concurrent_prefix_chunks(int64_t key_tiles, int64_t groups, int64_t decode_s
 // plus ~12 us of start and row ends.  Of the CTA counts within 1 us of the
 // best the smallest is taken (the decode keeps the most SMs).  decode_slabs
 // counts (page, kv head) slabs of 8 KiB.
-int prefill_beside_ctas(const std::vector<int32_t>& job_tiles, int64_t decode_slabs) {
-  const int sms = sm_count();
+int prefill_beside_ctas(const std::vector<int32_t>& job_tiles, int64_t decode_slabs, int sms) {
   const int64_t n = (int64_t)job_tiles.size();
   if (n == 0 || decode_slabs == 0) return 0;
   const double decode_bytes = (double)decode_slabs * 2 * pa::kSlabBytesHost;
@@ -291,17 +290,16 @@ int prefill_beside_ctas(const std::vector<int32_t>& job_tiles, int64_t decode_sl
 
 // Persistent CTAs for a batch of tile jobs alone, each job one query tile
 // of a row that reads its keys once (verify rows): such a launch is bound by
-// one CTA's stream (its copy, MMA and softmax chain: ~1.44 us per 128-key
-// tile) and by HBM shared among the CTAs running (~0.013 us per tile per
+// one CTA's stream (its copy, MMA and softmax chain: ~1.28 us per 128-key
+// tile) and by HBM shared among the CTAs running (~0.0116 us per tile per
 // CTA).  Over rounds of G jobs in the kernel's order, a round takes its
-// longest job's tiles x max(1.44, CTAs in the round x 0.013) us; the grid is
-// the one with the shortest sum, among the smallest grids for 1, 2, 3 ...
-// more rounds than one CTA per SM gives.  Verify batch (512 jobs of 16
-// tiles), G = 104 / 116 / 128 / 136 / 144 / 152: measured 115.3 / 121.1 /
-// 106.6 / 108.3 / 109.9 / 114.1 us, modelled 115.2 / 119.5 / 106.5 / 107.9 /
-// 112.9 / 117.9 us; the model picks 128.
-int prefill_alone_ctas(const std::vector<int32_t>& job_tiles) {
-  const int sms = sm_count();
+// longest job's tiles x max(1.28, CTAs in the round x 0.0116) us; the grid
+// is the one with the shortest sum, among the smallest grids for 0 to 3 more
+// rounds than one CTA per SM gives.  Verify batch (512 jobs of 17-18 tiles),
+// G = 104 / 116 / 128 / 136 / 144 / 152: measured 115.3 / 121.1 / 106.6 /
+// 108.3 / 109.9 / 114.1 us, modelled 115.2 / 119.7 / 106.6 / 108.0 / 113.0 /
+// 118.0 us; the model picks 128.
+int prefill_alone_ctas(const std::vector<int32_t>& job_tiles, int sms) {
   const int64_t n = (int64_t)job_tiles.size();
   if (n == 0) return 0;
   auto cost = [&](int64_t g) {
@@ -310,7 +308,7 @@ int prefill_alone_ctas(const std::vector<int32_t>& job_tiles) {
       const int64_t r1 = std::min(n, r0 + g);
       int32_t longest = 0;
       for (int64_t u = r0; u < r1; ++u) longest = std::max(longest, job_tiles[(size_t)u]);
-      t += longest * std::max(1.44, (double)(r1 - r0) * 0.013);
+      t += longest * std::max(1.28, (double)(r1 - r0) * 0.0116);
     }
     return t;
   };
@@ -646,7 +644,7 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
           for (const auto& t : tiles) job_tiles.push_back((t.first + pa::kTcKeyTile - 1) / pa::kTcKeyTile);
         int64_t decode_pages = 0;
         for (int32_t r : decode_rows) decode_pages += pages_of(seq_lens_host[r]);
-        prefill_ctas = prefill_beside_ctas(job_tiles, decode_pages * num_kv_heads);
+        prefill_ctas = prefill_beside_ctas(job_tiles, decode_pages * num_kv_heads, sm_count());
       }
       if (prefill_ctas > 0) {
         concurrent = true;
@@ -674,7 +672,7 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
         job_tiles.reserve((size_t)jobs);
         for (int h = 0; h < num_kv_heads; ++h)  // the kernel's job order
           for (const auto& t : tiles) job_tiles.push_back((t.first + pa::kTcKeyTile - 1) / pa::kTcKeyTile);
-        prefill_ctas = std::min(prefill_alone_ctas(job_tiles), jobs - 1);
+        prefill_ctas = std::min(prefill_alone_ctas(job_tiles, sm_count()), jobs - 1);
       }
     }
     pa::PrefillParams pp;
@@ -1094,6 +1092,25 @@ pa_status pa_set_prefill_ctas(int32_t n) {
   if (n < -1 || n > pa::kPlanMaxCtas)
     return fail(PA_ERR_INVALID_ARG, "prefill CTAs %d outside [-1, %d]", n, pa::kPlanMaxCtas);
   g_prefill_ctas.store(n);
+  return ok();
+}
+
+pa_status pa_plan_tile_grid(const int32_t* job_tiles, int32_t n_jobs, int64_t decode_slabs, int32_t sms,
+                            int32_t* ctas) {
+  if (!ctas) return fail(PA_ERR_INVALID_ARG, "ctas is null");
+  *ctas = 0;
+  if (n_jobs < 0 || (n_jobs > 0 && !job_tiles))
+    return fail(PA_ERR_INVALID_ARG, "job_tiles must hold n_jobs = %d counts", n_jobs);
+  if (sms < 1 || sms > pa::kPlanMaxCtas) return fail(PA_ERR_INVALID_ARG, "sms %d outside [1, %d]", sms, pa::kPlanMaxCtas);
+  if (decode_slabs < 0) return fail(PA_ERR_INVALID_ARG, "decode_slabs %lld < 0", (long long)decode_slabs);
+  std::vector<int32_t> tiles(job_tiles, job_tiles + n_jobs);
+  for (int32_t i = 0; i < n_jobs; ++i)
+    if (tiles[(size_t)i] < 1) return fail(PA_ERR_INVALID_ARG, "job %d has %d key tiles (>= 1)", i, tiles[(size_t)i]);
+  if (n_jobs == 0) return ok();
+  if (decode_slabs > 0)
+    *ctas = prefill_beside_ctas(tiles, decode_slabs, sms);  // (fewer than the jobs, at most half the SMs)
+  else if (n_jobs >= 2 * sms)
+    *ctas = std::min(prefill_alone_ctas(tiles, sms), n_jobs - 1);
   return ok();
 }
 

@@ -239,3 +239,60 @@ def test_decode_step_empty_batch_launches_nothing():
     n0 = lib.pa_launch_count()
     assert _step(R=0, q=None, kn=None, vn=None, bt=None, sl=None, out=None) == b.PA_OK
     assert lib.pa_launch_count() == n0
+
+
+# ------------------------------------------------- tile-job grid (host model)
+def _tile_jobs(batch, kv_heads=8):
+    """Key tiles of each tensor-core job in the kernel's order (for each kv
+    head, the 32-query tiles by decreasing key extent) and the decode rows'
+    (page, kv head) slab count, from a batch's metadata."""
+    seq = [int(x) for x in batch.seq_lens]
+    qoi = [int(x) for x in batch.qo_indptr]
+    qo = [qoi[i + 1] - qoi[i] for i in range(len(seq))]
+    ext = sorted((L - q + min(q, j0 + 32) for L, q in zip(seq, qo) if q > 1 for j0 in range(0, q, 32)), reverse=True)
+    slabs = sum(-(-L // 16) for L, q in zip(seq, qo) if q == 1) * kv_heads
+    return [-(-e // 128) for e in ext] * kv_heads, slabs
+
+
+def test_tile_grid_model_picks_the_measured_grids():
+    from paged_kv_decode_varlen_gb300 import workloads as W
+    # mixed batch: the 512-token chunk's 128 jobs beside the decode launch on
+    # 16 CTAs (step 215.5 us; 8 / 12 / 24 CTAs measured 359 / 253 / 220 us)
+    jobs, slabs = _tile_jobs(W.workload_batch("mixed", scale=1.0))
+    assert len(jobs) == 128 and slabs > 0
+    assert b.pa_plan_tile_grid(jobs, slabs, 152) == 16
+    # verify rows: 512 jobs of 17-18 tiles alone on 128 CTAs, four full
+    # rounds (measured 106.6 us against 114.1 us on 152 and 115.3 us on 104)
+    jobs, slabs = _tile_jobs(W.workload_batch("verify", scale=1.0))
+    assert len(jobs) == 512 and slabs == 0 and set(jobs) <= {17, 18}
+    assert b.pa_plan_tile_grid(jobs, 0, 152) == 128
+
+
+def test_tile_grid_model_rounds_and_fallbacks():
+    # equal jobs alone: the smallest grid for the fewest rounds (320 jobs: 3
+    # rounds of 107, not 152 + 152 + 16)
+    assert b.pa_plan_tile_grid([16] * 320, 0, 152) == 107
+    # 1024 jobs: 7 rounds either way, every SM busy
+    assert b.pa_plan_tile_grid([16] * 1024, 0, 152) == 152
+    # fewer than two jobs per SM alone, or no jobs: one CTA per job
+    assert b.pa_plan_tile_grid([16] * 303, 0, 152) == 0
+    assert b.pa_plan_tile_grid([], 0, 152) == 0
+    # beside a decode stream: fewer CTAs than jobs, at most half the SMs
+    g = b.pa_plan_tile_grid([16] * 40, 10 ** 6, 152)
+    assert 0 <= g < 40 and g <= 76
+    # a decode stream too short to hide the jobs behind: the jobs first
+    assert b.pa_plan_tile_grid([16] * 128, 8, 152) == 0
+
+
+def test_tile_grid_model_rejects_bad_arguments():
+    arr = (ctypes.c_int32 * 2)(16, 16)
+    out = ctypes.c_int32(7)
+    assert lib.pa_plan_tile_grid(arr, 2, 0, 152, None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_tile_grid(None, 2, 0, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG and out.value == 0
+    assert lib.pa_plan_tile_grid(arr, -1, 0, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_tile_grid(arr, 2, 0, 0, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_tile_grid(arr, 2, 0, 1025, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_tile_grid(arr, 2, -1, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
+    bad = (ctypes.c_int32 * 2)(16, 0)
+    assert lib.pa_plan_tile_grid(bad, 2, 0, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_tile_grid(arr, 2, 0, 152, ctypes.byref(out)) == b.PA_OK and out.value == 0
