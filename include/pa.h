@@ -480,9 +480,10 @@ pa_status pa_set_prefill_ctas(int32_t n);
  * CTA each); with decode_slabs = 0 the count for the jobs alone, which
  * pa_attention_varlen uses when every such row has at most 32 queries (0:
  * one CTA per job).  Ownership: job_tiles is read, *ctas written; both host
- * memory.  Errors: PA_ERR_INVALID_ARG for a null ctas, n_jobs < 0, a null
- * job_tiles with n_jobs > 0, a tile count below 1, sms outside [1, 1024] or
- * decode_slabs < 0 (*ctas is then 0).
+ * memory.  Errors: PA_ERR_INVALID_ARG for a null ctas, n_jobs outside
+ * [0, 393216] (1536 query tiles x 256 kv heads), a null job_tiles with
+ * n_jobs > 0, a tile count below 1, sms outside [1, 1024] or decode_slabs < 0
+ * (*ctas is then 0).
  */
 pa_status pa_plan_tile_grid(const int32_t* job_tiles, int32_t n_jobs, int64_t decode_slabs, int32_t sms,
                             int32_t* ctas);

@@ -1099,8 +1099,9 @@ pa_status pa_plan_tile_grid(const int32_t* job_tiles, int32_t n_jobs, int64_t de
                             int32_t* ctas) {
   if (!ctas) return fail(PA_ERR_INVALID_ARG, "ctas is null");
   *ctas = 0;
-  if (n_jobs < 0 || (n_jobs > 0 && !job_tiles))
-    return fail(PA_ERR_INVALID_ARG, "job_tiles must hold n_jobs = %d counts", n_jobs);
+  if (n_jobs < 0 || n_jobs > pa::kMaxPrefillItems * 256 || (n_jobs > 0 && !job_tiles))
+    return fail(PA_ERR_INVALID_ARG, "job_tiles must hold n_jobs = %d counts (at most %d)", n_jobs,
+                pa::kMaxPrefillItems * 256);
   if (sms < 1 || sms > pa::kPlanMaxCtas) return fail(PA_ERR_INVALID_ARG, "sms %d outside [1, %d]", sms, pa::kPlanMaxCtas);
   if (decode_slabs < 0) return fail(PA_ERR_INVALID_ARG, "decode_slabs %lld < 0", (long long)decode_slabs);
   std::vector<int32_t> tiles(job_tiles, job_tiles + n_jobs);

@@ -290,6 +290,7 @@ def test_tile_grid_model_rejects_bad_arguments():
     assert lib.pa_plan_tile_grid(arr, 2, 0, 152, None) == b.PA_ERR_INVALID_ARG
     assert lib.pa_plan_tile_grid(None, 2, 0, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG and out.value == 0
     assert lib.pa_plan_tile_grid(arr, -1, 0, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_tile_grid(arr, 393217, 0, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
     assert lib.pa_plan_tile_grid(arr, 2, 0, 0, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
     assert lib.pa_plan_tile_grid(arr, 2, 0, 1025, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
     assert lib.pa_plan_tile_grid(arr, 2, -1, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
