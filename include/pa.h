@@ -41,6 +41,12 @@
  *     num_q_heads = 4 * num_kv_heads (GQA groups of 4 consecutive query
  *     heads per kv head: q head h reads kv head h / 4), num_kv_heads <= 256.
  *     Others give PA_ERR_UNSUPPORTED.
+ *   - Decode rows are planned in launches of up to 1024 rows; the rows of
+ *     one launch may hold at most 1,048,576 / num_kv_heads key pages of 16
+ *     tokens in all (131,072 pages, 2,097,152 tokens, with 8 kv heads: 1024
+ *     CTA segments of at most 1024 pages, shared by the kv heads).  Beyond
+ *     that the attention calls give PA_ERR_UNSUPPORTED; pa_plan_decode_grid
+ *     answers the same on the host alone.
  *   - Kernels never trap.  A block id or slot outside the pool found on the
  *     device is skipped (its keys are masked out / its write is dropped) and
  *     recorded in the error word at the start of the workspace; read it with
@@ -487,6 +493,22 @@ pa_status pa_set_prefill_ctas(int32_t n);
  */
 pa_status pa_plan_tile_grid(const int32_t* job_tiles, int32_t n_jobs, int64_t decode_slabs, int32_t sms,
                             int32_t* ctas);
+/*
+ * pa_plan_decode_grid(seq_lens, n_rows, num_kv_heads, sms, grid,
+ * warp_granular) -- the decode launch pa_attention_varlen plans for a batch
+ * of n_rows decode rows (qo_len 1, bf16 pages, no shared prefix, no rows with
+ * qo_len > 1) of these seq_lens on a device of sms SMs, computed on the host
+ * alone (no device is touched): *grid CTAs (0: nothing to do) of the
+ * warp-granular decode kernel (*warp_granular = 1) or of the CTA-granular one
+ * (0).  A grid forced by pa_set_decode_ctas applies here as in the call.
+ * Ownership: seq_lens is read, *grid and *warp_granular written; all host
+ * memory.  Errors: PA_ERR_INVALID_ARG for a null output, n_rows outside
+ * [0, 1024], a null seq_lens with n_rows > 0, a seq_len below 1, num_kv_heads
+ * outside [1, 256] or sms outside [1, 1024]; PA_ERR_UNSUPPORTED when no plan
+ * fits the kernels' limits, as the call would return.
+ */
+pa_status pa_plan_decode_grid(const int32_t* seq_lens, int32_t n_rows, int32_t num_kv_heads, int32_t sms,
+                              int32_t* grid, int32_t* warp_granular);
 /*
  * pa_set_decode_fault_injection(on) -- a test of the bounded-wait path, off
  * (0) by default, process-wide.  With on = 1, decode launches of

@@ -71,6 +71,8 @@ _SIGS = {
     "pa_set_decode_ctas": (_i32, [_i32]),
     "pa_set_prefill_ctas": (_i32, [_i32]),
     "pa_plan_tile_grid": (_i32, [ctypes.POINTER(_i32), _i32, _i64, _i32, ctypes.POINTER(_i32)]),
+    "pa_plan_decode_grid": (_i32, [ctypes.POINTER(_i32), _i32, _i32, _i32, ctypes.POINTER(_i32),
+                                   ctypes.POINTER(_i32)]),
     "pa_set_decode_fault_injection": (_i32, [_i32]),
     "pa_launch_count": (_i64, []),
     "pa_trace_enable": (_i32, [_i32]),
@@ -459,6 +461,17 @@ def pa_plan_tile_grid(job_tiles, decode_slabs: int, sms: int) -> int:
     out = _i32(0)
     _check(_lib.pa_plan_tile_grid(arr if n else None, n, int(decode_slabs), int(sms), ctypes.byref(out)))
     return out.value
+
+
+def pa_plan_decode_grid(seq_lens, num_kv_heads: int, sms: int):
+    """(grid, warp_granular) of the decode launch planned for decode rows
+    of these seq_lens on sms SMs (see include/pa.h).  Host only."""
+    n = len(seq_lens)
+    arr = (_i32 * max(n, 1))(*[int(x) for x in seq_lens])
+    grid, wg = _i32(0), _i32(0)
+    _check(_lib.pa_plan_decode_grid(arr if n else None, n, int(num_kv_heads), int(sms), ctypes.byref(grid),
+                                    ctypes.byref(wg)))
+    return grid.value, bool(wg.value)
 
 
 def pa_set_decode_fault_injection(on: bool):

@@ -11,6 +11,7 @@
 #include <cmath>
 #include <atomic>
 #include <mutex>
+#include <memory>
 #include <vector>
 
 #include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
@@ -398,6 +399,37 @@ int plan_decode(const int32_t* rows, int n, const int32_t* seq_lens_host, const 
   }
 }
 
+// The decode launch over rows[0..n): segments of whole pages for the
+// CTA-granular kernel; when they are long enough for four warp segments of
+// kMinWarpSegPages (or a pass runs beside the launch, or the timeout
+// diagnostic is on), planned again in whole warp segments for the
+// warp-granular kernel, one CTA per SM (a third of the CTA-granular slots and
+// grid bound, so the workspace's pieces cover its warps).  With no
+// warp-granular plan within its limits, the CTA-granular kernel (beside
+// prefill jobs too: it waits for them at its start, so they run first; beside
+// a prefix pass it cannot run, as it does not fold the pass's chunks).
+// Returns the grid (0: nothing to do, -1: no plan) and sets cta_granular.
+int choose_decode_plan(const int32_t* rows, int n, const int32_t* seq_lens_host, const int32_t* qo_indptr_host,
+                       int page_offset, int num_kv_heads, int gcap, int slots, bool concurrent, bool diag,
+                       pa::DecodePlan& plan, bool& cta_granular) {
+  auto plan_cta = [&] {
+    return plan_decode(rows, n, seq_lens_host, qo_indptr_host, page_offset, num_kv_heads, gcap, slots, 1,
+                       pa::kDecodeMaxPagesPerCta, pa::kDecodeMaxItemsPerCta, plan);
+  };
+  int grid = plan_cta();
+  cta_granular = grid > 0 && !concurrent && !diag && plan.seg < pa::kDecodeWarps * pa::kMinWarpSegPages;
+  static_assert(pa::kWgWarps <= kDecodeCtasPerSm * pa::kDecodeWarps, "warp-granular pieces fit the workspace");
+  if (grid > 0 && !cta_granular) {
+    grid = plan_decode(rows, n, seq_lens_host, qo_indptr_host, page_offset, num_kv_heads, gcap / kDecodeCtasPerSm,
+                       slots / kDecodeCtasPerSm, pa::kWgWarps, pa::kWgMaxPagesPerCta, pa::kWgMaxItemsPerCta, plan);
+    if (grid < 0 && (!concurrent || page_offset == 0) && !diag) {
+      grid = plan_cta();
+      cta_granular = grid > 0;
+    }
+  }
+  return grid;
+}
+
 // ------------------------------------------------------------- TMA maps
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -749,33 +781,10 @@ pa_status attention(const void* q, const void* k_cache, const void* v_cache, int
       // the tile kernel's tail, they made the step 1-2 us longer, not shorter.
       // Beside a concurrent prefix pass they start as soon as it has.
       const bool overlap = d0 > 0 || (P == 0 && tiles.empty()) || concurrent;
-      // segments of whole pages for the CTA-granular kernel; when they are
-      // long enough for four warp segments of kMinWarpSegPages (or a prefix
-      // pass runs beside the launch, or the timeout diagnostic is on), planned
-      // again in whole warp segments for the warp-granular kernel
       const bool diag = !q8 && g_decode_fault.load() != 0;
-      auto plan_cta = [&] {
-        return plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads, gcap,
-                           decode_slots, 1, pa::kDecodeMaxPagesPerCta, pa::kDecodeMaxItemsPerCta, plan);
-      };
-      int grid = plan_cta();
-      bool cta_granular = grid > 0 && !concurrent && !diag && plan.seg < pa::kDecodeWarps * pa::kMinWarpSegPages;
-      // the warp-granular kernel: one CTA per SM (a third of the CTA-granular
-      // slots and grid bound, so the workspace's pieces cover its warps)
-      static_assert(pa::kWgWarps <= kDecodeCtasPerSm * pa::kDecodeWarps, "warp-granular pieces fit the workspace");
-      if (grid > 0 && !cta_granular) {
-        grid = plan_decode(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads,
-                           gcap / kDecodeCtasPerSm, decode_slots / kDecodeCtasPerSm, pa::kWgWarps,
-                           pa::kWgMaxPagesPerCta, pa::kWgMaxItemsPerCta, plan);
-        // no warp-granular plan within its limits: the CTA-granular kernel
-        // (beside prefill jobs too: it waits for them at its start, so they
-        // run first; beside a prefix pass it cannot run, as it does not fold
-        // the pass's chunks)
-        if (grid < 0 && (!concurrent || P == 0) && !diag) {
-          grid = plan_cta();
-          cta_granular = grid > 0;
-        }
-      }
+      bool cta_granular = false;
+      const int grid = choose_decode_plan(decode_rows.data() + d0, n, seq_lens_host, qo_indptr_host, P, num_kv_heads,
+                                          gcap, decode_slots, concurrent, diag, plan, cta_granular);
       if (grid < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
       if (grid == 0) continue;
       s = run_launch(PA_KERNEL_DECODE, "decode", stream,
@@ -1112,6 +1121,37 @@ pa_status pa_plan_tile_grid(const int32_t* job_tiles, int32_t n_jobs, int64_t de
     *ctas = prefill_beside_ctas(tiles, decode_slabs, sms);  // (fewer than the jobs, at most half the SMs)
   else if (n_jobs >= 2 * sms)
     *ctas = std::min(prefill_alone_ctas(tiles, sms), n_jobs - 1);
+  return ok();
+}
+
+pa_status pa_plan_decode_grid(const int32_t* seq_lens, int32_t n_rows, int32_t num_kv_heads, int32_t sms,
+                              int32_t* grid, int32_t* warp_granular) {
+  if (!grid || !warp_granular) return fail(PA_ERR_INVALID_ARG, "grid and warp_granular must not be null");
+  *grid = 0;
+  *warp_granular = 0;
+  if (n_rows < 0 || n_rows > pa::kPlanMaxRows || (n_rows > 0 && !seq_lens))
+    return fail(PA_ERR_INVALID_ARG, "seq_lens must hold n_rows = %d lengths (at most %d)", n_rows, pa::kPlanMaxRows);
+  if (num_kv_heads < 1 || num_kv_heads > 256) return fail(PA_ERR_INVALID_ARG, "num_kv_heads %d outside [1, 256]", num_kv_heads);
+  if (sms < 1 || sms > pa::kPlanMaxCtas) return fail(PA_ERR_INVALID_ARG, "sms %d outside [1, %d]", sms, pa::kPlanMaxCtas);
+  int32_t max_len = 0;
+  for (int32_t r = 0; r < n_rows; ++r) {
+    if (seq_lens[r] < 1) return fail(PA_ERR_INVALID_ARG, "row %d: seq_len %d < 1", r, seq_lens[r]);
+    max_len = std::max(max_len, seq_lens[r]);
+  }
+  if (n_rows == 0) return ok();
+  std::vector<int32_t> rows((size_t)n_rows), qo_indptr((size_t)n_rows + 1);
+  for (int32_t r = 0; r <= n_rows; ++r) {
+    if (r < n_rows) rows[(size_t)r] = r;
+    qo_indptr[(size_t)r] = r;  // one query per row
+  }
+  auto plan = std::make_unique<pa::DecodePlan>();
+  bool cta_granular = false;
+  const int g = choose_decode_plan(rows.data(), n_rows, seq_lens, qo_indptr.data(), 0, num_kv_heads,
+                                   grid_cap(n_rows, num_kv_heads, max_len), sms * kDecodeCtasPerSm, false, false,
+                                   *plan, cta_granular);
+  if (g < 0) return fail(PA_ERR_UNSUPPORTED, "no decode plan within the kernel limits");
+  *grid = g;
+  *warp_granular = (g > 0 && !cta_granular) ? 1 : 0;
   return ok();
 }
 

@@ -4,6 +4,8 @@ Runs without a GPU: no call here reaches a kernel."""
 import ctypes
 import subprocess
 
+import numpy as np
+
 import pytest
 
 from paged_kv_decode_varlen_gb300 import binding as b
@@ -297,3 +299,79 @@ def test_tile_grid_model_rejects_bad_arguments():
     bad = (ctypes.c_int32 * 2)(16, 0)
     assert lib.pa_plan_tile_grid(bad, 2, 0, 152, ctypes.byref(out)) == b.PA_ERR_INVALID_ARG
     assert lib.pa_plan_tile_grid(arr, 2, 0, 152, ctypes.byref(out)) == b.PA_OK and out.value == 0
+
+
+# ------------------------------------------------------- decode plan (host)
+def test_decode_plan_picks_the_measured_kernels():
+    from paged_kv_decode_varlen_gb300 import workloads as W
+    # short dialogue: the warp-granular kernel, one 12-warp CTA per SM
+    seq = [int(x) for x in W.workload_batch("short", scale=1.0).seq_lens]
+    assert b.pa_plan_decode_grid(seq, 8, 152) == (152, True)
+    # 36-layer sweep at 2048 tokens: short segments at b = 1 and 8 keep the
+    # CTA-granular kernel (the warp-granular one measured 28.6 and 23.9 us
+    # per layer there against 10.5 and 22.2); from b = 32 the warp-granular
+    for bsz, wg in [(1, False), (8, False), (32, True), (64, True), (128, True)]:
+        grid, got = b.pa_plan_decode_grid([2048] * bsz, 8, 152)
+        assert got == wg and grid % 8 == 0, (bsz, grid, got)
+        if wg:
+            assert grid == 152
+        else:
+            assert grid <= 3 * 152
+    # a single 128K-token row: every SM, warp segments of whole pages
+    assert b.pa_plan_decode_grid([131072], 8, 152) == (152, True)
+
+
+@pytest.mark.parametrize("hkv", [1, 2, 4, 8])
+@pytest.mark.parametrize("rows", [1, 64, 1024])
+def test_decode_plan_size_limit(hkv, rows):
+    # one launch's decode rows hold at most 1,048,576 / num_kv_heads pages
+    per_row = (1048576 // hkv) // rows
+    grid, _ = b.pa_plan_decode_grid([per_row * 16] * rows, hkv, 152)
+    assert grid == 1024
+    with pytest.raises(b.PAError) as e:
+        b.pa_plan_decode_grid([(per_row + 1) * 16] * rows, hkv, 152)
+    assert e.value.status == b.PA_ERR_UNSUPPORTED
+
+
+def test_decode_plan_grids_are_whole_kv_heads():
+    rng = np.random.default_rng(11)
+    for _ in range(40):
+        n = int(rng.integers(1, 1025))
+        hkv = int(rng.choice([1, 2, 4, 8]))
+        # lengths within the size limit (at most 1,048,576 / hkv pages)
+        cap = max(1, min(20000, (1048576 // hkv) // n * 16))
+        seq = [int(x) for x in rng.integers(1, cap + 1, n)]
+        grid, wg = b.pa_plan_decode_grid(seq, hkv, 152)
+        assert 0 < grid <= 1024 and grid % hkv == 0
+        # the warp-granular kernel fills one wave of one CTA per SM before it
+        # takes more (segments capped at 3,072 pages or 192 rows)
+        pages = sum(-(-L // 16) for L in seq)
+        if wg and grid > 152:
+            assert pages > (152 // hkv) * 3072 or n > (152 // hkv) * 192 or grid // hkv > 152 // hkv
+    assert b.pa_plan_decode_grid([], 8, 152) == (0, False)
+
+
+def test_decode_plan_follows_a_forced_grid():
+    b.pa_set_decode_ctas(64)
+    try:
+        grid, _ = b.pa_plan_decode_grid([2048] * 64, 8, 152)
+    finally:
+        b.pa_set_decode_ctas(0)
+    assert grid == 64
+
+
+def test_decode_plan_rejects_bad_arguments():
+    arr = (ctypes.c_int32 * 2)(100, 200)
+    g, w = ctypes.c_int32(5), ctypes.c_int32(5)
+    ok_args = (arr, 2, 8, 152, ctypes.byref(g), ctypes.byref(w))
+    assert lib.pa_plan_decode_grid(*ok_args) == b.PA_OK and g.value > 0
+    assert lib.pa_plan_decode_grid(arr, 2, 8, 152, None, ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_decode_grid(arr, 2, 8, 152, ctypes.byref(g), None) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_decode_grid(None, 2, 8, 152, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
+    assert g.value == 0 and w.value == 0
+    assert lib.pa_plan_decode_grid(arr, 1025, 8, 152, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_decode_grid(arr, 2, 0, 152, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_decode_grid(arr, 2, 257, 152, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
+    assert lib.pa_plan_decode_grid(arr, 2, 8, 0, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
+    bad = (ctypes.c_int32 * 2)(100, 0)
+    assert lib.pa_plan_decode_grid(bad, 2, 8, 152, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
