@@ -372,6 +372,11 @@ def pin_append_then_read(o):
             continue
         for h in range(Hq):
             assert np.array_equal(o.round_bf16(out[i, h]), b.v_new[i, h // 4]), (i, h)
+    # a token whose slot is negative alone: the pool is left as it was (no
+    # other token's write could hide a stray one)
+    k_alone, v_alone = k.copy(), v.copy()
+    o.kv_append(k_new[2:3], b.v_new[2:3], np.array([-1], np.int64), k_alone, v_alone)
+    assert np.array_equal(k_alone, k) and np.array_equal(v_alone, v)
     bad = slots.copy()
     bad[0] = 12 * P
     try:

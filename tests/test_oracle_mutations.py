@@ -49,6 +49,23 @@ MUTANTS = {
     "step_padding_written": ("    if (L == 0) continue;\n    if (L < 0 ||", "    if (L < 0 ||"),
     "step_bound_ignored": ("if (L < 0 || L > max_seq_len ||", "if (L < 0 ||"),
     "f16_round_trunc": ("r = ldexp(rint(ldexp(m, 11)), e - 11);", "r = ldexp(trunc(ldexp(m, 11)), e - 11);"),
+    "q_row_of_request": ("a->q + ((size_t)tok * (size_t)a->Hq + (size_t)h)", "a->q + ((size_t)r * (size_t)a->Hq + (size_t)h)"),
+    "q_head_of_group": ("a->q + ((size_t)tok * (size_t)a->Hq + (size_t)h)",
+                        "a->q + ((size_t)tok * (size_t)a->Hq + (size_t)(kvh * G))"),
+    "table_row_stride": ("a->block_tables + (size_t)r * (size_t)a->max_blocks_per_req;",
+                         "a->block_tables + (size_t)r * (size_t)(a->max_blocks_per_req - 1);"),
+    "request_boundary": ("if (tok >= a->qo_indptr[r] && tok < a->qo_indptr[r + 1]) return r;",
+                         "if (tok >= a->qo_indptr[r] && tok <= a->qo_indptr[r + 1]) return r;"),
+    "append_src_head_stride": ("size_t src = ((size_t)i * (size_t)num_kv_heads + (size_t)h) * (size_t)head_dim",
+                               "size_t src = ((size_t)h * (size_t)n_tokens + (size_t)i) * (size_t)head_dim"),
+    "append_skip_kept": ("    if (slot < 0) continue;\n    int64_t block = slot / block_size;\n"
+                         "    int off = (int)(slot % block_size);\n    if (block >= num_blocks) return ORACLE_ERR_INDEX;\n"
+                         "    for (int h = 0; h < num_kv_heads; ++h) {\n      for (int d = 0;",
+                         "    if (slot < 0) slot = 0;\n    int64_t block = slot / block_size;\n"
+                         "    int off = (int)(slot % block_size);\n    if (block >= num_blocks) return ORACLE_ERR_INDEX;\n"
+                         "    for (int h = 0; h < num_kv_heads; ++h) {\n      for (int d = 0;"),
+    "merge_other_part_zero": ("double ta = wa > 0.0 ? wa * va : 0.0, tb = wb > 0.0 ? wb * vb : 0.0;",
+                              "double ta = wa > 0.0 ? wa * va : 0.0, tb = 0.0;"),
 }
 
 
