@@ -549,6 +549,26 @@ def pin_q8_quantization(o):
                 assert cg[i, gi, top[i, gi]] == 127 * np.sign(xv[i, gi, top[i, gi]])
     assert scales[3, 1] == 0 and not codes[3, 32:64].any()
     assert codes[5, 7] == -127 and np.count_nonzero(codes[5, :32]) == 1
+    # groups whose scale is a binary16 subnormal (max|x| / 127 near 1.1-1.5 x
+    # 2^-24): the scale rounds down by up to a third, |x| / d16 passes 127.5
+    # and the clamp acts.  Both the rounding and the clamp are odd functions,
+    # so a negated group gets the same scale and negated codes, all in
+    # [-127, 127]; the largest element's code is the clamp itself.
+    tiny = np.zeros((8, 32))
+    for gi in range(8):
+        amax = 127 * (1.1 + 0.05 * gi) * 2.0 ** -24
+        tiny[gi] = rng.uniform(-amax, amax, 32)
+        tiny[gi, gi] = -amax if gi % 2 == 0 else amax
+    xt = o.round_bf16(tiny)
+    ct, st = o.quantize_q8(xt)
+    cn, sn = o.quantize_q8(xt ^ np.uint16(0x8000))
+    assert np.array_equal(st, sn) and np.array_equal(cn.astype(np.int32), -ct.astype(np.int32))
+    assert np.all(np.abs(ct.astype(np.int32)) <= 127)
+    d16 = st.view(np.float16).astype(np.float64)
+    at = np.abs(oracle.bf16_to_f64(xt).reshape(8, 32))
+    assert np.any(at.max(axis=1) / d16 > 127.5)             # the clamp is exercised
+    for gi in range(8):
+        assert abs(int(ct.reshape(8, 32)[gi, gi])) == 127
 
 
 def _q8_values(cache, P, D):

@@ -64,6 +64,11 @@ MUTANTS = {
                          "    if (slot < 0) slot = 0;\n    int64_t block = slot / block_size;\n"
                          "    int off = (int)(slot % block_size);\n    if (block >= num_blocks) return ORACLE_ERR_INDEX;\n"
                          "    for (int h = 0; h < num_kv_heads; ++h) {\n      for (int d = 0;"),
+    "q8_clamp_128": ("c = t > 127.0f ? 127 : (t < -127.0f ? -127 : (int)t);",
+                     "c = t > 127.0f ? 127 : (t < -128.0f ? -128 : (int)t);"),
+    "q8_amax_signed": ("float v = (float)fabs(bf16_to_double(x[i]));", "float v = (float)bf16_to_double(x[i]);"),
+    "q8_scale_unrounded": ("float t = rintf((float)bf16_to_double(x[i]) / d16);",
+                           "float t = rintf((float)bf16_to_double(x[i]) / d);"),
     "merge_other_part_zero": ("double ta = wa > 0.0 ? wa * va : 0.0, tb = wb > 0.0 ? wb * vb : 0.0;",
                               "double ta = wa > 0.0 ? wa * va : 0.0, tb = 0.0;"),
 }
