@@ -69,6 +69,10 @@ MUTANTS = {
     "q8_amax_signed": ("float v = (float)fabs(bf16_to_double(x[i]));", "float v = (float)bf16_to_double(x[i]);"),
     "q8_scale_unrounded": ("float t = rintf((float)bf16_to_double(x[i]) / d16);",
                            "float t = rintf((float)bf16_to_double(x[i]) / d);"),
+    "f16_subnormal_flushed": ("if (r < ldexp(1.0, -14)) return sign | (uint16_t)ldexp(r, 24);",
+                              "if (r < ldexp(1.0, -14)) return sign;"),
+    "f16_overflow_late": ("if (r >= 65520.0 || isinf(a)) return sign | 0x7c00;",
+                          "if (r >= 131072.0 || isinf(a)) return sign | 0x7c00;"),
     "merge_other_part_zero": ("double ta = wa > 0.0 ? wa * va : 0.0, tb = wb > 0.0 ? wb * vb : 0.0;",
                               "double ta = wa > 0.0 ? wa * va : 0.0, tb = 0.0;"),
 }
