@@ -75,6 +75,8 @@ MUTANTS = {
                           "if (r >= 131072.0 || isinf(a)) return sign | 0x7c00;"),
     "round_ties_away": ("double r = ldexp(rint(ldexp(m, 8)), e - 8);", "double r = ldexp(round(ldexp(m, 8)), e - 8);"),
     "f16_ties_away": ("r = ldexp(rint(ldexp(m, 11)), e - 11);", "r = ldexp(round(ldexp(m, 11)), e - 11);"),
+    "sampled_head_swapped": ("int e = attend_one(&a, request_of(&a, sample_tok[i]), sample_tok[i], sample_head[i], s,",
+                             "int e = attend_one(&a, request_of(&a, sample_tok[i]), sample_tok[i], sample_head[i] ^ 1, s,"),
     "merge_other_part_zero": ("double ta = wa > 0.0 ? wa * va : 0.0, tb = wb > 0.0 ? wb * vb : 0.0;",
                               "double ta = wa > 0.0 ? wa * va : 0.0, tb = 0.0;"),
 }
