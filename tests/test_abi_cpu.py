@@ -375,3 +375,36 @@ def test_decode_plan_rejects_bad_arguments():
     assert lib.pa_plan_decode_grid(arr, 2, 8, 0, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
     bad = (ctypes.c_int32 * 2)(100, 0)
     assert lib.pa_plan_decode_grid(bad, 2, 8, 152, ctypes.byref(g), ctypes.byref(w)) == b.PA_ERR_INVALID_ARG
+
+
+def test_binding_signatures_match_the_header():
+    """Every prototype in include/pa.h has a ctypes signature in the binding
+    with the same number of arguments and matching C types, so no argument
+    crosses the C ABI in the wrong width."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", open(b.HEADER).read(), flags=re.S)
+    protos = dict(re.findall(r"\b(pa_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S))
+    rets = dict((n, t.strip()) for t, n in re.findall(r"^\s*([\w\s\*]+?)\s*\b(pa_\w+)\s*\(", src, flags=re.M))
+    assert set(protos) == set(b._SIGS) and len(protos) >= 26
+
+    def ctype_of(decl):
+        decl = decl.strip()
+        if "*" in decl or decl.split()[0] == "pa_stream_t":
+            return "ptr"
+        base = decl.replace("const ", "").split()[0]
+        return {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+                "float": ctypes.c_float, "pa_status": ctypes.c_int32}[base]
+
+    for name, (res, args) in b._SIGS.items():
+        params = [p for p in (x.strip() for x in protos[name].split(",")) if p and p != "void"]
+        assert len(params) == len(args), name
+        for p, a in zip(params, args):
+            want = ctype_of(p)
+            if want == "ptr":
+                assert a in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(a, "_type_") and a.__name__.startswith("LP_"), \
+                    (name, p, a)
+            else:
+                assert a is want, (name, p, a)
+        ret = rets[name]
+        want = ctypes.c_char_p if "char" in ret and "*" in ret else ctype_of(ret)
+        assert res is want, (name, ret, res)
